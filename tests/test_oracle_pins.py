@@ -1,0 +1,463 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle.
+
+Each test fixes part of the oracle with something independent of its own
+code: closed forms, invariants, special cases that reduce to a library
+routine, an exact error bound, a 50-digit brute force on a tiny input, and
+the planted-bug symptom the "Fix TileLang mHC pre on 64-wide wavefronts"
+page reports (section "The bug").
+"""
+import math
+import os
+import subprocess
+import tempfile
+from decimal import Decimal, getcontext
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import seam_inputs, bf16_bits
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+N = 4
+
+
+def _rand_case(T=3, C=64, seed=0, fold=False, alpha=(1.0, 1.0, 1.0)):
+    d = seam_inputs(T, C=C, seed=seed, fold=fold)
+    a = {
+        "x": bf16_bits(d["x"]),
+        "pre_in": d["pre_in"].numpy(),
+        "fn": d["fn"].numpy(),
+        "bias": d["bias"].numpy(),
+        "alpha": np.asarray(alpha, np.float32),
+        "norm_w": None if d["norm_w"] is None else bf16_bits(d["norm_w"]),
+    }
+    return a
+
+
+def _run(a, **kw):
+    return oracle.pre_delayed(a["x"], a["pre_in"], a["fn"], a["bias"], a["alpha"], a["norm_w"], **kw)
+
+
+# ----------------------------------------------------------------- bf16 ---
+
+def test_bf16_round_matches_torch_on_fp32_values():
+    rng = np.random.default_rng(1)
+    v = np.concatenate([
+        rng.standard_normal(20000).astype(np.float32),
+        (rng.standard_normal(2000) * 1e-39).astype(np.float32),   # fp32 subnormals
+        (rng.standard_normal(2000) * 1e37).astype(np.float32),
+        # exact ties: bf16 value + half its spacing
+        (np.arange(1, 3000, dtype=np.uint32) << 16 | 0x8000).view(np.float32),
+        np.array([0.0, -0.0, 3.3895e38, -3.3895e38, 3.4e38, np.inf, -np.inf], np.float32),
+    ])
+    ours = oracle.bf16_round(v.astype(np.float64))
+    ref = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+def test_bf16_round_is_nearest_on_doubles():
+    """Brute force: for values that are not fp32 numbers the result is the
+    nearest of the neighbouring bf16 values (ties to the even pattern)."""
+    rng = np.random.default_rng(2)
+    v = rng.standard_normal(4000) * np.exp2(rng.integers(-30, 30, 4000))
+    got = oracle.bf16_round(v)
+    base = (np.abs(v).astype(np.float32).view(np.uint32) >> 16).astype(np.int64)
+    for k in range(v.size):
+        cands = [c for c in (base[k] - 1, base[k], base[k] + 1) if 0 <= c < 0x7f80]
+        vals = [float(np.uint32(c << 16).view(np.float32)) for c in cands]
+        dist = [abs(abs(v[k]) - x) for x in vals]
+        best = min(range(len(cands)), key=lambda i: (dist[i], cands[i] & 1))
+        want = cands[best] | (0x8000 if v[k] < 0 else 0)
+        assert got[k] == want
+
+
+# ------------------------------------------------- projection and logits ---
+
+def test_logits_match_numpy_matmul():
+    """Library cross-check of steps 1-2 (RMS scale and projection, including
+    the stream-major flattening x_flat[i*C + c] = x[i][c] and the per-segment
+    alpha) against numpy's float64 matmul."""
+    a = _rand_case(T=5, C=96, alpha=(0.5, 1.5, 2.0))
+    out = _run(a)
+    x = oracle.bf16_to_f64(a["x"]).reshape(5, -1)
+    K = x.shape[1]
+    r = 1.0 / np.sqrt((x * x).sum(1) / K + oracle.RMS_EPS)
+    dot = x @ a["fn"].astype(np.float64).T
+    al = np.array([0.5] * N + [1.5] * N + [2.0] * (N * N))
+    want = r[:, None] * dot * al[None, :] + a["bias"].astype(np.float64)[None, :]
+    np.testing.assert_allclose(out["logits"], want, rtol=1e-12, atol=1e-12)
+
+
+def test_one_hot_row_closed_form():
+    """x = s * e_k: r = 1/sqrt(s^2/K + eps), l = r s fn[:, k] alpha + b."""
+    a = _rand_case(T=1, C=32)
+    K = N * 32
+    for k, s in [(0, 1.0), (37, -3.5), (K - 1, 0.125)]:
+        xv = np.zeros(K)
+        xv[k] = s
+        a["x"] = oracle.bf16_round(xv).reshape(1, N, 32)
+        out = _run(a)
+        r = 1.0 / math.sqrt(s * s / K + oracle.RMS_EPS)
+        want = r * s * a["fn"][:, k].astype(np.float64) + a["bias"]
+        np.testing.assert_allclose(out["logits"][0], want, rtol=1e-13, atol=1e-15)
+
+
+def test_zero_row_gives_bias_logits():
+    a = _rand_case(T=2, C=32)
+    a["x"][:] = 0
+    out = _run(a, nthreads=2)
+    assert np.array_equal(out["logits"], np.tile(a["bias"].astype(np.float64), (2, 1)))
+    assert np.all(out["layer_input"] == 0)
+
+
+# ------------------------------------------------------ gates, Sinkhorn ---
+
+def _logits_with_comb(comb_logits, pre=None, post=None):
+    l = np.zeros(2 * N + N * N)
+    if pre is not None:
+        l[:N] = pre
+    if post is not None:
+        l[N:2 * N] = post
+    l[2 * N:] = np.asarray(comb_logits, np.float64).reshape(-1)
+    return l
+
+
+def test_gate_closed_forms():
+    l = _logits_with_comb(np.zeros((N, N)), pre=[0, math.log(3), -math.log(3), 0],
+                          post=[0, math.log(3), -math.log(3), 40])
+    g = oracle.gates_from_logits(l)
+    np.testing.assert_allclose(g["pre"][0], [0.5, 0.75, 0.25, 0.5], rtol=1e-15)
+    np.testing.assert_allclose(g["post"][0], [1.0, 1.5, 0.5, 2.0], rtol=1e-15)
+
+
+@pytest.mark.parametrize("iters", [1, 2, 20])
+def test_additive_comb_logits_give_uniform(iters):
+    """Equal or rank-1 (a_i + b_j) comb logits give the uniform 1/n comb."""
+    rng = np.random.default_rng(3)
+    for _ in range(20):
+        a, b = rng.normal(size=N) * 5, rng.normal(size=N) * 5
+        g = oracle.gates_from_logits(_logits_with_comb(a[:, None] + b[None, :]), iters=iters)
+        np.testing.assert_allclose(g["comb"][0], np.full((N, N), 0.25), rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("eps", [1e-6, 0.1])
+def test_circulant_closed_form(eps):
+    """Circulant logits l_ij = f((j - i) mod n) are balanced after the first
+    row softmax, so comb_ij = (softmax(f)_{(j-i) mod n} + eps) / (1 + n eps)."""
+    f = np.array([0.3, -1.2, 2.0, 0.7])
+    L = np.array([[f[(j - i) % N] for j in range(N)] for i in range(N)])
+    g = oracle.gates_from_logits(_logits_with_comb(L), sinkhorn_eps=eps)
+    sm = np.exp(f - f.max()) / np.exp(f - f.max()).sum()
+    want = np.array([[(sm[(j - i) % N] + eps) / (1 + N * eps) for j in range(N)] for i in range(N)])
+    np.testing.assert_allclose(g["comb"][0], want, rtol=1e-14)
+
+
+def test_sinkhorn_invariants_on_workload_logits():
+    """Non-negative, column sums 1 (the last step normalises columns), row
+    sums 1 within 1e-3 after 20 iterations, on the synthetic workload."""
+    a = _rand_case(T=64, C=128, seed=7)
+    out = _run(a, nthreads=4)
+    comb = out["comb"]
+    assert np.all(comb >= 0)
+    np.testing.assert_allclose(comb.sum(1), 1.0, atol=1e-12)
+    np.testing.assert_allclose(comb.sum(2), 1.0, atol=1e-3)
+
+
+def test_first_iteration_orientation():
+    """With one iteration the result is the column-normalised row softmax:
+    columns sum to exactly 1 and rows do not, for an unbalanced matrix."""
+    L = np.array([[4.0, 0, 0, 0], [3.0, 1, 0, 0], [2.0, 2, 1, 0], [0.0, 0, 0, 5]])
+    g = oracle.gates_from_logits(_logits_with_comb(L), iters=1)
+    np.testing.assert_allclose(g["comb"][0].sum(0), 1.0, atol=1e-15)
+    assert np.max(np.abs(g["comb"][0].sum(1) - 1.0)) > 0.1
+
+
+def test_row_shift_invariance_and_extreme_rows():
+    """Adding a_i to row i does not change the comb (exactly, in real
+    arithmetic); rows 1600 apart in logit stay finite (per-row max)."""
+    rng = np.random.default_rng(4)
+    L = rng.normal(size=(N, N)) * 3
+    base = oracle.gates_from_logits(_logits_with_comb(L))["comb"][0]
+    shifted = oracle.gates_from_logits(_logits_with_comb(L + np.array([[800.0], [-800.0], [3.0], [0.0]])))["comb"][0]
+    np.testing.assert_allclose(shifted, base, rtol=1e-13)
+    assert np.all(np.isfinite(shifted))
+
+
+def test_sinkhorn_converges_to_doubly_stochastic():
+    rng = np.random.default_rng(5)
+    L = rng.normal(size=(N, N)) * 2
+    g = oracle.gates_from_logits(_logits_with_comb(L), iters=10000)
+    np.testing.assert_allclose(g["comb"][0].sum(0), 1.0, atol=1e-14)
+    np.testing.assert_allclose(g["comb"][0].sum(1), 1.0, atol=1e-13)
+    g20 = oracle.gates_from_logits(_logits_with_comb(L), iters=20)
+    np.testing.assert_allclose(g20["comb"][0], g["comb"][0], atol=1e-3)
+
+
+def test_stream_permutation_equivariance():
+    """Permuting the streams (x, pre_in, fn's K blocks and gate rows, bias)
+    permutes pre/post/comb and leaves layer_input unchanged."""
+    C = 48
+    a = _rand_case(T=4, C=C, seed=11, fold=True, alpha=(0.7, 1.3, 0.9))
+    perm = np.array([2, 0, 3, 1])
+    b = dict(a)
+    b["x"] = a["x"][:, perm, :].copy()
+    b["pre_in"] = a["pre_in"][:, perm].copy()
+    fn = a["fn"].reshape(-1, N, C)[:, perm, :].reshape(-1, N * C)
+    rows = list(perm) + [N + j for j in perm] + [2 * N + N * i + j for i in perm for j in perm]
+    b["fn"] = fn[rows].copy()
+    b["bias"] = a["bias"][rows].copy()
+    oa, ob = _run(a), _run(b)
+    np.testing.assert_allclose(ob["pre"], oa["pre"][:, perm], rtol=1e-13)
+    np.testing.assert_allclose(ob["post"], oa["post"][:, perm], rtol=1e-13)
+    np.testing.assert_allclose(ob["comb"], oa["comb"][:, perm][:, :, perm], rtol=1e-12)
+    li_a = oracle.bf16_to_f64(oa["layer_input"])
+    li_b = oracle.bf16_to_f64(ob["layer_input"])
+    np.testing.assert_allclose(li_b, li_a, rtol=2 ** -7, atol=1e-30)
+
+
+# -------------------------------------------------------------- collapse ---
+
+def test_collapse_one_hot_premix_is_exact_stream():
+    a = _rand_case(T=3, C=64, seed=12)
+    for i in range(N):
+        a["pre_in"][:] = 0.0
+        a["pre_in"][:, i] = 1.0
+        out = _run(a)
+        assert np.array_equal(out["layer_input"], a["x"][:, i, :])
+
+
+def test_collapse_error_bound():
+    """The fp32 collapse (4 rounded products, 3 rounded adds) is within
+    4 u sum_i |p_i x_i| (u = 2^-24) of the exact value."""
+    a = _rand_case(T=8, C=256, seed=13)
+    out = _run(a)
+    x = oracle.bf16_to_f64(a["x"])
+    p = a["pre_in"].astype(np.float64)
+    exact = (p[:, :, None] * x).sum(1)
+    bound = 4 * 2.0 ** -24 * (np.abs(p[:, :, None] * x)).sum(1)
+    err = np.abs(out["h32"].astype(np.float64) - exact)
+    assert np.all(err <= bound + 1e-45)
+    li = oracle.bf16_to_f64(out["layer_input"])
+    assert np.array_equal(out["layer_input"], oracle.bf16_round(out["h32"].astype(np.float64)))
+    np.testing.assert_allclose(li, exact, rtol=2 ** -8 + 1e-6, atol=1e-30)
+
+
+# ------------------------------------------------------------------ fold ---
+
+def test_fold_unit_weight_is_textbook_rmsnorm():
+    a = _rand_case(T=6, C=512, seed=14, fold=True)
+    a["norm_w"] = oracle.bf16_round(np.ones(512))
+    out = _run(a)
+    h = torch.from_numpy(out["h32"].astype(np.float64))
+    ref = torch.nn.functional.rms_norm(h, (512,), eps=oracle.NORM_EPS)
+    ref_bits = oracle.bf16_round(ref.numpy())
+    assert np.array_equal(out["layer_input"], ref_bits)
+
+
+def _fold_ratio(out, norm_w_bits):
+    li = oracle.bf16_to_f64(out["layer_input"])
+    w = oracle.bf16_to_f64(norm_w_bits)
+    h = out["h32"].astype(np.float64)
+    ms = (h * h).mean(1)
+    rms_unit = np.sqrt(((li / w) ** 2).mean(1))
+    return rms_unit / np.sqrt(ms / (ms + oracle.NORM_EPS))
+
+
+def test_fold_norm_check():
+    """RMS_c(layer_input / w) = sqrt(ms/(ms+eps)) up to bf16 rounding; the
+    w-weighted form: RMS(layer_input) ~ mean(w^2)^(1/2)."""
+    a = _rand_case(T=16, C=1024, seed=15, fold=True)
+    out = _run(a)
+    ratio = _fold_ratio(out, a["norm_w"])
+    np.testing.assert_allclose(ratio, 1.0, atol=2e-3)
+    li = oracle.bf16_to_f64(out["layer_input"])
+    w = oracle.bf16_to_f64(a["norm_w"])
+    rms = np.sqrt((li ** 2).mean(1))
+    np.testing.assert_allclose(rms, np.sqrt((w ** 2).mean()), rtol=0.05)
+
+
+def _planted_oracle(tmpdir):
+    """Build a copy of the oracle with the half-reduction bug planted: the
+    fold's sum of squares covers only half of it."""
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "mhc_oracle.c")).read()
+    needle = "        ms /= (double)C;\n"
+    assert src.count(needle) == 1
+    src = src.replace(needle, "        ms /= (double)C;\n        ms *= 0.5;\n")
+    path = os.path.join(tmpdir, "planted.c")
+    with open(path, "w") as f:
+        f.write(src)
+    so = os.path.join(tmpdir, "libplanted.so")
+    subprocess.run(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fPIC", "-shared",
+                    "-pthread", "-o", so, path, "-lm"], check=True)
+    return so
+
+
+def test_norm_check_catches_half_reduction_bug():
+    """Plant the defect the page describes (sum of squares over half the
+    lanes) in a copy of the oracle: the norm check must report the page's
+    ratio (golden/sqrt2_fold_bug.txt), constant over token counts."""
+    golden = {}
+    with open(os.path.join(os.path.dirname(__file__), "golden", "sqrt2_fold_bug.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                k, v = line.split("=")
+                golden[k.strip()] = v.strip()
+    page_ratio = float(golden["measured_ratio"])
+    token_counts = [int(t) for t in golden["token_counts"].split(",")]
+    import ctypes
+    with tempfile.TemporaryDirectory() as td:
+        lib = ctypes.CDLL(_planted_oracle(td))
+        saved = oracle._lib
+        try:
+            lib.mhc_oracle_pre_delayed.argtypes = saved.mhc_oracle_pre_delayed.argtypes
+            lib.mhc_oracle_pre_delayed.restype = ctypes.c_int
+            oracle._lib = lib
+            for T in token_counts[:3]:
+                a = _rand_case(T=T, C=256, seed=16, fold=True)
+                out = _run(a, nthreads=4)
+                ratio = _fold_ratio(out, a["norm_w"])
+                np.testing.assert_allclose(ratio, page_ratio, rtol=1e-3)
+        finally:
+            oracle._lib = saved
+    # and the unplanted oracle passes the same check
+    a = _rand_case(T=8, C=256, seed=16, fold=True)
+    np.testing.assert_allclose(_fold_ratio(_run(a), a["norm_w"]), 1.0, atol=2e-3)
+
+
+# ------------------------------------------------------------------ post ---
+
+def test_post_identity_and_residual_add():
+    rng = np.random.default_rng(17)
+    T, C = 5, 64
+    x = oracle.bf16_round(rng.standard_normal((T, N, C)))
+    y = oracle.bf16_round(rng.standard_normal((T, C)))
+    eye = np.tile(np.eye(N, dtype=np.float32), (T, 1, 1))
+    xn, _ = oracle.post(x, y, eye, np.zeros((T, N), np.float32))
+    assert np.array_equal(xn, x)
+    xn, _ = oracle.post(x, y, eye, np.ones((T, N), np.float32))
+    xs = torch.from_numpy(oracle.bf16_to_f64(x).astype(np.float32))
+    ys = torch.from_numpy(oracle.bf16_to_f64(y).astype(np.float32))
+    want = (xs + ys[:, None, :]).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(xn, want)
+
+
+def test_post_orientation_permutation():
+    """comb[i][j] routes source stream i to destination j: a permutation
+    matrix P (P[i][pi(i)] = 1) gives x_new[pi(i)] = x[i]."""
+    rng = np.random.default_rng(18)
+    T, C = 2, 32
+    x = oracle.bf16_round(rng.standard_normal((T, N, C)))
+    y = oracle.bf16_round(rng.standard_normal((T, C)))
+    pi = [1, 3, 0, 2]
+    P = np.zeros((N, N), np.float32)
+    for i in range(N):
+        P[i, pi[i]] = 1.0
+    xn, _ = oracle.post(x, y, np.tile(P, (T, 1, 1)), np.zeros((T, N), np.float32))
+    for i in range(N):
+        assert np.array_equal(xn[:, pi[i]], x[:, i])
+
+
+def test_post_conservation():
+    """With a doubly-stochastic comb, sum_j x_new[j] = sum_i x[i] + (sum_j post_j) y."""
+    rng = np.random.default_rng(19)
+    T, C = 3, 40
+    x = oracle.bf16_round(rng.standard_normal((T, N, C)))
+    y = oracle.bf16_round(rng.standard_normal((T, C)))
+    comb = np.full((T, N, N), 0.25, np.float32)
+    post = rng.uniform(0, 2, (T, N)).astype(np.float32)
+    _, x64 = oracle.post(x, y, comb, post)
+    xv, yv = oracle.bf16_to_f64(x), oracle.bf16_to_f64(y)
+    want = xv.sum(1) + post.astype(np.float64).sum(1)[:, None] * yv
+    np.testing.assert_allclose(x64.sum(1), want, rtol=1e-12, atol=1e-12)
+
+
+# ----------------------------------------------- 50-digit brute force ---
+
+def _dec_bf16_bits(v: Decimal) -> int:
+    """Nearest bf16 (ties to even) of a Decimal, by brute force over the
+    neighbouring patterns."""
+    if v == 0:
+        return 0
+    sign = 0x8000 if v < 0 else 0
+    av = abs(v)
+    base = int(np.array([float(av)], np.float32).view(np.uint32)[0] >> 16)
+    best = None
+    for c in (base - 1, base, base + 1):
+        if c < 0:
+            continue
+        val = Decimal(float(np.array([c << 16], np.uint32).view(np.float32)[0]))
+        key = (abs(av - val), c & 1)
+        if best is None or key < best[0]:
+            best = (key, c)
+    return sign | best[1]
+
+
+def test_brute_force_50_digits_T1_C8():
+    """T=1, C=8 (K=32, 24 logits) in 50-digit decimal arithmetic, sharing no
+    code with the C oracle: RMS scale, projection, gates, 20-iteration
+    Sinkhorn, fp32 collapse, fold rounded once."""
+    getcontext().prec = 50
+    C = 8
+    a = _rand_case(T=1, C=C, seed=21, fold=True, alpha=(0.8, 1.25, 1.5))
+    a["fn"] = (a["fn"] * 25).astype(np.float32)      # logits of order 1
+    out = _run(a)
+    D = Decimal
+    x = [D(float(v)) for v in oracle.bf16_to_f64(a["x"]).reshape(-1)]
+    K = len(x)
+    eps = D(oracle.RMS_EPS)
+    ss = sum(v * v for v in x)
+    r = 1 / (ss / K + eps).sqrt()
+    M = 2 * N + N * N
+    al = [D(float(a["alpha"][0]))] * N + [D(float(a["alpha"][1]))] * N + [D(float(a["alpha"][2]))] * (N * N)
+    l = []
+    for m in range(M):
+        dot = sum(x[k] * D(float(a["fn"][m, k])) for k in range(K))
+        l.append(r * dot * al[m] + D(float(a["bias"][m])))
+    sig = lambda z: 1 / (1 + (-z).exp())
+    pre = [sig(l[i]) for i in range(N)]
+    post = [2 * sig(l[N + i]) for i in range(N)]
+    E = D(oracle.SINKHORN_EPS)
+    P = [[None] * N for _ in range(N)]
+    for i in range(N):
+        row = l[2 * N + N * i: 2 * N + N * i + N]
+        mx = max(row)
+        e = [(v - mx).exp() for v in row]
+        s = sum(e)
+        for j in range(N):
+            P[i][j] = e[j] / s + E
+    for it in range(oracle.SINKHORN_ITERS):
+        if it:
+            for i in range(N):
+                s = sum(P[i])
+                P[i] = [v / s for v in P[i]]
+        for j in range(N):
+            s = sum(P[i][j] for i in range(N))
+            for i in range(N):
+                P[i][j] = P[i][j] / s
+    np.testing.assert_allclose(out["logits"][0], [float(v) for v in l], rtol=1e-13)
+    np.testing.assert_allclose(out["pre"][0], [float(v) for v in pre], rtol=1e-14)
+    np.testing.assert_allclose(out["post"][0], [float(v) for v in post], rtol=1e-14)
+    np.testing.assert_allclose(out["comb"][0], [[float(v) for v in row] for row in P], rtol=1e-13)
+    # collapse in fp32, stream order, each operation rounded (numpy float32)
+    xs = oracle.bf16_to_f64(a["x"]).astype(np.float32)[0]
+    p = a["pre_in"][0]
+    h = p[0] * xs[0]
+    for i in range(1, N):
+        h = (h + p[i] * xs[i]).astype(np.float32)
+    assert np.array_equal(out["h32"][0], h)
+    hd = [D(float(v)) for v in h]
+    ms = sum(v * v for v in hd) / C
+    s = 1 / (ms + D(oracle.NORM_EPS)).sqrt()
+    w = [D(float(v)) for v in oracle.bf16_to_f64(a["norm_w"])]
+    want = [_dec_bf16_bits(hd[c] * s * w[c]) for c in range(C)]
+    assert [int(b) for b in out["layer_input"][0]] == want
+
+
+def test_threads_do_not_change_results():
+    a = _rand_case(T=9, C=64, seed=22, fold=True)
+    o1, o4 = _run(a, nthreads=1), _run(a, nthreads=4)
+    for k in o1:
+        assert np.array_equal(o1[k], o4[k]), k
