@@ -1,0 +1,483 @@
+"""Benchmark of the GB300 mHC seam (delayed pre + post).
+
+Headline workload: the prefill seam, T = 16384 tokens, n = 4 streams,
+C = 5120, 20 Sinkhorn iterations, fused RMSNorm fold on; one step = one
+mhc_pre_delayed + one mhc_post over the batch (every step of the seam).
+`value` = tokens/s (whole job, all ranks).  Inputs (x 671 MB) are larger than
+L2 (129 MB), so no explicit flush is needed between steps.  Secondary keys
+carry the decode sweep (graph-captured mhc_pre_delayed, T = 1..128, median of
+5 x 200 replays), the 80-seam decode chain (one graph) and per-kernel HBM
+roofline figures.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--skip-decode] [--skip-cpu]
+
+`--impl reference` times the CPU oracle (this seam has no other reference
+implementation) on the same workload and metric, on a bounded token sample
+per step.  Multi-GPU (torchrun): independent replicas, one batch per rank,
+no collective on the data path (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "mHC seam µs/call T=1–128 (graph); tokens/s + HBM GB/s vs peak at T=16384"
+T_PREFILL, N_STREAMS, HIDDEN, ITERS = 16384, 4, 5120, 20
+DECODE_T = (1, 2, 4, 8, 16, 32, 64, 128)
+CHAIN_SEAMS, CHAIN_T = 80, 4
+
+# algorithmic bytes (what the method must move; fn counted once per call)
+PRE_BYTES_PER_TOKEN = 40960 + 10240 + 16 + 16 + 16 + 64   # x, layer_input, pre_in, pre, post, comb
+PRE_BYTES_FIXED = 24 * 20480 * 4 + 24 * 4 + 12 + 5120 * 2  # fn, bias, alpha, norm_weight
+POST_BYTES_PER_TOKEN = 40960 + 10240 + 64 + 16 + 40960     # x, y, comb, post, x_new
+PRE_FLOP_PER_TOKEN = 2 * 24 * 20480
+
+
+def pre_bytes(T):
+    return T * PRE_BYTES_PER_TOKEN + PRE_BYTES_FIXED
+
+
+def post_bytes(T):
+    return T * POST_BYTES_PER_TOKEN
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mhc_hyper_connection_pre_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or
+    None when the kernels changed since that capture."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("source_hash") != kernel_source_hash():
+        return None
+    k = d.get("kernels", {}).get(kernel)
+    return None if k is None else k.get("dram_bytes_per_launch_full_size")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines = []
+        sel = ["-i", str(device_index)]
+        try:
+            import torch
+            props = torch.cuda.get_device_properties(device_index)
+            bus_id = "{:08x}:{:02x}:{:02x}.0".format(props.pci_domain_id, props.pci_bus_id,
+                                                    props.pci_device_id)
+            probe = subprocess.run(["nvidia-smi", "-i", bus_id, "--query-gpu=clocks.max.sm",
+                                    "--format=csv,noheader"], capture_output=True, text=True,
+                                   timeout=20)
+            if probe.returncode == 0 and probe.stdout.strip():
+                sel = ["-i", bus_id]
+        except Exception:
+            pass
+        self.cmd = ["nvidia-smi", *sel, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                    "-lms", "100"]
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for name, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_info():
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for l in f:
+                if l.lower().startswith(("model name", "cpu part", "hardware")):
+                    model = l.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return os.cpu_count() or 1, model
+
+
+def time_oracle_sample(d, tokens: int, nthreads: int):
+    """Oracle pre + post on the first `tokens` rows of the workload; seconds."""
+    import numpy as np
+    import oracle
+    from workloads import bf16_bits
+    x = bf16_bits(d["x"][:tokens])
+    y = bf16_bits(d["y"][:tokens])
+    pre_in = d["pre_in"][:tokens].cpu().numpy()
+    fn, bias, alpha = d["fn"].cpu().numpy(), d["bias"].cpu().numpy(), d["alpha"].cpu().numpy()
+    nw = bf16_bits(d["norm_w"])
+    t0 = time.perf_counter()
+    o = oracle.pre_delayed(x, pre_in, fn, bias, alpha, nw, nthreads=nthreads)
+    oracle.post(x, y, o["comb"].astype(np.float32), o["post"].astype(np.float32), nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+# ------------------------------------------------------------ our arm ---
+
+def run_ours(args, rank, world, local):
+    import torch
+    import mhc_hyper_connection_pre_gb300 as mhc
+    from mhc_hyper_connection_pre_gb300.graphs import SeamGraph
+    from workloads import seam_inputs, chain_seam_params, chain_stub_delta
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    hbm_peak, peak_kind = load_peaks()
+    T = T_PREFILL
+    d = seam_inputs(T, seed=rank, fold=True, with_y=True, device=f"cuda:{local}")
+    x, y = d["x"], d["y"]
+    pre_in = [d["pre_in"], torch.empty_like(d["pre_in"])]
+    outs = [{"pre": torch.empty(T, 4, device=dev), "post": torch.empty(T, 4, device=dev),
+             "comb": torch.empty(T, 4, 4, device=dev),
+             "layer_input": torch.empty(T, HIDDEN, dtype=torch.bfloat16, device=dev)} for _ in range(2)]
+    x_new = torch.empty_like(x)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i, ev=None):
+        o = outs[i & 1]
+        o["pre"] = pre_in[(i + 1) & 1]          # this seam's pre-mix feeds the next step
+        if ev is not None:
+            ev[0].record(stream)
+        mhc.pre_delayed(x, pre_in[i & 1], d["fn"], d["bias"], d["alpha"], d["norm_w"], out=o)
+        if ev is not None:
+            ev[1].record(stream)
+        mhc.post(x, y, o["comb"], o["post"], out=x_new)
+        if ev is not None:
+            ev[2].record(stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for i in range(args.warmup):
+        step(i)
+    barrier()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        barrier()
+        t_begin = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_begin.record(stream)
+        for i in range(args.steps):
+            step(i, evs[i])
+        t_end.record(stream)
+        barrier()
+    elapsed_ms = t_begin.elapsed_time(t_end)
+    pre_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    post_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    ms_per_step = elapsed_ms / args.steps
+    tokens_per_s = world * T * args.steps / (elapsed_ms / 1e3)
+
+    pre_avg = sum(pre_ms) / len(pre_ms)
+    post_avg = sum(post_ms) / len(post_ms)
+    kernels = {
+        "mhc_pre_delayed": {"us": pre_avg * 1e3, "bytes": pre_bytes(T),
+                            "gbs": pre_bytes(T) / (pre_avg / 1e3) / 1e9},
+        "mhc_post": {"us": post_avg * 1e3, "bytes": post_bytes(T),
+                     "gbs": post_bytes(T) / (post_avg / 1e3) / 1e9},
+    }
+    for k in kernels.values():
+        k["frac_of_hbm_peak"] = k["gbs"] / hbm_peak
+    dom = max(kernels, key=lambda k: kernels[k]["us"])
+    roof = {"bound": "hbm", "kernel": dom, "achieved": round(kernels[dom]["gbs"], 1),
+            "peak": hbm_peak, "unit": "GB/s", "frac": round(kernels[dom]["gbs"] / hbm_peak, 4),
+            "traffic": ncu_traffic(dom), "peak_kind": f"{peak_kind} (STREAM-style copy)"}
+    seam_frac = (pre_bytes(T) + post_bytes(T)) / hbm_peak / 1e9 / (ms_per_step / 1e3)
+
+    # ---- end to end through the public API: pinned host in, pinned host out
+    e2e = None
+    if rank == 0 or world > 1:
+        hx = torch.empty(x.shape, dtype=x.dtype, pin_memory=True).copy_(x)
+        hy = torch.empty(y.shape, dtype=y.dtype, pin_memory=True).copy_(y)
+        hp = torch.empty(pre_in[0].shape, pin_memory=True).copy_(pre_in[0])
+        ho = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+        hpo = torch.empty(pre_in[0].shape, pin_memory=True)
+        ek = max(3, min(20, args.steps))
+        dx, dy, dp = torch.empty_like(x), torch.empty_like(y), torch.empty_like(pre_in[0])
+
+        def e2e_step():
+            dx.copy_(hx, non_blocking=True)
+            dy.copy_(hy, non_blocking=True)
+            dp.copy_(hp, non_blocking=True)
+            o = mhc.pre_delayed(dx, dp, d["fn"], d["bias"], d["alpha"], d["norm_w"], out=outs[0])
+            mhc.post(dx, dy, o["comb"], o["post"], out=x_new)
+            ho.copy_(x_new, non_blocking=True)
+            hpo.copy_(o["pre"], non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(ek):
+            e2e_step()
+        b.record(stream)
+        barrier()
+        e_ms = a.elapsed_time(b)
+        if world > 1:
+            import torch.distributed as dist
+            tt = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e_ms = float(tt.item())
+        h2d = x.numel() * 2 + y.numel() * 2 + pre_in[0].numel() * 4
+        d2h = x_new.numel() * 2 + pre_in[0].numel() * 4
+        e2e = {"value": round(world * T * ek / (e_ms / 1e3), 1), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e_ms / ek, 4)}
+        del hx, hy, hp, ho, hpo, dx, dy, dp
+
+    # ---- decode sweep and the 80-seam chain (rank 0 only)
+    decode = chain = None
+    if rank == 0 and not args.skip_decode:
+        decode = {}
+        s = torch.cuda.Stream(dev)
+        for Td in DECODE_T:
+            dd = seam_inputs(Td, seed=Td, fold=True, with_y=True, device=f"cuda:{local}")
+            o = mhc.pre_delayed(dd["x"], dd["pre_in"], dd["fn"], dd["bias"], dd["alpha"], dd["norm_w"])
+            xn = torch.empty_like(dd["x"])
+            torch.cuda.synchronize()
+            res = {}
+            for name, fn_ in (
+                ("pre", lambda st: mhc.pre_delayed(dd["x"], dd["pre_in"], dd["fn"], dd["bias"],
+                                                   dd["alpha"], dd["norm_w"], out=o, stream=st)),
+                ("seam", lambda st: (mhc.pre_delayed(dd["x"], dd["pre_in"], dd["fn"], dd["bias"],
+                                                     dd["alpha"], dd["norm_w"], out=o, stream=st),
+                                     mhc.post(dd["x"], dd["y"], o["comb"], o["post"], out=xn, stream=st)))):
+                g = SeamGraph(fn_, s)
+                g.replay(20)
+                meds = []
+                for _ in range(5):
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(s)
+                    g.replay(200)
+                    b.record(s)
+                    s.synchronize()
+                    meds.append(a.elapsed_time(b) * 1e3 / 200)
+                res[name + "_us"] = round(statistics.median(meds), 3)
+                res[name + "_launches"] = g.kernel_nodes
+                g.close()
+            decode[str(Td)] = res
+        # 80 seams, each with its own weights, pre-mix carried seam to seam
+        params = [chain_seam_params(si, device=f"cuda:{local}") for si in range(CHAIN_SEAMS)]
+        deltas = [chain_stub_delta(si, device=f"cuda:{local}") for si in range(CHAIN_SEAMS)]
+        c0 = seam_inputs(CHAIN_T, seed=0, device=f"cuda:{local}")
+        cx = c0["x"].clone()
+        cp = [c0["pre_in"].clone(), torch.empty_like(c0["pre_in"])]
+        co = {"post": torch.empty(CHAIN_T, 4, device=dev), "comb": torch.empty(CHAIN_T, 4, 4, device=dev),
+              "layer_input": torch.empty(CHAIN_T, HIDDEN, dtype=torch.bfloat16, device=dev)}
+        cy = torch.empty(CHAIN_T, HIDDEN, dtype=torch.bfloat16, device=dev)
+
+        def chain_step(st):
+            for si in range(CHAIN_SEAMS):
+                p = params[si]
+                o = dict(co, pre=cp[(si + 1) & 1])
+                mhc.pre_delayed(cx, cp[si & 1], p["fn"], p["bias"], p["alpha"], p["norm_w"], out=o, stream=st)
+                with torch.cuda.stream(st):
+                    torch.add(co["layer_input"], deltas[si], out=cy)   # synthetic sublayer
+                mhc.post(cx, cy, co["comb"], co["post"], out=cx, stream=st)
+
+        with torch.cuda.stream(s):
+            chain_step(s)
+        s.synchronize()
+        g = SeamGraph(chain_step, s)
+        g.replay(3)
+        meds = []
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            g.replay(200)
+            b.record(s)
+            s.synchronize()
+            meds.append(a.elapsed_time(b) * 1e3 / 200)
+        chain = {"us_per_step": round(statistics.median(meds), 2), "seams": CHAIN_SEAMS, "T": CHAIN_T,
+                 "kernel_nodes": g.kernel_nodes,
+                 "launches_per_seam": (g.kernel_nodes - CHAIN_SEAMS) / CHAIN_SEAMS,
+                 "l2": "fn of 80 seams = 157 MB > L2"}
+        g.close()
+
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        cores, model = cpu_info()
+        probe = 64
+        dt = time_oracle_sample(d, probe, cores)
+        tokens = int(max(probe, min(T, probe * 12.0 / max(dt, 1e-6))))
+        dt = time_oracle_sample(d, tokens, cores)
+        cpu = {"value": round(tokens / dt, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"first {tokens} of the {T} tokens, pre + post, fp64 oracle, {cores} threads"
+                         + (f" ({model})" if model else "")}
+
+    line = {
+        "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16/fp32",
+        "data": "synthetic (seeded N(0,1) streams, N(0,0.02^2) fn; no checkpoint)",
+        "config": {"workload": "prefill seam: mhc_pre_delayed (fold) + mhc_post, T=16384, n=4, C=5120, "
+                               "20 Sinkhorn iters", "T": T, "n": N_STREAMS, "C": HIDDEN,
+                   "sinkhorn_iters": ITERS, "fold": True, "per_rank_tokens": T,
+                   "l2": "inputs larger than L2 (x 671 MB vs 129 MB), no flush",
+                   "parallelism": f"replicas x{world}"},
+        "seam_hbm_frac": round(seam_frac, 4),
+        "kernels": {k: {kk: round(vv, 3) if isinstance(vv, float) else vv for kk, vv in v.items()}
+                    for k, v in kernels.items()},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+        "decode_graph": decode,
+        "decode_chain_80": chain,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------ reference arm ---
+
+def run_reference(args, rank, world, local):
+    if rank != 0:
+        return
+    import torch
+    from workloads import seam_inputs
+    T = T_PREFILL
+    d = seam_inputs(T, seed=0, fold=True, with_y=True, device="cpu")
+    cores, model = cpu_info()
+    probe = 16
+    dt = time_oracle_sample(d, probe, cores)
+    per_token = dt / probe
+    budget = 150.0
+    steps_total = args.steps + args.warmup
+    tokens = int(max(1, min(T, budget / max(1, steps_total) / per_token)))
+    for _ in range(args.warmup):
+        time_oracle_sample(d, tokens, cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        time_oracle_sample(d, tokens, cores)
+    el = time.perf_counter() - t0
+    value = tokens * args.steps / el
+    sample = (f"first {tokens} of the {T} tokens per step, pre + post, fp64 oracle, {cores} threads"
+              + (f" ({model})" if model else ""))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "prefill seam: mhc_pre_delayed (fold) + mhc_post, T=16384, n=4, C=5120, "
+                               "20 Sinkhorn iters", "T": T, "n": N_STREAMS, "C": HIDDEN,
+                   "sinkhorn_iters": ITERS, "fold": True},
+        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    _ = torch
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--skip-decode", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world, local)
+    else:
+        run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

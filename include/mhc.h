@@ -1,0 +1,124 @@
+/*
+ * mhc.h -- C ABI of the GB300 (sm_103a) mHC seam library, libmhc.so.
+ *
+ * The manifold-constrained hyper-connection (mHC) seam of DeepSeek-V4.1-style
+ * decoders, as described on the vLLM pull-request pages
+ *   [A] "[ROCm][DSV4.1][Perf] Use AITER mHC for the delayed pre block" (#56503)
+ *   [B] "[ROCm][DSv4.1] Fix TileLang mHC pre on 64-wide wavefronts and use the
+ *        fused kernels on the AMD path" (#56342)
+ * Every pointer argument is a caller-owned DEVICE pointer (CUDA global
+ * memory) unless stated otherwise; the library never allocates, frees,
+ * synchronises or copies between host and device inside a call.  Calls are
+ * asynchronous on the given stream (a cudaStream_t passed as void*; NULL is
+ * the legacy default stream).  Arguments are checked on the host before any
+ * launch: a rejected call launches nothing and returns the status.
+ *
+ * Types: bf16 tensors are passed as uint16_t bit patterns; fp32 as float.
+ * All tensors are dense, row-major, and every array pointer must be 16-byte
+ * aligned.
+ */
+#ifndef MHC_H
+#define MHC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mhc_status {
+    MHC_OK = 0,
+    MHC_ERR_INVALID_ARGUMENT = 1, /* NULL, misaligned or aliasing pointer, bad count   */
+    MHC_ERR_UNSUPPORTED = 2,      /* valid but outside the shapes this build handles   */
+    MHC_ERR_CUDA = 3,             /* a CUDA runtime call or launch failed               */
+    MHC_ERR_TIMEOUT = 4           /* a bounded device-side wait gave up (see below)      */
+} mhc_status;
+
+/*
+ * mhc_pre_delayed -- the delayed mHC pre block ([A], commit message and
+ * section "Why V4.1 cannot just reuse MHCPreOp": it collapses the sublayer's
+ * input with the PREVIOUS seam's pre-mix and returns this seam's pre-mix;
+ * "Approach": projection against fn plus row square-sums, post/comb gates and
+ * every Sinkhorn iteration; "Result": the collapse is an fp32 multiply-and-sum;
+ * [B] "Measurements": the optional RMSNorm fold x * rsqrt * norm_weight is
+ * evaluated in fp32 and rounded once).  Per token t, with K = n*C and
+ * x_flat[t][i*C + c] = x[t][i][c]:
+ *   r      = 1 / sqrt(sum_k x_flat^2 / K + rms_eps)
+ *   l[m]   = r * (x_flat . fn[m]) * alpha_seg(m) + bias[m],  m < 2n + n^2,
+ *            alpha_seg = alpha[0] (m < n), alpha[1] (m < 2n), alpha[2] (rest)
+ *   pre_out[i]  = sigmoid(l[i]);  post_out[i] = 2 sigmoid(l[n + i])
+ *   comb_out    = sinkhorn_iters Sinkhorn iterations on comb logits
+ *                 l[2n + i*n + j] (row i = source stream, column j =
+ *                 destination): iteration 1 = row softmax, + sinkhorn_eps on
+ *                 every entry, column normalisation; later iterations = row
+ *                 then column normalisation
+ *   h[c]   = ((pre_in[0] x[0][c] + pre_in[1] x[1][c]) + pre_in[2] x[2][c])
+ *            + pre_in[3] x[3][c], every product and sum rounded to fp32
+ *   layer_input[c] = bf16(h[c])                                 (norm_weight NULL)
+ *                  = bf16(h[c] / sqrt(mean_c h^2 + norm_eps) * w[c])  (fold)
+ *
+ *  x            [T, n, C] bf16   residual streams (read only)
+ *  pre_in       [T, n]    fp32   incoming pre-mix of the previous seam
+ *  fn           [2n+n^2, n*C] fp32  projection weight
+ *  bias         [2n+n^2]  fp32
+ *  alpha        [3]       fp32   pre / post / comb logit scales
+ *  norm_weight  [C] bf16 or NULL (NULL: no RMSNorm fold)
+ *  T            tokens, >= 0 (T == 0 launches nothing and returns MHC_OK)
+ *  n            streams; this build supports n == 4 only
+ *  C            hidden size; multiple of 8, 8 <= C <= 6144
+ *  sinkhorn_iters >= 1 (the pages use 20)
+ *  rms_eps, norm_eps, sinkhorn_eps  >= 0 (the pages' workload: 1e-6 each)
+ *  pre_out [T,n], post_out [T,n], comb_out [T,n,n] fp32; layer_input [T,C] bf16
+ *  logits_out   [T, 2n+n^2] fp32 or NULL (debug / parity layer)
+ *  stream       cudaStream_t
+ * Outputs must not overlap any input (pre_out must not alias pre_in:
+ * ping-pong two buffers across seams).  Errors: MHC_ERR_INVALID_ARGUMENT,
+ * MHC_ERR_UNSUPPORTED, MHC_ERR_CUDA.  One kernel launch per call.
+ */
+mhc_status mhc_pre_delayed(const uint16_t *x, const float *pre_in, const float *fn,
+                           const float *bias, const float *alpha,
+                           const uint16_t *norm_weight, int64_t T, int n, int C,
+                           int sinkhorn_iters, float rms_eps, float norm_eps,
+                           float sinkhorn_eps, float *pre_out, float *post_out,
+                           float *comb_out, uint16_t *layer_input, float *logits_out,
+                           void *stream);
+
+/*
+ * mhc_post -- the mHC post block ([A] "Result": the mhc_post call sites go
+ * through MHCPostOp; the post mixes the residual streams through comb and
+ * adds the post-gated sublayer output):
+ *   x_new[t][j][c] = bf16( sum_i comb[t][i][j] * x[t][i][c] + post[t][j] * y[t][c] )
+ * accumulated in fp32, rounded once.
+ *  x     [T, n, C] bf16;  y [T, C] bf16 (sublayer output)
+ *  comb  [T, n, n] fp32;  post [T, n] fp32 (from mhc_pre_delayed)
+ *  x_new [T, n, C] bf16; may be exactly x (in place); must not otherwise
+ *        overlap an input.
+ *  n == 4; C multiple of 8; T >= 0.  Errors as mhc_pre_delayed.
+ *  One kernel launch per call.
+ */
+mhc_status mhc_post(const uint16_t *x, const uint16_t *y, const float *comb,
+                    const float *post, int64_t T, int n, int C, uint16_t *x_new,
+                    void *stream);
+
+/* Static description of the status code (never NULL). */
+const char *mhc_status_string(mhc_status status);
+
+/*
+ * Launch plan of mhc_pre_delayed for a shape, without launching (host only,
+ * no device needed for the shape checks).  kernel: 1 = CUDA-core cluster
+ * kernel; grid/cluster: CTAs launched and CTAs per cluster; tokens_per_tile.
+ * Returns the status mhc_pre_delayed would return for the shape checks.
+ * Any output pointer may be NULL.
+ */
+mhc_status mhc_pre_delayed_plan(int64_t T, int n, int C, int *kernel, int *grid,
+                                int *cluster, int *tokens_per_tile);
+
+/* Library version, (major << 16) | minor. */
+int mhc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MHC_H */

@@ -1,0 +1,173 @@
+"""GB300 (sm_103a) mHC seam: Python binding of libmhc.so.
+
+Thin ctypes marshalling over the C ABI declared in ``include/mhc.h``: it
+checks dtypes, devices and contiguity, allocates outputs with torch when the
+caller passes none, and hands raw device pointers plus the current CUDA
+stream to the library.  Every step of the seam runs in the library's CUDA
+kernels; there is no CPU or PyTorch fallback.  If the library is missing or
+cannot be loaded, every call raises.
+
+    pre_delayed(x, pre_in, fn, bias, alpha, norm_weight=None, ...) -> dict
+    post(x, y, comb, post_gate, out=None) -> Tensor
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = ["pre_delayed", "post", "pre_plan", "library_path", "load_library",
+           "MhcError", "SINKHORN_ITERS"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "_build", "libmhc.so")
+SINKHORN_ITERS = 20
+_STATUS = {0: "MHC_OK", 1: "MHC_ERR_INVALID_ARGUMENT", 2: "MHC_ERR_UNSUPPORTED",
+           3: "MHC_ERR_CUDA", 4: "MHC_ERR_TIMEOUT"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MhcError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn}: {msg}")
+        self.status = status
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libmhc.so (built by ``build.py``); raises if it is absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"libmhc.so not found at {_LIB_PATH}: build it with "
+                "`python -m mhc_hyper_connection_pre_gb300.build` (no fallback exists)")
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, I64, I, F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+        lib.mhc_pre_delayed.argtypes = [P, P, P, P, P, P, I64, I, I, I, F, F, F, P, P, P, P, P, P]
+        lib.mhc_pre_delayed.restype = I
+        lib.mhc_post.argtypes = [P, P, P, P, I64, I, I, P, P]
+        lib.mhc_post.restype = I
+        lib.mhc_status_string.argtypes = [I]
+        lib.mhc_status_string.restype = ctypes.c_char_p
+        lib.mhc_pre_delayed_plan.argtypes = [I64, I, I, P, P, P, P]
+        lib.mhc_pre_delayed_plan.restype = I
+        lib.mhc_version.argtypes = []
+        lib.mhc_version.restype = I
+        _lib = lib
+        return lib
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        lib = load_library()
+        raise MhcError(fn, status, lib.mhc_status_string(status).decode())
+
+
+def _dev_ptr(t: torch.Tensor | None, name: str, dtype: torch.dtype, device) -> int | None:
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda" or (device is not None and t.device != device):
+        raise ValueError(f"{name} must be on the same CUDA device as x (got {t.device})")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype} (got {t.dtype})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream_ptr(stream, device) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return s.cuda_stream
+
+
+def pre_delayed(x: torch.Tensor, pre_in: torch.Tensor, fn: torch.Tensor, bias: torch.Tensor,
+                alpha: torch.Tensor, norm_weight: torch.Tensor | None = None, *,
+                sinkhorn_iters: int = SINKHORN_ITERS, rms_eps: float = 1e-6,
+                norm_eps: float = 1e-6, sinkhorn_eps: float = 1e-6, out: dict | None = None,
+                return_logits: bool = False, stream=None) -> dict:
+    """Delayed mHC pre block (``mhc_pre_delayed`` in include/mhc.h).
+
+    x bf16 [T, 4, C]; pre_in fp32 [T, 4] (previous seam's pre-mix);
+    fn fp32 [24, 4C]; bias fp32 [24]; alpha fp32 [3]; norm_weight bf16 [C]
+    or None.  Returns {"pre", "post", "comb", "layer_input"[, "logits"]}
+    (``out`` may supply preallocated tensors under the same keys).
+    """
+    lib = load_library()
+    if x.dim() != 3:
+        raise ValueError("x must be [T, n, C]")
+    T, n, C = x.shape
+    dev = x.device
+    M = 2 * n + n * n
+    o = dict(out) if out else {}
+    if "pre" not in o:
+        o["pre"] = torch.empty(T, n, dtype=torch.float32, device=dev)
+    if "post" not in o:
+        o["post"] = torch.empty(T, n, dtype=torch.float32, device=dev)
+    if "comb" not in o:
+        o["comb"] = torch.empty(T, n, n, dtype=torch.float32, device=dev)
+    if "layer_input" not in o:
+        o["layer_input"] = torch.empty(T, C, dtype=torch.bfloat16, device=dev)
+    if return_logits and "logits" not in o:
+        o["logits"] = torch.empty(T, M, dtype=torch.float32, device=dev)
+    args = [
+        _dev_ptr(x, "x", torch.bfloat16, dev), _dev_ptr(pre_in, "pre_in", torch.float32, dev),
+        _dev_ptr(fn, "fn", torch.float32, dev), _dev_ptr(bias, "bias", torch.float32, dev),
+        _dev_ptr(alpha, "alpha", torch.float32, dev),
+        _dev_ptr(norm_weight, "norm_weight", torch.bfloat16, dev),
+    ]
+    if pre_in.numel() != T * n or fn.numel() != M * n * C or bias.numel() != M or alpha.numel() != 3:
+        raise ValueError("pre_in / fn / bias / alpha have the wrong number of elements")
+    if norm_weight is not None and norm_weight.numel() != C:
+        raise ValueError("norm_weight must have C elements")
+    outs = [_dev_ptr(o["pre"], "pre", torch.float32, dev), _dev_ptr(o["post"], "post", torch.float32, dev),
+            _dev_ptr(o["comb"], "comb", torch.float32, dev),
+            _dev_ptr(o["layer_input"], "layer_input", torch.bfloat16, dev),
+            _dev_ptr(o.get("logits"), "logits", torch.float32, dev)]
+    st = lib.mhc_pre_delayed(*args, T, n, C, int(sinkhorn_iters), float(rms_eps), float(norm_eps),
+                             float(sinkhorn_eps), *outs, _stream_ptr(stream, dev))
+    _check("mhc_pre_delayed", st)
+    return o
+
+
+def post(x: torch.Tensor, y: torch.Tensor, comb: torch.Tensor, post_gate: torch.Tensor, *,
+         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """mHC post block (``mhc_post``): x_new[j] = sum_i comb[i, j] x[i] + post[j] y.
+    x bf16 [T, 4, C]; y bf16 [T, C]; comb fp32 [T, 4, 4]; post_gate fp32 [T, 4].
+    ``out`` may be ``x`` itself (in place)."""
+    lib = load_library()
+    if x.dim() != 3:
+        raise ValueError("x must be [T, n, C]")
+    T, n, C = x.shape
+    dev = x.device
+    if out is None:
+        out = torch.empty_like(x)
+    if y.numel() != T * C or comb.numel() != T * n * n or post_gate.numel() != T * n or out.shape != x.shape:
+        raise ValueError("y / comb / post / out have the wrong shape")
+    st = lib.mhc_post(_dev_ptr(x, "x", torch.bfloat16, dev), _dev_ptr(y, "y", torch.bfloat16, dev),
+                      _dev_ptr(comb, "comb", torch.float32, dev),
+                      _dev_ptr(post_gate, "post", torch.float32, dev), T, n, C,
+                      _dev_ptr(out, "out", torch.bfloat16, dev), _stream_ptr(stream, dev))
+    _check("mhc_post", st)
+    return out
+
+
+def pre_plan(T: int, n: int = 4, C: int = 5120) -> dict:
+    """Launch plan of ``mhc_pre_delayed`` for a shape (``mhc_pre_delayed_plan``)."""
+    lib = load_library()
+    k, g, c, tt = (ctypes.c_int(0) for _ in range(4))
+    st = lib.mhc_pre_delayed_plan(T, n, C, ctypes.byref(k), ctypes.byref(g), ctypes.byref(c),
+                                  ctypes.byref(tt))
+    _check("mhc_pre_delayed_plan", st)
+    return {"kernel": k.value, "grid": g.value, "cluster": c.value, "tokens_per_tile": tt.value}

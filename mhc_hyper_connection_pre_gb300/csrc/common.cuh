@@ -1,0 +1,85 @@
+// common.cuh -- device helpers shared by the seam kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace mhc {
+
+constexpr int kStreams = 4;                       // hc_mult n
+constexpr int kLogits = 2 * kStreams + kStreams * kStreams;  // 24
+
+// Two bf16 packed in a 32-bit word -> two exact fp32 values.
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Round two fp32 to bf16 (nearest, ties to even) and pack lo | hi << 16.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+    f[0] = bf16lo(v.x); f[1] = bf16hi(v.x);
+    f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
+    f[4] = bf16lo(v.z); f[5] = bf16hi(v.z);
+    f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+    uint4 v;
+    v.x = pack_bf16x2(f[0], f[1]);
+    v.y = pack_bf16x2(f[2], f[3]);
+    v.z = pack_bf16x2(f[4], f[5]);
+    v.w = pack_bf16x2(f[6], f[7]);
+    return v;
+}
+
+// Streaming 16-byte global load / store (data touched once).
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
+__device__ __forceinline__ void st_stream(uint4* p, const uint4& v) { __stcs(p, v); }
+
+// Per-token gates and comb from the 2n+n^2 logits, in fp32, by one thread.
+// pre = sigmoid(l[0:4]), post = 2 sigmoid(l[4:8]); comb = Sinkhorn on the
+// 4x4 row-major comb logits l[8:24]: iteration 1 is the row softmax (max
+// subtracted per row) plus eps on every entry, then a column normalisation;
+// iterations 2..iters normalise rows then columns.
+__device__ __forceinline__ void gates_and_comb(const float (&l)[kLogits], int iters, float eps,
+                                               float (&pre)[4], float (&post)[4],
+                                               float (&P)[16]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        pre[i] = 1.0f / (1.0f + expf(-l[i]));
+        post[i] = 2.0f / (1.0f + expf(-l[4 + i]));
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float mx = fmaxf(fmaxf(l[8 + 4 * i], l[9 + 4 * i]), fmaxf(l[10 + 4 * i], l[11 + 4 * i]));
+        float e0 = expf(l[8 + 4 * i] - mx), e1 = expf(l[9 + 4 * i] - mx);
+        float e2 = expf(l[10 + 4 * i] - mx), e3 = expf(l[11 + 4 * i] - mx);
+        float inv = 1.0f / (((e0 + e1) + e2) + e3);
+        P[4 * i + 0] = e0 * inv + eps;
+        P[4 * i + 1] = e1 * inv + eps;
+        P[4 * i + 2] = e2 * inv + eps;
+        P[4 * i + 3] = e3 * inv + eps;
+    }
+    for (int it = 0; it < iters; ++it) {
+        if (it > 0) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float inv = 1.0f / (((P[4 * i] + P[4 * i + 1]) + P[4 * i + 2]) + P[4 * i + 3]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) P[4 * i + j] *= inv;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float inv = 1.0f / (((P[j] + P[4 + j]) + P[8 + j]) + P[12 + j]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) P[4 * i + j] *= inv;
+        }
+    }
+}
+
+}  // namespace mhc

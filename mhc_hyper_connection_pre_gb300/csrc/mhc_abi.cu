@@ -1,0 +1,188 @@
+// mhc_abi.cu -- the C ABI of libmhc.so (declared in include/mhc.h): host-side
+// argument checks, launch-plan choice and the kernel launches.
+#include "../../include/mhc.h"
+
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+namespace mhc {
+cudaError_t launch_post(const uint16_t* x, const uint16_t* y, const float* comb,
+                        const float* post, int64_t T, int C, uint16_t* x_new,
+                        cudaStream_t stream, int num_sms);
+cudaError_t launch_pre_cluster(const uint16_t* x, const float* pre_in, const float* fn,
+                               const float* bias, const float* alpha, const uint16_t* norm_w,
+                               int64_t T, int C, int iters, float rms_eps, float norm_eps,
+                               float sk_eps, float* pre_out, float* post_out, float* comb_out,
+                               uint16_t* layer_input, float* logits_out, cudaStream_t stream,
+                               int max_clusters);
+int pre_cluster_tile_tokens();
+int pre_cluster_ctas();
+int pre_cluster_prepare(int C);
+}  // namespace mhc
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxC = 6144;
+
+// Per-device cache: SM count, and the cluster kernel's set-up result per
+// hidden size (the kernel instance, and with it the occupancy, depends on C
+// only through the number of 8-column groups per CTA).
+struct DeviceInfo {
+    int num_sms = 0;
+    int cached_C[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    int cached_clusters[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+};
+
+std::mutex g_mutex;
+DeviceInfo g_dev[kMaxDevices];
+
+int current_device() {
+    int d = -1;
+    if (cudaGetDevice(&d) != cudaSuccess) return -1;
+    return (d >= 0 && d < kMaxDevices) ? d : -1;
+}
+
+int num_sms(int dev) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_dev[dev].num_sms == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        g_dev[dev].num_sms = n;
+    }
+    return g_dev[dev].num_sms;
+}
+
+// Maximum co-resident clusters of the pre kernel for hidden size C on device
+// dev, after its one-time set-up; cached for up to 8 hidden sizes per device
+// (others are set up at every call).  0 on error.
+int max_clusters(int dev, int C) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo& d = g_dev[dev];
+    for (int i = 0; i < 8; ++i)
+        if (d.cached_C[i] == C) return d.cached_clusters[i];
+    int n = mhc::pre_cluster_prepare(C);
+    if (n <= 0) return 0;
+    for (int i = 0; i < 8; ++i)
+        if (d.cached_C[i] == 0) {
+            d.cached_C[i] = C;
+            d.cached_clusters[i] = n;
+            break;
+        }
+    return n;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
+    if (!a || !b || an == 0 || bn == 0) return false;
+    uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + bn && b0 < a0 + an;
+}
+
+mhc_status check_pre_shape(int64_t T, int n, int C, int iters) {
+    if (T < 0 || n < 1 || C < 1 || iters < 1) return MHC_ERR_INVALID_ARGUMENT;
+    if (n != 4 || C % 8 != 0 || C > kMaxC) return MHC_ERR_UNSUPPORTED;
+    if (T > ((int64_t)1 << 40) / ((int64_t)n * C)) return MHC_ERR_UNSUPPORTED;
+    return MHC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mhc_status_string(mhc_status s) {
+    switch (s) {
+        case MHC_OK: return "MHC_OK";
+        case MHC_ERR_INVALID_ARGUMENT: return "MHC_ERR_INVALID_ARGUMENT: null, misaligned or overlapping pointer, or bad count";
+        case MHC_ERR_UNSUPPORTED: return "MHC_ERR_UNSUPPORTED: shape outside this build (n must be 4, C a multiple of 8 up to 6144)";
+        case MHC_ERR_CUDA: return "MHC_ERR_CUDA: a CUDA runtime call or kernel launch failed";
+        case MHC_ERR_TIMEOUT: return "MHC_ERR_TIMEOUT: a bounded device-side wait gave up";
+    }
+    return "unknown mhc_status";
+}
+
+int mhc_version(void) { return (0 << 16) | 1; }
+
+mhc_status mhc_pre_delayed_plan(int64_t T, int n, int C, int* kernel, int* grid, int* cluster,
+                                int* tokens_per_tile) {
+    mhc_status st = check_pre_shape(T, n, C, 1);
+    if (st != MHC_OK) return st;
+    const int tt = mhc::pre_cluster_tile_tokens();
+    if (kernel) *kernel = 1;
+    if (cluster) *cluster = mhc::pre_cluster_ctas();
+    if (tokens_per_tile) *tokens_per_tile = tt;
+    if (grid) {
+        *grid = 0;
+        if (T > 0) {
+            int dev = current_device();
+            int mc = dev >= 0 ? max_clusters(dev, C) : 0;
+            int64_t tiles = (T + tt - 1) / tt;
+            if (mc > 0) *grid = (int)((tiles < mc ? tiles : mc) * mhc::pre_cluster_ctas());
+        }
+    }
+    return MHC_OK;
+}
+
+mhc_status mhc_pre_delayed(const uint16_t* x, const float* pre_in, const float* fn,
+                           const float* bias, const float* alpha, const uint16_t* norm_weight,
+                           int64_t T, int n, int C, int sinkhorn_iters, float rms_eps,
+                           float norm_eps, float sinkhorn_eps, float* pre_out, float* post_out,
+                           float* comb_out, uint16_t* layer_input, float* logits_out,
+                           void* stream) {
+    mhc_status st = check_pre_shape(T, n, C, sinkhorn_iters);
+    if (st != MHC_OK) return st;
+    if (!(rms_eps >= 0.f) || !(norm_eps >= 0.f) || !(sinkhorn_eps >= 0.f)) return MHC_ERR_INVALID_ARGUMENT;
+    if (T == 0) return MHC_OK;
+    const void* req[] = {x, pre_in, fn, bias, alpha, pre_out, post_out, comb_out, layer_input};
+    for (const void* p : req)
+        if (!p || !aligned16(p)) return MHC_ERR_INVALID_ARGUMENT;
+    if ((norm_weight && !aligned16(norm_weight)) || (logits_out && !aligned16(logits_out)))
+        return MHC_ERR_INVALID_ARGUMENT;
+    const int M = 2 * n + n * n;
+    const size_t xb = (size_t)T * n * C * 2, pb = (size_t)T * n * 4, cb = (size_t)T * n * n * 4;
+    const size_t lib = (size_t)T * C * 2, lob = (size_t)T * M * 4;
+    const size_t fnb = (size_t)M * n * C * 4, bb = (size_t)M * 4, ab = 12, nwb = (size_t)C * 2;
+    struct R { const void* p; size_t n; };
+    const R ins[] = {{x, xb}, {pre_in, pb}, {fn, fnb}, {bias, bb}, {alpha, ab}, {norm_weight, nwb}};
+    const R outs[] = {{pre_out, pb}, {post_out, pb}, {comb_out, cb}, {layer_input, lib}, {logits_out, lob}};
+    for (const R& o : outs) {
+        for (const R& i : ins)
+            if (overlaps(o.p, o.n, i.p, i.n)) return MHC_ERR_INVALID_ARGUMENT;
+        for (const R& o2 : outs)
+            if (&o != &o2 && overlaps(o.p, o.n, o2.p, o2.n)) return MHC_ERR_INVALID_ARGUMENT;
+    }
+    int dev = current_device();
+    if (dev < 0) return MHC_ERR_CUDA;
+    int mc = max_clusters(dev, C);
+    if (mc <= 0) return MHC_ERR_CUDA;
+    cudaError_t e = mhc::launch_pre_cluster(
+        x, pre_in, fn, bias, alpha, norm_weight, T, C, sinkhorn_iters, rms_eps, norm_eps,
+        sinkhorn_eps, pre_out, post_out, comb_out, layer_input, logits_out,
+        static_cast<cudaStream_t>(stream), mc);
+    return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA;
+}
+
+mhc_status mhc_post(const uint16_t* x, const uint16_t* y, const float* comb, const float* post,
+                    int64_t T, int n, int C, uint16_t* x_new, void* stream) {
+    if (T < 0 || n < 1 || C < 1) return MHC_ERR_INVALID_ARGUMENT;
+    if (n != 4 || C % 8 != 0) return MHC_ERR_UNSUPPORTED;
+    if (T == 0) return MHC_OK;
+    const void* req[] = {x, y, comb, post, x_new};
+    for (const void* p : req)
+        if (!p || !aligned16(p)) return MHC_ERR_INVALID_ARGUMENT;
+    const size_t xb = (size_t)T * n * C * 2;
+    if ((const void*)x_new != (const void*)x && overlaps(x_new, xb, x, xb)) return MHC_ERR_INVALID_ARGUMENT;
+    if (overlaps(x_new, xb, y, (size_t)T * C * 2) || overlaps(x_new, xb, comb, (size_t)T * n * n * 4) ||
+        overlaps(x_new, xb, post, (size_t)T * n * 4))
+        return MHC_ERR_INVALID_ARGUMENT;
+    int dev = current_device();
+    if (dev < 0) return MHC_ERR_CUDA;
+    int sms = num_sms(dev);
+    if (sms <= 0) return MHC_ERR_CUDA;
+    cudaError_t e = mhc::launch_post(x, y, comb, post, T, C, x_new, static_cast<cudaStream_t>(stream), sms);
+    return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,93 @@
+// post.cu -- mHC post block on sm_103a.
+//
+// x_new[t][j][c] = bf16( sum_i comb[t][i][j] x[t][i][c] + post[t][j] y[t][c] )
+// (the vLLM page "Use AITER mHC for the delayed pre block", section "Result":
+// the post call sites go through MHCPostOp, which mixes the residual streams
+// through comb and adds the post-gated sublayer output).
+//
+// Pure HBM streaming: per token 4 x 10240 B of x and 10240 B of y are read
+// and 4 x 10240 B written (C = 5120); 20 FMAs per output column.  One work
+// item is 8 consecutive columns of one token: four 16-byte loads of x (one
+// per stream), one of y, four 16-byte stores.  A grid-stride loop over
+// items, two items in flight per thread, streaming cache hints so that the
+// once-touched data does not evict reused lines from L2.  x_new may be x
+// (in place): a thread reads all four streams of its item before writing them
+// and items are disjoint, so x and x_new carry no __restrict__.
+#include "common.cuh"
+
+namespace mhc {
+
+__global__ void __launch_bounds__(256)
+post_kernel(const uint4* x, const uint4* __restrict__ y,
+            const float4* __restrict__ comb, const float4* __restrict__ post,
+            int64_t items, int c8, uint4* x_new) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; base < items;
+         base += 2 * stride) {
+        uint4 xv[2][4], yv[2];
+        int64_t tok[2], col[2];
+        bool ok[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            int64_t it = base + u * stride;
+            ok[u] = it < items;
+            if (!ok[u]) it = base;
+            tok[u] = it / c8;
+            col[u] = it - tok[u] * c8;
+            const uint4* xp = x + tok[u] * (4 * (int64_t)c8) + col[u];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) xv[u][i] = ld_stream(xp + (int64_t)i * c8);
+            yv[u] = ld_stream(y + tok[u] * c8 + col[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            if (!ok[u]) continue;
+            float4 cm[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) cm[i] = __ldg(comb + tok[u] * 4 + i);  // row i of comb
+            float4 pg = __ldg(post + tok[u]);
+            const float cw[4][4] = {{cm[0].x, cm[0].y, cm[0].z, cm[0].w},
+                                    {cm[1].x, cm[1].y, cm[1].z, cm[1].w},
+                                    {cm[2].x, cm[2].y, cm[2].z, cm[2].w},
+                                    {cm[3].x, cm[3].y, cm[3].z, cm[3].w}};
+            const float pw[4] = {pg.x, pg.y, pg.z, pg.w};
+            float xs[4][8], ys[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) unpack8(xv[u][i], xs[i]);
+            unpack8(yv[u], ys);
+            uint4* op = x_new + tok[u] * (4 * (int64_t)c8) + col[u];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float o[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    float acc = cw[0][j] * xs[0][e];
+                    acc = fmaf(cw[1][j], xs[1][e], acc);
+                    acc = fmaf(cw[2][j], xs[2][e], acc);
+                    acc = fmaf(cw[3][j], xs[3][e], acc);
+                    o[e] = fmaf(pw[j], ys[e], acc);
+                }
+                st_stream(op + (int64_t)j * c8, pack8(o));
+            }
+        }
+    }
+}
+
+cudaError_t launch_post(const uint16_t* x, const uint16_t* y, const float* comb,
+                        const float* post, int64_t T, int C, uint16_t* x_new,
+                        cudaStream_t stream, int num_sms) {
+    const int c8 = C / 8;
+    const int64_t items = T * (int64_t)c8;
+    const int threads = 256;
+    int64_t want = (items + 2 * threads - 1) / (2 * threads);
+    int64_t cap = (int64_t)num_sms * 8;
+    int blocks = (int)(want < cap ? want : cap);
+    if (blocks < 1) blocks = 1;
+    post_kernel<<<blocks, threads, 0, stream>>>(
+        reinterpret_cast<const uint4*>(x), reinterpret_cast<const uint4*>(y),
+        reinterpret_cast<const float4*>(comb), reinterpret_cast<const float4*>(post), items,
+        c8, reinterpret_cast<uint4*>(x_new));
+    return cudaGetLastError();
+}
+
+}  // namespace mhc

@@ -72,7 +72,7 @@ def _load():
                 P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_double, P, P, P]
             lib.mhc_oracle_gates_from_logits.restype = ctypes.c_int
             lib.mhc_oracle_post.argtypes = [
-                P, P, P, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, P, P]
+                P, P, P, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int]
             lib.mhc_oracle_post.restype = ctypes.c_int
             lib.mhc_oracle_bf16_round.argtypes = [P, ctypes.c_int64, P]
             lib.mhc_oracle_bf16_round.restype = None
@@ -163,7 +163,7 @@ def gates_from_logits(logits, n=4, *, iters=SINKHORN_ITERS,
     return {"pre": pre, "post": post, "comb": comb}
 
 
-def post(x_bits, y_bits, comb, post_gate) -> tuple[np.ndarray, np.ndarray]:
+def post(x_bits, y_bits, comb, post_gate, *, nthreads=1) -> tuple[np.ndarray, np.ndarray]:
     """mHC post (MHCPostOp on the #56503 page): x_new[j] = bf16(sum_i
     comb[i, j] x[i] + post[j] y), exact in fp64 then rounded once.
     Returns (x_new bf16 bits [T, n, C], exact fp64 values [T, n, C])."""
@@ -175,7 +175,7 @@ def post(x_bits, y_bits, comb, post_gate) -> tuple[np.ndarray, np.ndarray]:
     xn = np.empty((T, n, C), np.uint16)
     x64 = np.empty((T, n, C), np.float64)
     rc = _load().mhc_oracle_post(_ptr(x_bits), _ptr(y_bits), _ptr(comb), _ptr(post_gate),
-                                 T, n, C, _ptr(xn), _ptr(x64))
+                                 T, n, C, _ptr(xn), _ptr(x64), int(nthreads))
     if rc != 0:
         raise ValueError("oracle: bad arguments to post")
     return xn, x64

@@ -291,21 +291,28 @@ ORACLE_API int mhc_oracle_pre_delayed(
 
 /* --------------------------------------------------------------- post --- */
 
+typedef struct {
+    const uint16_t *x, *y;
+    const float *comb, *post;
+    int n, C;
+    uint16_t *x_new;
+    double *x_new64;
+    int64_t t0, t1;
+} post_chunk;
+
 /* x_new[t][j][c] = bf16( sum_i comb[t][i][j] * x[t][i][c] + post[t][j] * y[t][c] ),
  * evaluated exactly in fp64 from the given fp32 comb/post and bf16 x, y, then
  * rounded once ("mix the residual streams through comb and add the
  * post-gated sublayer output"; MHCPostOp in the pages). */
-ORACLE_API int mhc_oracle_post(const uint16_t *x, const uint16_t *y, const float *comb,
-                               const float *post, int64_t T, int n, int C,
-                               uint16_t *x_new, double *x_new64)
+static void *post_worker(void *p)
 {
-    if (T < 0 || n < 1 || C < 1)
-        return 1;
-    for (int64_t t = 0; t < T; ++t) {
-        const uint16_t *xt = x + t * (int64_t)n * C;
-        const uint16_t *yt = y + t * (int64_t)C;
-        const float *cb = comb + t * n * n;
-        const float *pt = post + t * n;
+    const post_chunk *a = (const post_chunk *)p;
+    const int n = a->n, C = a->C;
+    for (int64_t t = a->t0; t < a->t1; ++t) {
+        const uint16_t *xt = a->x + t * (int64_t)n * C;
+        const uint16_t *yt = a->y + t * (int64_t)C;
+        const float *cb = a->comb + t * n * n;
+        const float *pt = a->post + t * n;
         for (int j = 0; j < n; ++j) {
             for (int c = 0; c < C; ++c) {
                 double acc = 0.0;
@@ -313,11 +320,42 @@ ORACLE_API int mhc_oracle_post(const uint16_t *x, const uint16_t *y, const float
                     acc += (double)cb[i * n + j] * bf16_value(xt[(int64_t)i * C + c]);
                 acc += (double)pt[j] * bf16_value(yt[c]);
                 int64_t o = (t * n + j) * (int64_t)C + c;
-                x_new[o] = bf16_round(acc);
-                if (x_new64)
-                    x_new64[o] = acc;
+                a->x_new[o] = bf16_round(acc);
+                if (a->x_new64)
+                    a->x_new64[o] = acc;
             }
         }
     }
+    return NULL;
+}
+
+ORACLE_API int mhc_oracle_post(const uint16_t *x, const uint16_t *y, const float *comb,
+                               const float *post, int64_t T, int n, int C,
+                               uint16_t *x_new, double *x_new64, int nthreads)
+{
+    if (T < 0 || n < 1 || C < 1)
+        return 1;
+    if (T > 0 && (!x || !y || !comb || !post || !x_new))
+        return 1;
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > T)
+        nthreads = T > 0 ? (int)T : 1;
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    post_chunk *ch = (post_chunk *)malloc(sizeof(post_chunk) * (size_t)nthreads);
+    for (int i = 0; i < nthreads; ++i) {
+        post_chunk c = {x, y, comb, post, n, C, x_new, x_new64,
+                        T * i / nthreads, T * (i + 1) / nthreads};
+        ch[i] = c;
+        if (nthreads == 1)
+            post_worker(&ch[i]);
+        else
+            pthread_create(&th[i], NULL, post_worker, &ch[i]);
+    }
+    if (nthreads > 1)
+        for (int i = 0; i < nthreads; ++i)
+            pthread_join(th[i], NULL);
+    free(th);
+    free(ch);
     return 0;
 }

@@ -1,0 +1,94 @@
+"""Comparison rules between the CUDA path and the CPU oracle.
+
+Tolerances (the spec bars of this seam, restated):
+  * collapse without the fold: bit-exact (the oracle's fp32 path, stream
+    order, no fused multiply-add; the #56503 page reports the collapse as
+    bit-exact because it is the same fp32 multiply-and-sum);
+  * pre / post / comb: |gpu - oracle| <= 2e-5 |oracle| + 1e-37 (fp32 gates vs
+    the fp64 oracle);
+  * bf16 outputs (folded layer_input, post): within 1 bf16 ulp of the
+    oracle's rounded value, or -- where the exact value is so close to zero
+    that fp32 cancellation dominates -- within 2^-20 of the sum of the
+    absolute terms;
+  * logits: |dl| <= 1e-6 r |alpha| sum_k |x_k fn_mk| + 2^-22 |l|, the fp32
+    accumulation bound of a 20480-term dot product (rounding-order
+    independent).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+
+REL_GATES = 2e-5
+
+
+def ulp_distance_bf16(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
+    """Distance in representable bf16 steps (sign-magnitude mapped to an
+    ordered integer line)."""
+    def ordered(b):
+        b = b.astype(np.int32)
+        return np.where(b & 0x8000, -(b & 0x7fff), b & 0x7fff)
+    return np.abs(ordered(a_bits) - ordered(b_bits))
+
+
+def assert_gates(g: np.ndarray, o: np.ndarray, what: str, rel: float = REL_GATES):
+    g = np.asarray(g, np.float64)
+    o = np.asarray(o, np.float64)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite values"
+    err = np.abs(g - o)
+    bad = err > rel * np.abs(o) + 1e-37
+    if np.any(bad):
+        i = np.argwhere(bad)[0]
+        worst = np.max(err / (np.abs(o) + 1e-37))
+        raise AssertionError(f"{what}: {bad.sum()} elements beyond rel {rel}; first at {tuple(i)} "
+                             f"gpu={g[tuple(i)]!r} oracle={o[tuple(i)]!r}; worst rel {worst:.3e}")
+
+
+def assert_bf16(g_bits: np.ndarray, o_bits: np.ndarray, what: str, abs_scale: np.ndarray | None = None):
+    d = ulp_distance_bf16(g_bits, o_bits)
+    bad = d > 1
+    if abs_scale is not None and np.any(bad):
+        diff = np.abs(oracle.bf16_to_f64(g_bits) - oracle.bf16_to_f64(o_bits))
+        bad &= diff > 2.0 ** -20 * abs_scale
+    if np.any(bad):
+        i = np.argwhere(bad)[0]
+        raise AssertionError(f"{what}: {bad.sum()} elements beyond 1 bf16 ulp; first at {tuple(i)} "
+                             f"gpu=0x{int(g_bits[tuple(i)]):04x} oracle=0x{int(o_bits[tuple(i)]):04x}")
+
+
+def assert_bitexact(g_bits: np.ndarray, o_bits: np.ndarray, what: str):
+    if not np.array_equal(g_bits, o_bits):
+        bad = g_bits != o_bits
+        i = np.argwhere(bad)[0]
+        raise AssertionError(f"{what}: {bad.sum()} elements differ; first at {tuple(i)} "
+                             f"gpu=0x{int(g_bits[tuple(i)]):04x} oracle=0x{int(o_bits[tuple(i)]):04x}")
+
+
+def logit_bound(x_bits: np.ndarray, fn: np.ndarray, alpha: np.ndarray, logits64: np.ndarray,
+                rms_eps: float = oracle.RMS_EPS) -> np.ndarray:
+    x = oracle.bf16_to_f64(x_bits).reshape(x_bits.shape[0], -1)
+    K = x.shape[1]
+    r = 1.0 / np.sqrt((x * x).sum(1) / K + rms_eps)
+    n = 4
+    al = np.array([alpha[0]] * n + [alpha[1]] * n + [alpha[2]] * (n * n), np.float64)
+    s_abs = np.abs(x) @ np.abs(fn.astype(np.float64)).T
+    return 1e-6 * r[:, None] * np.abs(al)[None, :] * s_abs + 2.0 ** -22 * np.abs(logits64)
+
+
+def assert_logits(g: np.ndarray, o: np.ndarray, bound: np.ndarray, what: str = "logits"):
+    err = np.abs(np.asarray(g, np.float64) - o)
+    bad = err > bound
+    if np.any(bad):
+        i = np.argwhere(bad)[0]
+        raise AssertionError(f"{what}: {bad.sum()} beyond the fp32 dot-product bound; first at "
+                             f"{tuple(i)} gpu={g[tuple(i)]!r} oracle={o[tuple(i)]!r} bound={bound[tuple(i)]:.3e}")
+
+
+def post_abs_scale(x_bits, y_bits, comb, post_gate) -> np.ndarray:
+    """sum_i |comb[i, j] x_i| + |post_j y| per output element [T, n, C]."""
+    x = oracle.bf16_to_f64(x_bits)
+    y = oracle.bf16_to_f64(y_bits)
+    cb = np.abs(np.asarray(comb, np.float64))
+    pg = np.abs(np.asarray(post_gate, np.float64))
+    return np.einsum("tij,tic->tjc", cb, np.abs(x)) + pg[:, :, None] * np.abs(y)[:, None, :]

@@ -1,0 +1,125 @@
+"""Host-only checks of the C ABI (no GPU needed): the library loads, exports
+every function include/mhc.h declares, and rejects bad arguments on the host
+before any CUDA call (fake pointer values are never dereferenced because
+every call here is rejected by the host checks)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mhc_hyper_connection_pre_gb300 as mhc
+from mhc_hyper_connection_pre_gb300 import build as mbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, INVALID, UNSUPPORTED, CUDA_ERR = 0, 1, 2, 3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mbuild.build()
+    return mhc.load_library()
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(mhc_[a-z0-9_]+)\s*\(", src))
+    return sorted(names)
+
+
+def test_exports_every_declared_function(lib):
+    names = _declared_functions()
+    assert {"mhc_pre_delayed", "mhc_post", "mhc_status_string"} <= set(names)
+    for name in names:
+        assert hasattr(lib, name), f"libmhc.so does not export {name}"
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        s = lib.mhc_status_string(code).decode()
+        assert s.startswith("MHC_")
+    assert lib.mhc_status_string(99).decode() == "unknown mhc_status"
+    assert lib.mhc_version() >= 1
+
+
+A = 0x10000  # a 16-byte aligned fake address; never dereferenced here
+
+
+def _pre(lib, **kw):
+    args = dict(x=A, pre_in=A + 0x100000, fn=A + 0x200000, bias=A + 0x3000000, alpha=A + 0x3001000,
+                norm_weight=None, T=16, n=4, C=5120, iters=20, rms_eps=1e-6, norm_eps=1e-6,
+                sk_eps=1e-6, pre_out=A + 0x4000000, post_out=A + 0x4100000, comb_out=A + 0x4200000,
+                layer_input=A + 0x4300000, logits_out=None, stream=None)
+    args.update(kw)
+    return lib.mhc_pre_delayed(*args.values())
+
+
+def test_pre_rejects_bad_shapes(lib):
+    assert _pre(lib, n=3) == UNSUPPORTED
+    assert _pre(lib, C=5121) == UNSUPPORTED
+    assert _pre(lib, C=5124) == UNSUPPORTED
+    assert _pre(lib, C=6152) == UNSUPPORTED
+    assert _pre(lib, T=-1) == INVALID
+    assert _pre(lib, iters=0) == INVALID
+    assert _pre(lib, n=0) == INVALID
+    assert _pre(lib, rms_eps=-1.0) == INVALID
+    assert _pre(lib, norm_eps=float("nan")) == INVALID
+
+
+def test_pre_zero_tokens_is_a_no_op(lib):
+    # T == 0 returns before any pointer is looked at or any launch
+    assert _pre(lib, T=0, x=None, pre_in=None, fn=None) == OK
+
+
+def test_pre_rejects_null_misaligned_and_overlapping(lib):
+    assert _pre(lib, x=None) == INVALID
+    assert _pre(lib, fn=None) == INVALID
+    assert _pre(lib, layer_input=None) == INVALID
+    assert _pre(lib, x=A + 8) == INVALID
+    assert _pre(lib, comb_out=A + 0x4200004) == INVALID
+    assert _pre(lib, norm_weight=A + 0x5000002) == INVALID
+    # pre_out aliasing pre_in (the carried pre-mix must be ping-ponged)
+    assert _pre(lib, pre_out=A + 0x100000) == INVALID
+    # layer_input inside x
+    assert _pre(lib, layer_input=A + 0x1000) == INVALID
+    # two outputs overlapping
+    assert _pre(lib, post_out=A + 0x4000010) == INVALID
+
+
+def _post(lib, **kw):
+    args = dict(x=A, y=A + 0x1000000, comb=A + 0x2000000, post=A + 0x2100000, T=16, n=4, C=5120,
+                x_new=A + 0x3000000, stream=None)
+    args.update(kw)
+    return lib.mhc_post(*args.values())
+
+
+def test_post_rejects_bad_arguments(lib):
+    assert _post(lib, n=2) == UNSUPPORTED
+    assert _post(lib, C=100) == UNSUPPORTED
+    assert _post(lib, T=-5) == INVALID
+    assert _post(lib, T=0, x=None) == OK
+    assert _post(lib, y=None) == INVALID
+    assert _post(lib, comb=A + 0x2000004) == INVALID
+    assert _post(lib, x_new=A + 0x10) == INVALID           # overlaps x, not equal
+    assert _post(lib, x_new=A + 0x1000000) == INVALID      # overlaps y
+
+
+def test_plan_shape_checks(lib):
+    kernel, grid, cluster, tt = (ctypes.c_int(-1) for _ in range(4))
+    st = lib.mhc_pre_delayed_plan(16, 4, 5120, ctypes.byref(kernel), ctypes.byref(grid),
+                                  ctypes.byref(cluster), ctypes.byref(tt))
+    assert st == OK
+    assert kernel.value == 1 and cluster.value == 16 and tt.value == 8
+    assert lib.mhc_pre_delayed_plan(16, 4, 5121, None, None, None, None) == UNSUPPORTED
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    x = torch.zeros(2, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        mhc.post(x, torch.zeros(2, 64, dtype=torch.bfloat16), torch.zeros(2, 4, 4),
+                 torch.zeros(2, 4))

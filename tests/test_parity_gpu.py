@@ -1,0 +1,293 @@
+"""GPU parity: the CUDA seam (through the C ABI) against the CPU oracle on
+the same seeded inputs, element by element, plus launch-count, graph-replay
+and determinism checks.  Needs a GB300 and a built libmhc.so."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import mhc_hyper_connection_pre_gb300 as mhc
+from mhc_hyper_connection_pre_gb300.graphs import SeamGraph
+from workloads import seam_inputs, bf16_bits
+from parity import (assert_gates, assert_bf16, assert_bitexact, assert_logits, logit_bound,
+                    post_abs_scale)
+
+pytestmark = pytest.mark.gpu
+
+NTHREADS = os.cpu_count() or 1
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    mhc.load_library()
+    oracle.build()
+
+
+def _to_dev(d):
+    return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+
+
+def _gpu_pre(g, **kw):
+    out = mhc.pre_delayed(g["x"], g["pre_in"], g["fn"], g["bias"], g["alpha"], g["norm_w"],
+                          return_logits=True, **kw)
+    torch.cuda.synchronize()
+    return {k: v.cpu() for k, v in out.items()}
+
+
+def _oracle_pre(d, rows=None):
+    x = bf16_bits(d["x"])
+    pre_in = d["pre_in"].cpu().numpy()
+    if rows is not None:
+        x, pre_in = x[rows], pre_in[rows]
+    nw = None if d["norm_w"] is None else bf16_bits(d["norm_w"])
+    return oracle.pre_delayed(x, pre_in, d["fn"].cpu().numpy(), d["bias"].cpu().numpy(),
+                              d["alpha"].cpu().numpy(), nw, nthreads=NTHREADS), x
+
+
+def _check_pre(g, o, x_bits, d, fold, rows=None):
+    sl = slice(None) if rows is None else rows
+    li = g["layer_input"].view(torch.int16).numpy().view(np.uint16)[sl]
+    if fold:
+        assert_bf16(li, o["layer_input"], "layer_input (fold)")
+    else:
+        assert_bitexact(li, o["layer_input"], "layer_input (collapse)")
+    assert_gates(g["pre"].numpy()[sl], o["pre"], "pre")
+    assert_gates(g["post"].numpy()[sl], o["post"], "post")
+    assert_gates(g["comb"].numpy()[sl], o["comb"], "comb")
+    bound = logit_bound(x_bits, d["fn"].cpu().numpy(), d["alpha"].cpu().numpy(), o["logits"])
+    assert_logits(g["logits"].numpy()[sl], o["logits"], bound)
+
+
+def test_config0_pr1_reference():
+    """T=16, seed 0, no fold: collapse bit-exact, gates within 2e-5."""
+    d = seam_inputs(16, seed=0)
+    g = _gpu_pre(_to_dev(d))
+    o, xb = _oracle_pre(d)
+    _check_pre(g, o, xb, d, fold=False)
+
+
+@pytest.mark.parametrize("T", [1, 2, 4, 8, 16, 32, 64, 128])
+def test_config1_decode_sweep(T):
+    """Decode sweep with the fused RMSNorm fold, seed = T."""
+    d = seam_inputs(T, seed=T, fold=True)
+    g = _gpu_pre(_to_dev(d))
+    o, xb = _oracle_pre(d)
+    _check_pre(g, o, xb, d, fold=True)
+
+
+@pytest.mark.parametrize("T,C,fold", [
+    (1, 8, False), (3, 8, True), (7, 136, True), (31, 1000, False), (9, 2056, True),
+    (127, 5120, False), (129, 5120, True), (17, 6144, True), (64, 6144, False),
+    (1000, 5120, True), (33, 4096, False), (5, 128, True), (2, 2048, True),
+])
+def test_token_and_hidden_sweep(T, C, fold):
+    """Ragged token tails (not multiples of the 8-token tile), hidden sizes
+    whose 8-column groups do not split evenly over the 16 CTA slices, and
+    slices with no columns at all (C = 8)."""
+    d = seam_inputs(T, C=C, seed=100 + T + C, fold=fold)
+    g = _gpu_pre(_to_dev(d))
+    o, xb = _oracle_pre(d)
+    _check_pre(g, o, xb, d, fold=fold)
+
+
+def test_alpha_and_sinkhorn_parameters():
+    """Non-unit alphas, another iteration count and eps reach the kernel."""
+    d = seam_inputs(24, seed=5, fold=True)
+    d["alpha"] = torch.tensor([0.5, 1.7, 2.5])
+    gd = _to_dev(d)
+    out = mhc.pre_delayed(gd["x"], gd["pre_in"], gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"],
+                          sinkhorn_iters=3, sinkhorn_eps=1e-3, rms_eps=1e-5, norm_eps=1e-4,
+                          return_logits=True)
+    torch.cuda.synchronize()
+    g = {k: v.cpu() for k, v in out.items()}
+    o = oracle.pre_delayed(bf16_bits(d["x"]), d["pre_in"].numpy(), d["fn"].numpy(), d["bias"].numpy(),
+                           d["alpha"].numpy(), bf16_bits(d["norm_w"]), iters=3, sinkhorn_eps=1e-3,
+                           rms_eps=float(np.float32(1e-5)), norm_eps=float(np.float32(1e-4)),
+                           nthreads=NTHREADS)
+    li = g["layer_input"].view(torch.int16).numpy().view(np.uint16)
+    assert_bf16(li, o["layer_input"], "layer_input")
+    for k in ("pre", "post", "comb"):
+        assert_gates(g[k].numpy(), o[k], k)
+
+
+def test_staggering_invariance():
+    """Changing the incoming pre-mix leaves logits, gates and comb
+    bit-identical (the #56503 page: the staggering does not change the
+    gates); feeding pre_in := this seam's pre gives the non-delayed collapse."""
+    d = seam_inputs(40, seed=6, fold=False)
+    gd = _to_dev(d)
+    a = _gpu_pre(gd)
+    gd2 = dict(gd)
+    gd2["pre_in"] = torch.rand(40, 4, device="cuda")
+    b = _gpu_pre(gd2)
+    for k in ("pre", "post", "comb", "logits"):
+        assert torch.equal(a[k], b[k]), k
+    gd3 = dict(gd)
+    gd3["pre_in"] = a["pre"].cuda()
+    c = _gpu_pre(gd3)
+    o = oracle.pre_delayed(bf16_bits(d["x"]), a["pre"].numpy(), d["fn"].numpy(), d["bias"].numpy(),
+                           d["alpha"].numpy(), None, nthreads=NTHREADS)
+    assert_bitexact(c["layer_input"].view(torch.int16).numpy().view(np.uint16), o["layer_input"],
+                    "non-delayed collapse")
+
+
+def test_deterministic():
+    d = _to_dev(seam_inputs(300, seed=8, fold=True))
+    a, b = _gpu_pre(d), _gpu_pre(d)
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_zero_tokens():
+    x = torch.empty(0, 4, 5120, dtype=torch.bfloat16, device="cuda")
+    out = mhc.pre_delayed(x, torch.empty(0, 4, device="cuda"), torch.zeros(24, 20480, device="cuda"),
+                          torch.zeros(24, device="cuda"), torch.ones(3, device="cuda"))
+    assert out["layer_input"].shape == (0, 5120)
+    xn = mhc.post(x, torch.empty(0, 5120, dtype=torch.bfloat16, device="cuda"),
+                  torch.empty(0, 4, 4, device="cuda"), torch.empty(0, 4, device="cuda"))
+    assert xn.shape == (0, 4, 5120)
+
+
+def _post_case(T, C, seed):
+    d = seam_inputs(T, C=C, seed=seed, fold=True, with_y=True)
+    gd = _to_dev(d)
+    pre = mhc.pre_delayed(gd["x"], gd["pre_in"], gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"])
+    return d, gd, pre
+
+
+@pytest.mark.parametrize("T,C", [(1, 5120), (5, 5120), (64, 5120), (1000, 5120), (3, 8), (17, 2056)])
+def test_post_parity(T, C):
+    d, gd, pre = _post_case(T, C, seed=200 + T)
+    xn = mhc.post(gd["x"], gd["y"], pre["comb"], pre["post"])
+    torch.cuda.synchronize()
+    comb, pg = pre["comb"].cpu().numpy(), pre["post"].cpu().numpy()
+    xb, yb = bf16_bits(d["x"]), bf16_bits(d["y"])
+    o_bits, _ = oracle.post(xb, yb, comb, pg)
+    g_bits = xn.cpu().view(torch.int16).numpy().view(np.uint16)
+    assert_bf16(g_bits, o_bits, "x_new", abs_scale=post_abs_scale(xb, yb, comb, pg))
+
+
+def test_post_in_place():
+    d, gd, pre = _post_case(50, 5120, seed=301)
+    ref = mhc.post(gd["x"], gd["y"], pre["comb"], pre["post"])
+    x2 = gd["x"].clone()
+    mhc.post(x2, gd["y"], pre["comb"], pre["post"], out=x2)
+    torch.cuda.synchronize()
+    assert torch.equal(ref, x2)
+
+
+def test_graph_seam_is_two_launches_and_replays_exactly():
+    """One seam (pre + post) captured in a CUDA graph holds exactly 2 kernel
+    nodes; 200 replays give the eager result bit for bit."""
+    d, gd, pre = _post_case(4, 5120, seed=400)
+    eager_pre = {k: v.clone() for k, v in pre.items()}
+    eager_xn = mhc.post(gd["x"], gd["y"], pre["comb"], pre["post"])
+    out = {k: torch.empty_like(v) for k, v in pre.items()}
+    xn = torch.empty_like(gd["x"])
+    s = torch.cuda.Stream()
+
+    def seam(stream):
+        mhc.pre_delayed(gd["x"], gd["pre_in"], gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"],
+                        out=out, stream=stream)
+        mhc.post(gd["x"], gd["y"], out["comb"], out["post"], out=xn, stream=stream)
+
+    g = SeamGraph(seam, s)
+    assert g.kernel_nodes == 2, g.kernel_nodes
+    g.replay(200)
+    s.synchronize()
+    for k in eager_pre:
+        assert torch.equal(out[k], eager_pre[k]), k
+    assert torch.equal(xn, eager_xn)
+    g.close()
+
+
+# ------------------------------------------------- stress and full sizes ---
+
+def _check_comb_properties(comb: np.ndarray):
+    assert np.all(np.isfinite(comb))
+    assert np.all(comb >= 0)
+    np.testing.assert_allclose(comb.sum(1), 1.0, atol=1e-5)   # columns, fp32
+
+
+def test_stress_small_layered():
+    """Config-4 distribution at T=2048: comb logits of order +-300, 1% rows
+    scaled by 1e3, 1% zero rows.  Layered check: logits within the fp32 dot
+    bound; gates and comb recomputed by the oracle from the GPU's own logits
+    within 2e-5; pre/post end to end; no NaN/Inf; Sinkhorn invariants."""
+    T = 2048
+    d = seam_inputs(T, seed=0, fold=True, stress=True)
+    g = _gpu_pre(_to_dev(d))
+    o, xb = _oracle_pre(d)
+    bound = logit_bound(xb, d["fn"].numpy(), d["alpha"].numpy(), o["logits"])
+    assert_logits(g["logits"].numpy(), o["logits"], bound)
+    og = oracle.gates_from_logits(g["logits"].numpy().astype(np.float64))
+    for k in ("pre", "post", "comb"):
+        assert_gates(g[k].numpy(), og[k], k + " (from gpu logits)")
+    assert_gates(g["pre"].numpy(), o["pre"], "pre")
+    assert_gates(g["post"].numpy(), o["post"], "post")
+    assert_bf16(g["layer_input"].view(torch.int16).numpy().view(np.uint16), o["layer_input"],
+                "layer_input")
+    _check_comb_properties(g["comb"].numpy())
+    zero = np.all(xb.reshape(T, -1) == 0, axis=1)
+    assert zero.sum() == T // 100
+    assert np.all(g["layer_input"].view(torch.int16).numpy()[zero] == 0)
+
+
+def _sample_rows(T, extra=()):
+    rng = np.random.default_rng(T)
+    rows = set(rng.choice(T, size=min(T, 48), replace=False).tolist())
+    rows |= {0, 1, 7, 8, T // 2, T - 9, T - 8, T - 1}
+    rows |= set(int(r) for r in extra)
+    return np.array(sorted(r for r in rows if 0 <= r < T))
+
+
+def test_config2_prefill_full_size_sampled():
+    """T=16384 with the fold, the launch configuration the benchmark times:
+    pre and post on all tokens, compared with the oracle on sampled tokens,
+    and properties checked on every token."""
+    T = 16384
+    gd = seam_inputs(T, seed=0, fold=True, with_y=True, device="cuda")
+    out = mhc.pre_delayed(gd["x"], gd["pre_in"], gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"],
+                          return_logits=True)
+    xn = mhc.post(gd["x"], gd["y"], out["comb"], out["post"])
+    torch.cuda.synchronize()
+    rows = _sample_rows(T)
+    g = {k: v.cpu() for k, v in out.items()}
+    o, xb = _oracle_pre(gd, rows)
+    _check_pre(g, o, xb, gd, fold=True, rows=rows)
+    _check_comb_properties(g["comb"].numpy())
+    comb, pg = g["comb"].numpy()[rows], g["post"].numpy()[rows]
+    yb = bf16_bits(gd["y"])[rows]
+    o_bits, _ = oracle.post(xb, yb, comb, pg)
+    g_bits = xn[rows.tolist()].cpu().view(torch.int16).numpy().view(np.uint16)
+    assert_bf16(g_bits, o_bits, "x_new", abs_scale=post_abs_scale(xb, yb, comb, pg))
+
+
+def test_config4_stress_full_size_sampled():
+    T = 65536
+    gd = seam_inputs(T, seed=0, fold=True, stress=True, device="cuda")
+    out = mhc.pre_delayed(gd["x"], gd["pre_in"], gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"],
+                          return_logits=True)
+    torch.cuda.synchronize()
+    g = {k: v.cpu() for k, v in out.items()}
+    for k in g:
+        if g[k].dtype == torch.float32:
+            assert torch.isfinite(g[k]).all(), k
+    _check_comb_properties(g["comb"].numpy())
+    xr = gd["x"].reshape(T, -1)
+    zero = (xr == 0).all(1)
+    big = xr.abs().amax(1) > 100
+    extra = torch.nonzero(zero).flatten()[:8].tolist() + torch.nonzero(big).flatten()[:8].tolist()
+    rows = _sample_rows(T, extra)
+    o, xb = _oracle_pre(gd, rows)
+    bound = logit_bound(xb, gd["fn"].cpu().numpy(), gd["alpha"].cpu().numpy(), o["logits"])
+    assert_logits(g["logits"].numpy()[rows], o["logits"], bound)
+    og = oracle.gates_from_logits(g["logits"].numpy()[rows].astype(np.float64))
+    for k in ("pre", "post", "comb"):
+        assert_gates(g[k].numpy()[rows], og[k], k + " (from gpu logits)")
+    assert_bf16(g["layer_input"].view(torch.int16).numpy().view(np.uint16)[rows], o["layer_input"],
+                "layer_input")
+    assert torch.all(g["layer_input"].view(torch.int16)[zero.cpu()] == 0)
