@@ -199,7 +199,7 @@ def run_ours(args, rank, world, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     hbm_peak, peak_kind = load_peaks()
-    T = T_PREFILL
+    T = args.tokens
     d = seam_inputs(T, seed=rank, fold=True, with_y=True, device=f"cuda:{local}")
     x, y = d["x"], d["y"]
     pre_in = [d["pre_in"], torch.empty_like(d["pre_in"])]
@@ -269,7 +269,7 @@ def run_ours(args, rank, world, local):
 
     # ---- end to end through the public API: pinned host in, pinned host out
     e2e = None
-    if rank == 0 or world > 1:
+    if not args.skip_e2e:
         hx = torch.empty(x.shape, dtype=x.dtype, pin_memory=True).copy_(x)
         hy = torch.empty(y.shape, dtype=y.dtype, pin_memory=True).copy_(y)
         hp = torch.empty(pre_in[0].shape, pin_memory=True).copy_(pre_in[0])
@@ -395,10 +395,10 @@ def run_ours(args, rank, world, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16/fp32",
         "data": "synthetic (seeded N(0,1) streams, N(0,0.02^2) fn; no checkpoint)",
-        "config": {"workload": "prefill seam: mhc_pre_delayed (fold) + mhc_post, T=16384, n=4, C=5120, "
+        "config": {"workload": f"prefill seam: mhc_pre_delayed (fold) + mhc_post, T={T}, n=4, C=5120, "
                                "20 Sinkhorn iters", "T": T, "n": N_STREAMS, "C": HIDDEN,
                    "sinkhorn_iters": ITERS, "fold": True, "per_rank_tokens": T,
-                   "l2": "inputs larger than L2 (x 671 MB vs 129 MB), no flush",
+                   "l2": f"inputs larger than L2 (x {T * 40960 / 1e6:.0f} MB vs 129 MB), no flush",
                    "parallelism": f"replicas x{world}"},
         "seam_hbm_frac": round(seam_frac, 4),
         "kernels": {k: {kk: round(vv, 3) if isinstance(vv, float) else vv for kk, vv in v.items()}
@@ -449,7 +449,7 @@ def run_reference(args, rank, world, local):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "prefill seam: mhc_pre_delayed (fold) + mhc_post, T=16384, n=4, C=5120, "
+        "config": {"workload": f"prefill seam: mhc_pre_delayed (fold) + mhc_post, T={T}, n=4, C=5120, "
                                "20 Sinkhorn iters", "T": T, "n": N_STREAMS, "C": HIDDEN,
                    "sinkhorn_iters": ITERS, "fold": True},
         "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
@@ -469,6 +469,9 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--skip-decode", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--tokens", type=int, default=T_PREFILL,
+                    help="tokens per rank (default 16384; smaller only for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

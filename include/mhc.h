@@ -105,9 +105,20 @@ mhc_status mhc_post(const uint16_t *x, const uint16_t *y, const float *comb,
 const char *mhc_status_string(mhc_status status);
 
 /*
+ * Device status of the current device: synchronises the device, then reads
+ * and clears the library's device-side status word.  MHC_ERR_TIMEOUT means a
+ * bounded wait inside a kernel gave up since the last call (that launch's
+ * outputs are garbage; the kernel still released its resources and returned).
+ * MHC_ERR_CUDA if the synchronisation or the read failed.
+ */
+mhc_status mhc_device_status(void);
+
+/*
  * Launch plan of mhc_pre_delayed for a shape, without launching (host only,
  * no device needed for the shape checks).  kernel: 1 = CUDA-core cluster
- * kernel; grid/cluster: CTAs launched and CTAs per cluster; tokens_per_tile.
+ * kernel (8-token tiles), 2 = tensor-core kernel (128-token tiles, used from
+ * 256 tokens on when C is a multiple of 128 and at most 5120); grid/cluster:
+ * CTAs launched and CTAs per cluster; tokens_per_tile.
  * Returns the status mhc_pre_delayed would return for the shape checks.
  * Any output pointer may be NULL.
  */

@@ -18,7 +18,7 @@ import threading
 
 import torch
 
-__all__ = ["pre_delayed", "post", "pre_plan", "library_path", "load_library",
+__all__ = ["pre_delayed", "post", "pre_plan", "device_status", "library_path", "load_library",
            "MhcError", "SINKHORN_ITERS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -63,6 +63,8 @@ def load_library():
         lib.mhc_pre_delayed_plan.restype = I
         lib.mhc_version.argtypes = []
         lib.mhc_version.restype = I
+        lib.mhc_device_status.argtypes = []
+        lib.mhc_device_status.restype = I
         _lib = lib
         return lib
 
@@ -161,6 +163,13 @@ def post(x: torch.Tensor, y: torch.Tensor, comb: torch.Tensor, post_gate: torch.
                       _dev_ptr(out, "out", torch.bfloat16, dev), _stream_ptr(stream, dev))
     _check("mhc_post", st)
     return out
+
+
+def device_status() -> int:
+    """Synchronise the current device and read-and-clear the library's device
+    status word (``mhc_device_status``): 0 = OK, 4 = a bounded in-kernel wait
+    timed out since the last check."""
+    return load_library().mhc_device_status()
 
 
 def pre_plan(T: int, n: int = 4, C: int = 5120) -> dict:

@@ -44,21 +44,24 @@ __device__ __forceinline__ void st_stream(uint4* p, const uint4& v) { __stcs(p, 
 // pre = sigmoid(l[0:4]), post = 2 sigmoid(l[4:8]); comb = Sinkhorn on the
 // 4x4 row-major comb logits l[8:24]: iteration 1 is the row softmax (max
 // subtracted per row) plus eps on every entry, then a column normalisation;
-// iterations 2..iters normalise rows then columns.
+// iterations 2..iters normalise rows then columns.  Normalisations multiply
+// by the hardware reciprocal of the sum (__fdividef): a relative error of a
+// few fp32 ulps per step, far inside the 2e-5 gate tolerance, and no IEEE
+// division subroutine on the latency-critical path.
 __device__ __forceinline__ void gates_and_comb(const float (&l)[kLogits], int iters, float eps,
                                                float (&pre)[4], float (&post)[4],
                                                float (&P)[16]) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        pre[i] = 1.0f / (1.0f + expf(-l[i]));
-        post[i] = 2.0f / (1.0f + expf(-l[4 + i]));
+        pre[i] = __fdividef(1.0f, 1.0f + expf(-l[i]));
+        post[i] = __fdividef(2.0f, 1.0f + expf(-l[4 + i]));
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         float mx = fmaxf(fmaxf(l[8 + 4 * i], l[9 + 4 * i]), fmaxf(l[10 + 4 * i], l[11 + 4 * i]));
         float e0 = expf(l[8 + 4 * i] - mx), e1 = expf(l[9 + 4 * i] - mx);
         float e2 = expf(l[10 + 4 * i] - mx), e3 = expf(l[11 + 4 * i] - mx);
-        float inv = 1.0f / (((e0 + e1) + e2) + e3);
+        float inv = __fdividef(1.0f, ((e0 + e1) + e2) + e3);
         P[4 * i + 0] = e0 * inv + eps;
         P[4 * i + 1] = e1 * inv + eps;
         P[4 * i + 2] = e2 * inv + eps;
@@ -68,14 +71,14 @@ __device__ __forceinline__ void gates_and_comb(const float (&l)[kLogits], int it
         if (it > 0) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                float inv = 1.0f / (((P[4 * i] + P[4 * i + 1]) + P[4 * i + 2]) + P[4 * i + 3]);
+                float inv = __fdividef(1.0f, ((P[4 * i] + P[4 * i + 1]) + P[4 * i + 2]) + P[4 * i + 3]);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) P[4 * i + j] *= inv;
             }
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            float inv = 1.0f / (((P[j] + P[4 + j]) + P[8 + j]) + P[12 + j]);
+            float inv = __fdividef(1.0f, ((P[j] + P[4 + j]) + P[8 + j]) + P[12 + j]);
 #pragma unroll
             for (int i = 0; i < 4; ++i) P[4 * i + j] *= inv;
         }

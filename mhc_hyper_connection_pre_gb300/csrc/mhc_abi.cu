@@ -19,18 +19,31 @@ cudaError_t launch_pre_cluster(const uint16_t* x, const float* pre_in, const flo
 int pre_cluster_tile_tokens();
 int pre_cluster_ctas();
 int pre_cluster_prepare(int C);
+bool pre_tc_supports(int C);
+int pre_tc_tile_tokens();
+int pre_tc_prepare();
+cudaError_t launch_pre_tc(const uint16_t* x, const float* pre_in, const float* fn, const float* bias,
+                          const float* alpha, const uint16_t* norm_w, int64_t T, int C, int iters,
+                          float rms_eps, float norm_eps, float sk_eps, float* pre_out, float* post_out,
+                          float* comb_out, uint16_t* layer_input, float* logits_out, cudaStream_t stream,
+                          int max_clusters);
+cudaError_t read_device_status(unsigned int* status);
 }  // namespace mhc
 
 namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxC = 6144;
+// From this many tokens on, the tensor-core kernel (128-token tiles) runs the
+// pre block; below it the CUDA-core kernel (8-token tiles) has lower latency.
+constexpr int64_t kTcMinTokens = 256;
 
 // Per-device cache: SM count, and the cluster kernel's set-up result per
 // hidden size (the kernel instance, and with it the occupancy, depends on C
 // only through the number of 8-column groups per CTA).
 struct DeviceInfo {
     int num_sms = 0;
+    int tc_clusters = -1;  // -1: not yet set up; 0: unavailable
     int cached_C[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     int cached_clusters[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 };
@@ -73,6 +86,14 @@ int max_clusters(int dev, int C) {
     return n;
 }
 
+int tc_clusters(int dev) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_dev[dev].tc_clusters < 0) g_dev[dev].tc_clusters = mhc::pre_tc_prepare();
+    return g_dev[dev].tc_clusters;
+}
+
+bool use_tc(int64_t T, int C) { return T >= kTcMinTokens && mhc::pre_tc_supports(C); }
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
@@ -103,21 +124,29 @@ const char* mhc_status_string(mhc_status s) {
     return "unknown mhc_status";
 }
 
-int mhc_version(void) { return (0 << 16) | 1; }
+int mhc_version(void) { return (0 << 16) | 2; }
+
+mhc_status mhc_device_status(void) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return MHC_ERR_CUDA;
+    unsigned int v = 0;
+    if (mhc::read_device_status(&v) != cudaSuccess) return MHC_ERR_CUDA;
+    return v ? MHC_ERR_TIMEOUT : MHC_OK;
+}
 
 mhc_status mhc_pre_delayed_plan(int64_t T, int n, int C, int* kernel, int* grid, int* cluster,
                                 int* tokens_per_tile) {
     mhc_status st = check_pre_shape(T, n, C, 1);
     if (st != MHC_OK) return st;
-    const int tt = mhc::pre_cluster_tile_tokens();
-    if (kernel) *kernel = 1;
+    const bool tc = use_tc(T, C);
+    const int tt = tc ? mhc::pre_tc_tile_tokens() : mhc::pre_cluster_tile_tokens();
+    if (kernel) *kernel = tc ? 2 : 1;
     if (cluster) *cluster = mhc::pre_cluster_ctas();
     if (tokens_per_tile) *tokens_per_tile = tt;
     if (grid) {
         *grid = 0;
         if (T > 0) {
             int dev = current_device();
-            int mc = dev >= 0 ? max_clusters(dev, C) : 0;
+            int mc = dev < 0 ? 0 : (tc ? tc_clusters(dev) : max_clusters(dev, C));
             int64_t tiles = (T + tt - 1) / tt;
             if (mc > 0) *grid = (int)((tiles < mc ? tiles : mc) * mhc::pre_cluster_ctas());
         }
@@ -155,6 +184,15 @@ mhc_status mhc_pre_delayed(const uint16_t* x, const float* pre_in, const float* 
     }
     int dev = current_device();
     if (dev < 0) return MHC_ERR_CUDA;
+    if (use_tc(T, C)) {
+        int tcc = tc_clusters(dev);
+        if (tcc > 0) {
+            cudaError_t e = mhc::launch_pre_tc(x, pre_in, fn, bias, alpha, norm_weight, T, C, sinkhorn_iters,
+                                               rms_eps, norm_eps, sinkhorn_eps, pre_out, post_out, comb_out,
+                                               layer_input, logits_out, static_cast<cudaStream_t>(stream), tcc);
+            return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA;
+        }
+    }
     int mc = max_clusters(dev, C);
     if (mc <= 0) return MHC_ERR_CUDA;
     cudaError_t e = mhc::launch_pre_cluster(

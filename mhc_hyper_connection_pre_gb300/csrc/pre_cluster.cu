@@ -244,24 +244,29 @@ __global__ void __launch_bounds__(kPreThreads, 1) pre_cluster_kernel(const PreAr
         }
         cluster.sync();  // A: every CTA's partials are visible cluster-wide
 
-        // ---- 3. finalize token t0 + rank in CTA rank (rank < 8), warp 0
+        // ---- 3. finalize token t0 + rank in CTA rank (rank < 8), warp 0: the fold
+        //         scale is pushed first (it gates every CTA's stores), the gates and
+        //         the Sinkhorn comb follow while the other CTAs wait at barrier B
         if (rank < kTileTokens && warp == 0) {
             const int64_t t = t0 + rank;
             float v = 0.f;
             if (lane < kPartStride) {
-#pragma unroll 4
-                for (int s = 0; s < kClusterCtas; ++s) {
-                    const float* rp = cluster.map_shared_rank(part, s);
-                    v += rp[rank * kPartStride + lane];
-                }
+                float pv[kClusterCtas];
+#pragma unroll
+                for (int s = 0; s < kClusterCtas; ++s)
+                    pv[s] = cluster.map_shared_rank(part, s)[rank * kPartStride + lane];
+#pragma unroll
+                for (int s = 0; s < kClusterCtas; ++s) v += pv[s];
+            }
+            const float sh = __shfl_sync(0xffffffffu, v, 25);
+            if (fold && lane < kClusterCtas) {
+                float* rs = cluster.map_shared_rank(scale, lane);
+                rs[rank] = 1.0f / sqrtf(sh / (float)C + a.norm_eps);
             }
             float l[kLogits];
 #pragma unroll
             for (int m = 0; m < kLogits; ++m) l[m] = __shfl_sync(0xffffffffu, v, m);
             const float sx = __shfl_sync(0xffffffffu, v, 24);
-            const float sh = __shfl_sync(0xffffffffu, v, 25);
-            float s_fold = 1.f;
-            if (fold) s_fold = 1.0f / sqrtf(sh / (float)C + a.norm_eps);
             if (lane == 0 && t < a.T) {
                 const float r = 1.0f / sqrtf(sx / (float)K + a.rms_eps);
                 const float al0 = __ldg(a.alpha), al1 = __ldg(a.alpha + 1), al2 = __ldg(a.alpha + 2);
@@ -282,10 +287,6 @@ __global__ void __launch_bounds__(kPreThreads, 1) pre_cluster_kernel(const PreAr
                 float4* co = reinterpret_cast<float4*>(a.comb_out + t * 16);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) co[i] = make_float4(P[4 * i], P[4 * i + 1], P[4 * i + 2], P[4 * i + 3]);
-            }
-            if (fold && lane < kClusterCtas) {
-                float* rs = cluster.map_shared_rank(scale, lane);
-                rs[rank] = s_fold;
             }
         }
         cluster.sync();  // B: fold scales are in place; partial buffers may be reused

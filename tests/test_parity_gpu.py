@@ -93,6 +93,33 @@ def test_token_and_hidden_sweep(T, C, fold):
     _check_pre(g, o, xb, d, fold=fold)
 
 
+@pytest.mark.parametrize("T,C,fold", [
+    (256, 5120, True), (257, 5120, False), (300, 128, True), (512, 4096, True),
+    (640, 2048, False), (1383, 5120, True), (4096, 5120, False),
+])
+def test_tensor_core_path(T, C, fold):
+    """Shapes that take the tensor-core kernel (128-token tiles, fn split in
+    three bf16 planes): ragged last tiles, one 8-column group per CTA
+    (C = 128), other slice widths, more tiles than co-resident clusters."""
+    assert mhc.pre_plan(T, 4, C)["kernel"] == 2
+    d = seam_inputs(T, C=C, seed=700 + T, fold=fold)
+    g = _gpu_pre(_to_dev(d))
+    assert mhc.device_status() == 0
+    o, xb = _oracle_pre(d)
+    _check_pre(g, o, xb, d, fold=fold)
+
+
+def test_kernel_choice():
+    assert mhc.pre_plan(1)["kernel"] == 1
+    assert mhc.pre_plan(255)["kernel"] == 1
+    assert mhc.pre_plan(256)["kernel"] == 2
+    assert mhc.pre_plan(16384)["kernel"] == 2
+    assert mhc.pre_plan(4096, 4, 6144)["kernel"] == 1      # slice too wide for the TMEM park
+    assert mhc.pre_plan(4096, 4, 1000)["kernel"] == 1      # C not a multiple of 128
+    p = mhc.pre_plan(16384)
+    assert p["cluster"] == 16 and p["tokens_per_tile"] == 128 and p["grid"] % 16 == 0
+
+
 def test_alpha_and_sinkhorn_parameters():
     """Non-unit alphas, another iteration count and eps reach the kernel."""
     d = seam_inputs(24, seed=5, fold=True)
@@ -134,11 +161,13 @@ def test_staggering_invariance():
                     "non-delayed collapse")
 
 
-def test_deterministic():
-    d = _to_dev(seam_inputs(300, seed=8, fold=True))
+@pytest.mark.parametrize("T", [100, 3000])
+def test_deterministic(T):
+    d = _to_dev(seam_inputs(T, seed=8, fold=True))
     a, b = _gpu_pre(d), _gpu_pre(d)
     for k in a:
         assert torch.equal(a[k], b[k]), k
+    assert mhc.device_status() == 0
 
 
 def test_zero_tokens():
