@@ -59,6 +59,24 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """Maximum of a per-rank scalar over the default process group (the
+    timed region's slowest rank); the value itself when not distributed."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_throughput(tokens_per_rank: int, steps: int, world: int, elapsed_ms_max: float) -> float:
+    """Whole-job tokens/s: every rank processes its own batch each step; the
+    job time is the slowest rank's."""
+    return world * tokens_per_rank * steps / (elapsed_ms_max / 1e3)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -240,16 +258,11 @@ def run_ours(args, rank, world, local):
             step(i, evs[i])
         t_end.record(stream)
         barrier()
-    elapsed_ms = t_begin.elapsed_time(t_end)
+    elapsed_ms = max_over_ranks(t_begin.elapsed_time(t_end), dev)
     pre_ms = [e[0].elapsed_time(e[1]) for e in evs]
     post_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
     ms_per_step = elapsed_ms / args.steps
-    tokens_per_s = world * T * args.steps / (elapsed_ms / 1e3)
+    tokens_per_s = weak_scaling_throughput(T, args.steps, world, elapsed_ms)
 
     pre_avg = sum(pre_ms) / len(pre_ms)
     post_avg = sum(post_ms) / len(post_ms)
@@ -296,15 +309,10 @@ def run_ours(args, rank, world, local):
             e2e_step()
         b.record(stream)
         barrier()
-        e_ms = a.elapsed_time(b)
-        if world > 1:
-            import torch.distributed as dist
-            tt = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e_ms = float(tt.item())
+        e_ms = max_over_ranks(a.elapsed_time(b), dev)
         h2d = x.numel() * 2 + y.numel() * 2 + pre_in[0].numel() * 4
         d2h = x_new.numel() * 2 + pre_in[0].numel() * 4
-        e2e = {"value": round(world * T * ek / (e_ms / 1e3), 1), "unit": "tokens/s",
+        e2e = {"value": round(weak_scaling_throughput(T, ek, world, e_ms), 1), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": round(e_ms / ek, 4)}
         del hx, hy, hp, ho, hpo, dx, dy, dp

@@ -47,6 +47,7 @@ namespace tc {
 constexpr int kCtas = 16;                         // CTAs per cluster = column slices
 constexpr int kTile = 128;                        // tokens per tile = MMA M
 constexpr int kStages = 4;                        // TMA ring depth
+constexpr int kPrefetch = 16;                     // stages prefetched into L2 ahead of the ring
 constexpr int kStageBytes = 4 * kTile * 16;       // 4 streams x 128 tokens x 8 bf16
 constexpr int kMaxGroups = 40;                    // 8-column groups per CTA (C <= 5120)
 constexpr int kWBlock = 2 * 9 * 128;              // per (group, k-step): 2 K-chunks x 9 row-groups
@@ -179,9 +180,21 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
     if (warp == 0) {
         // ================================================== TMA producer
         if (lane == 0) {
+            // L2 prefetch of the first kPrefetch stages; afterwards each issued
+            // stage prefetches the one kPrefetch later (the shared-memory ring
+            // holds only 32 KB, the L2 keeps HBM requests in flight).
+            auto prefetch = [&](uint32_t q) {
+                const int tile_q = cid + (int)(q / ngroups) * ncl;
+                if (tile_q >= a.ntiles) return;
+                const int grp_q = (int)(q % ngroups);
+#pragma unroll
+                for (int st = 0; st < 4; ++st) tma_prefetch_3d(&xmap, c0 + 8 * grp_q, st, tile_q * kTile);
+            };
+            for (uint32_t q = 0; q < (uint32_t)kPrefetch; ++q) prefetch(q);
             uint32_t g = 0;
             for (int tile = cid; tile < a.ntiles && !*abort; tile += ncl) {
                 for (int grp = 0; grp < ngroups; ++grp, ++g) {
+                    prefetch(g + kPrefetch);
                     const int s = g % kStages;
                     const uint32_t ph = (g / kStages) & 1;
                     mbar_wait(&empty[s], ph ^ 1, abort);
@@ -236,6 +249,25 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
         const int fin = trow / kFinTok, slot = trow % kFinTok;
         const uint32_t inbox_dst = mapa(smem_u32(inbox + ((int)rank * kFinTok + slot) * kPart), fin);
         const uint32_t inbox_bar = mapa(smem_u32(inbox_full), fin);
+        // The folded store of tile i is deferred into tile i+1's stage loop:
+        // at group grp the thread first reads back tile i's parked h for that
+        // group, scales, rounds and stores it, then parks tile i+1's new h in
+        // the same TMEM columns.  The last tile is flushed after the loop.
+        bool have_prev = false, valid_prev = false;
+        int64_t t_prev = 0;
+        float sc_prev = 1.f;
+        auto store_folded = [&](int grp) {
+            uint32_t r[8];
+            tmem_ld8(tl + kHCol + 8 * grp, r);
+            tmem_wait_ld();
+            if (valid_prev) {
+                float wf[8], o[8];
+                unpack8(__ldg(reinterpret_cast<const uint4*>(a.norm_w + c0 + 8 * grp)), wf);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = __fmul_rn(__fmul_rn(__uint_as_float(r[e]), sc_prev), wf[e]);
+                st_stream(reinterpret_cast<uint4*>(a.layer_input + t_prev * C + c0 + 8 * grp), pack8(o));
+            }
+        };
         uint32_t g = 0;
         int it = 0;
         for (int tile = cid; tile < a.ntiles; tile += ncl, ++it) {
@@ -269,6 +301,7 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                     for (int st = 0; st < 4; ++st) sx = fmaf(xv[st][e], xv[st][e], sx);
                 }
                 if (fold) {
+                    if (have_prev) store_folded(grp);
                     uint32_t hb[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) hb[e] = __float_as_uint(h[e]);
@@ -304,24 +337,16 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
             for (int k = 0; k < kPart; k += 2) st_cluster_v2(inbox_dst + 4 * k, part[k], part[k + 1]);
             mbar_arrive_remote(inbox_bar);
 
-            // fold scale of this tile from every finalizer, then the folded store
+            // this tile's fold scale from the finalizers (also: every finalizer
+            // has read its inbox, so the next tile's partials may be pushed)
             mbar_wait<true>(scale_full, it & 1, abort);
-            if (fold) {
-                const float sc = scale[trow];
-                for (int grp = 0; grp < ngroups; ++grp) {
-                    uint32_t r[8];
-                    tmem_ld8(tl + kHCol + 8 * grp, r);
-                    tmem_wait_ld();
-                    if (valid) {
-                        float wf[8], o[8];
-                        unpack8(__ldg(reinterpret_cast<const uint4*>(a.norm_w + c0 + 8 * grp)), wf);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) o[e] = __fmul_rn(__fmul_rn(__uint_as_float(r[e]), sc), wf[e]);
-                        st_stream(reinterpret_cast<uint4*>(a.layer_input + t * C + c0 + 8 * grp), pack8(o));
-                    }
-                }
-            }
+            sc_prev = scale[trow];
+            t_prev = t;
+            valid_prev = valid;
+            have_prev = true;
         }
+        if (fold && have_prev)
+            for (int grp = 0; grp < ngroups; ++grp) store_folded(grp);
     } else {
         // ================================================== finalizer
         const uint32_t scale_dst = mapa(smem_u32(scale + (int)rank * kFinTok), lane & (kCtas - 1));
