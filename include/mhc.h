@@ -71,9 +71,16 @@ typedef enum mhc_status {
  *  rms_eps, norm_eps, sinkhorn_eps  >= 0 (the pages' workload: 1e-6 each)
  *  pre_out [T,n], post_out [T,n], comb_out [T,n,n] fp32; layer_input [T,C] bf16
  *  logits_out   [T, 2n+n^2] fp32 or NULL (debug / parity layer)
+ *  workspace    device scratch of at least mhc_pre_workspace_bytes(T, n, C)
+ *               bytes, 256-byte aligned, owned by the caller; NULL is allowed
+ *               when that size is 0.  Its contents on entry do not matter
+ *               (the call writes everything it later reads); it may be reused
+ *               by consecutive calls on one stream, but two calls that can
+ *               run concurrently need separate workspaces.
  *  stream       cudaStream_t
- * Outputs must not overlap any input (pre_out must not alias pre_in:
- * ping-pong two buffers across seams).  Errors: MHC_ERR_INVALID_ARGUMENT,
+ * Outputs must not overlap any input or the workspace (pre_out must not
+ * alias pre_in: ping-pong two buffers across seams).  Errors:
+ * MHC_ERR_INVALID_ARGUMENT (also: workspace too small or misaligned),
  * MHC_ERR_UNSUPPORTED, MHC_ERR_CUDA.  One kernel launch per call.
  */
 mhc_status mhc_pre_delayed(const uint16_t *x, const float *pre_in, const float *fn,
@@ -82,21 +89,18 @@ mhc_status mhc_pre_delayed(const uint16_t *x, const float *pre_in, const float *
                            int sinkhorn_iters, float rms_eps, float norm_eps,
                            float sinkhorn_eps, float *pre_out, float *post_out,
                            float *comb_out, uint16_t *layer_input, float *logits_out,
-                           void *stream);
+                           void *workspace, size_t workspace_bytes, void *stream);
 
 /*
- * mhc_post -- the mHC post block ([A] "Result": the mhc_post call sites go
- * through MHCPostOp; the post mixes the residual streams through comb and
- * adds the post-gated sublayer output):
- *   x_new[t][j][c] = bf16( sum_i comb[t][i][j] * x[t][i][c] + post[t][j] * y[t][c] )
- * accumulated in fp32, rounded once.
- *  x     [T, n, C] bf16;  y [T, C] bf16 (sublayer output)
- *  comb  [T, n, n] fp32;  post [T, n] fp32 (from mhc_pre_delayed)
- *  x_new [T, n, C] bf16; may be exactly x (in place); must not otherwise
- *        overlap an input.
- *  n == 4; C multiple of 8; T >= 0.  Errors as mhc_pre_delayed.
- *  One kernel launch per call.
+ * Workspace bytes mhc_pre_delayed needs for a shape on the current device
+ * (host only).  0 when the shape runs on the CUDA-core kernel (fewer than 256
+ * tokens, or a hidden size the tensor-core kernel does not take); otherwise
+ * the per-call copy of the fn slices split into three bf16 planes, one copy
+ * per co-resident 16-CTA cluster (about 20 MB at C = 5120 on a GB300).
+ * Returns 0 as well for shapes mhc_pre_delayed rejects.
  */
+size_t mhc_pre_workspace_bytes(int64_t T, int n, int C);
+
 mhc_status mhc_post(const uint16_t *x, const uint16_t *y, const float *comb,
                     const float *post, int64_t T, int n, int C, uint16_t *x_new,
                     void *stream);
@@ -117,7 +121,7 @@ mhc_status mhc_device_status(void);
  * Launch plan of mhc_pre_delayed for a shape, without launching (host only,
  * no device needed for the shape checks).  kernel: 1 = CUDA-core cluster
  * kernel (8-token tiles), 2 = tensor-core kernel (128-token tiles, used from
- * 256 tokens on when C is a multiple of 128 and at most 5120); grid/cluster:
+ * 256 tokens on when C is a multiple of 256 and at most 5120); grid/cluster:
  * CTAs launched and CTAs per cluster; tokens_per_tile.
  * Returns the status mhc_pre_delayed would return for the shape checks.
  * Any output pointer may be NULL.

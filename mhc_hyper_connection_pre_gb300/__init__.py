@@ -18,8 +18,8 @@ import threading
 
 import torch
 
-__all__ = ["pre_delayed", "post", "pre_plan", "device_status", "library_path", "load_library",
-           "MhcError", "SINKHORN_ITERS"]
+__all__ = ["pre_delayed", "post", "pre_plan", "device_status", "workspace_for", "library_path",
+           "load_library", "MhcError", "SINKHORN_ITERS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "_build", "libmhc.so")
@@ -29,6 +29,7 @@ _STATUS = {0: "MHC_OK", 1: "MHC_ERR_INVALID_ARGUMENT", 2: "MHC_ERR_UNSUPPORTED",
 
 _lock = threading.Lock()
 _lib = None
+_workspaces: dict = {}
 
 
 class MhcError(RuntimeError):
@@ -53,8 +54,11 @@ def load_library():
                 "`python -m mhc_hyper_connection_pre_gb300.build` (no fallback exists)")
         lib = ctypes.CDLL(_LIB_PATH)
         P, I64, I, F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
-        lib.mhc_pre_delayed.argtypes = [P, P, P, P, P, P, I64, I, I, I, F, F, F, P, P, P, P, P, P]
+        lib.mhc_pre_delayed.argtypes = [P, P, P, P, P, P, I64, I, I, I, F, F, F, P, P, P, P, P,
+                                         P, ctypes.c_size_t, P]
         lib.mhc_pre_delayed.restype = I
+        lib.mhc_pre_workspace_bytes.argtypes = [I64, I, I]
+        lib.mhc_pre_workspace_bytes.restype = ctypes.c_size_t
         lib.mhc_post.argtypes = [P, P, P, P, I64, I, I, P, P]
         lib.mhc_post.restype = I
         lib.mhc_status_string.argtypes = [I]
@@ -89,6 +93,22 @@ def _dev_ptr(t: torch.Tensor | None, name: str, dtype: torch.dtype, device) -> i
     return t.data_ptr()
 
 
+def workspace_for(T: int, n: int, C: int, device) -> torch.Tensor | None:
+    """A cached device workspace big enough for ``mhc_pre_delayed`` at this
+    shape (None when the shape needs none).  One buffer per device, grown on
+    demand; calls that may run concurrently on different streams must pass
+    their own ``workspace=``."""
+    need = int(load_library().mhc_pre_workspace_bytes(T, n, C))
+    if need == 0:
+        return None
+    key = torch.device(device).index if torch.device(device).index is not None else torch.cuda.current_device()
+    buf = _workspaces.get(key)
+    if buf is None or buf.numel() < need:
+        buf = torch.empty(need, dtype=torch.uint8, device=torch.device("cuda", key))
+        _workspaces[key] = buf
+    return buf
+
+
 def _stream_ptr(stream, device) -> int:
     s = stream if stream is not None else torch.cuda.current_stream(device)
     return s.cuda_stream
@@ -98,13 +118,16 @@ def pre_delayed(x: torch.Tensor, pre_in: torch.Tensor, fn: torch.Tensor, bias: t
                 alpha: torch.Tensor, norm_weight: torch.Tensor | None = None, *,
                 sinkhorn_iters: int = SINKHORN_ITERS, rms_eps: float = 1e-6,
                 norm_eps: float = 1e-6, sinkhorn_eps: float = 1e-6, out: dict | None = None,
-                return_logits: bool = False, stream=None) -> dict:
+                return_logits: bool = False, workspace: torch.Tensor | None = None,
+                stream=None) -> dict:
     """Delayed mHC pre block (``mhc_pre_delayed`` in include/mhc.h).
 
     x bf16 [T, 4, C]; pre_in fp32 [T, 4] (previous seam's pre-mix);
     fn fp32 [24, 4C]; bias fp32 [24]; alpha fp32 [3]; norm_weight bf16 [C]
     or None.  Returns {"pre", "post", "comb", "layer_input"[, "logits"]}
     (``out`` may supply preallocated tensors under the same keys).
+    ``workspace``: uint8 device buffer of at least ``mhc_pre_workspace_bytes``;
+    by default a cached per-device buffer is used.
     """
     lib = load_library()
     if x.dim() != 3:
@@ -137,8 +160,14 @@ def pre_delayed(x: torch.Tensor, pre_in: torch.Tensor, fn: torch.Tensor, bias: t
             _dev_ptr(o["comb"], "comb", torch.float32, dev),
             _dev_ptr(o["layer_input"], "layer_input", torch.bfloat16, dev),
             _dev_ptr(o.get("logits"), "logits", torch.float32, dev)]
+    if workspace is None:
+        workspace = workspace_for(T, n, C, dev)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr = _dev_ptr(workspace, "workspace", torch.uint8, dev)
+        ws_bytes = workspace.numel()
     st = lib.mhc_pre_delayed(*args, T, n, C, int(sinkhorn_iters), float(rms_eps), float(norm_eps),
-                             float(sinkhorn_eps), *outs, _stream_ptr(stream, dev))
+                             float(sinkhorn_eps), *outs, ws_ptr, ws_bytes, _stream_ptr(stream, dev))
     _check("mhc_pre_delayed", st)
     return o
 

@@ -22,11 +22,12 @@ int pre_cluster_prepare(int C);
 bool pre_tc_supports(int C);
 int pre_tc_tile_tokens();
 int pre_tc_prepare();
+size_t pre_tc_workspace_bytes(int64_t T, int C, int max_clusters);
 cudaError_t launch_pre_tc(const uint16_t* x, const float* pre_in, const float* fn, const float* bias,
                           const float* alpha, const uint16_t* norm_w, int64_t T, int C, int iters,
                           float rms_eps, float norm_eps, float sk_eps, float* pre_out, float* post_out,
-                          float* comb_out, uint16_t* layer_input, float* logits_out, cudaStream_t stream,
-                          int max_clusters);
+                          float* comb_out, uint16_t* layer_input, float* logits_out, void* workspace,
+                          cudaStream_t stream, int max_clusters);
 cudaError_t read_device_status(unsigned int* status);
 }  // namespace mhc
 
@@ -154,12 +155,20 @@ mhc_status mhc_pre_delayed_plan(int64_t T, int n, int C, int* kernel, int* grid,
     return MHC_OK;
 }
 
+size_t mhc_pre_workspace_bytes(int64_t T, int n, int C) {
+    if (check_pre_shape(T, n, C, 1) != MHC_OK || T == 0 || !use_tc(T, C)) return 0;
+    int dev = current_device();
+    if (dev < 0) return 0;
+    int tcc = tc_clusters(dev);
+    return tcc > 0 ? mhc::pre_tc_workspace_bytes(T, C, tcc) : 0;
+}
+
 mhc_status mhc_pre_delayed(const uint16_t* x, const float* pre_in, const float* fn,
                            const float* bias, const float* alpha, const uint16_t* norm_weight,
                            int64_t T, int n, int C, int sinkhorn_iters, float rms_eps,
                            float norm_eps, float sinkhorn_eps, float* pre_out, float* post_out,
                            float* comb_out, uint16_t* layer_input, float* logits_out,
-                           void* stream) {
+                           void* workspace, size_t workspace_bytes, void* stream) {
     mhc_status st = check_pre_shape(T, n, C, sinkhorn_iters);
     if (st != MHC_OK) return st;
     if (!(rms_eps >= 0.f) || !(norm_eps >= 0.f) || !(sinkhorn_eps >= 0.f)) return MHC_ERR_INVALID_ARGUMENT;
@@ -175,7 +184,8 @@ mhc_status mhc_pre_delayed(const uint16_t* x, const float* pre_in, const float* 
     const size_t fnb = (size_t)M * n * C * 4, bb = (size_t)M * 4, ab = 12, nwb = (size_t)C * 2;
     struct R { const void* p; size_t n; };
     const R ins[] = {{x, xb}, {pre_in, pb}, {fn, fnb}, {bias, bb}, {alpha, ab}, {norm_weight, nwb}};
-    const R outs[] = {{pre_out, pb}, {post_out, pb}, {comb_out, cb}, {layer_input, lib}, {logits_out, lob}};
+    const R outs[] = {{pre_out, pb}, {post_out, pb}, {comb_out, cb}, {layer_input, lib}, {logits_out, lob},
+                      {workspace, workspace_bytes}};
     for (const R& o : outs) {
         for (const R& i : ins)
             if (overlaps(o.p, o.n, i.p, i.n)) return MHC_ERR_INVALID_ARGUMENT;
@@ -187,9 +197,13 @@ mhc_status mhc_pre_delayed(const uint16_t* x, const float* pre_in, const float* 
     if (use_tc(T, C)) {
         int tcc = tc_clusters(dev);
         if (tcc > 0) {
+            const size_t need = mhc::pre_tc_workspace_bytes(T, C, tcc);
+            if (workspace_bytes < need || (need && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))))
+                return MHC_ERR_INVALID_ARGUMENT;
             cudaError_t e = mhc::launch_pre_tc(x, pre_in, fn, bias, alpha, norm_weight, T, C, sinkhorn_iters,
                                                rms_eps, norm_eps, sinkhorn_eps, pre_out, post_out, comb_out,
-                                               layer_input, logits_out, static_cast<cudaStream_t>(stream), tcc);
+                                               layer_input, logits_out, workspace,
+                                               static_cast<cudaStream_t>(stream), tcc);
             return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA;
         }
     }

@@ -16,25 +16,29 @@
 // added in fp32 in the epilogue.
 //
 // Decomposition: a cluster of 16 CTAs owns a tile of 128 tokens (the MMA's
-// M); CTA r owns C/16 columns of all four streams, holds the matching
-// K-slice of the three fn planes in shared memory for the whole persistent
-// launch (184 KB at C = 5120), and walks its slice in stages of
-// 8 columns x 4 streams x 128 tokens (8 KB, one 3-D TMA box per stream).
-// Warp roles (7 warps):
-//   warp 0  TMA producer      -- 4-stage ring, mbarrier full/empty;
-//   warp 1  MMA issuer        -- 2 x tcgen05.mma (M128 N80 K16) per stage into
-//                                a double-buffered fp32 accumulator in TMEM;
-//   warps 2-5  token rows     -- thread = token: collapse h (fp32, fixed order),
-//                                sum x^2, sum h^2; h parked in TMEM columns
-//                                while the fold scale is unknown; at the tile
-//                                end read the 72 accumulator columns, add the
-//                                planes, push 26 partials to the token's
-//                                finalizer CTA over DSMEM; after the scale
-//                                arrives, scale h, round once, store;
-//   warp 6  finalizer         -- for its 8 tokens of the tile: sum the 16 CTAs'
-//                                partials in rank order, push the fold scale
-//                                to all 16 CTAs, then logits, gates and the
-//                                Sinkhorn comb in registers, written to HBM.
+// M); CTA r owns C/16 columns of all four streams and walks its slice in
+// stages of 16 columns x 4 streams x 128 tokens (16 KB: one 3-D TMA box of
+// 128 tokens x 32 bytes per stream, 32-byte swizzle, so every DRAM sector
+// fetched is used whole).  At the start of the call each CTA writes its
+// K-slice of the three fn planes (184 KB at C = 5120), already in the MMA's
+// operand layout, to its region of the caller's workspace; every stage then
+// brings the matching 9 KB block with one bulk copy (L2 evict-last) next to
+// the x boxes (L2 evict-first).  Keeping fn resident in shared memory instead
+// would leave room for only two x stages (32 KB in flight per SM); this
+// 8-slot ring keeps 128 KB of x in flight per SM.  Warp roles (11 warps):
+//   warp 0     TMA producer;
+//   warp 1     MMA issuer: 4 x tcgen05.mma (M128 N80 K16, one per stream) per
+//              stage into a double-buffered fp32 accumulator in TMEM;
+//   warps 2-9  token rows, two groups of four taking alternate stages (thread
+//              = token, TMEM lane quadrant = warp % 4): collapse h (fp32,
+//              fixed order), sum x^2, sum h^2; h parked in TMEM until the fold
+//              scale is known and stored, folded, during the next tile's
+//              stages.  At the tile end group 0 adds group 1's sums, reads the
+//              72 accumulator columns, adds the planes and pushes 26 partials
+//              to the token's finalizer CTA over DSMEM;
+//   warp 10    finalizer: for its 8 tokens of the tile sums the 16 CTAs'
+//              partials in rank order, pushes the fold scale to all 16 CTAs,
+//              then logits, gates and the Sinkhorn comb in registers.
 // No global scratch; every wait is bounded (see sm100.cuh).
 #include "common.cuh"
 #include "sm100.cuh"
@@ -46,28 +50,38 @@ namespace tc {
 
 constexpr int kCtas = 16;                         // CTAs per cluster = column slices
 constexpr int kTile = 128;                        // tokens per tile = MMA M
-constexpr int kStages = 4;                        // TMA ring depth
-constexpr int kPrefetch = 16;                     // stages prefetched into L2 ahead of the ring
-constexpr int kStageBytes = 4 * kTile * 16;       // 4 streams x 128 tokens x 8 bf16
-constexpr int kMaxGroups = 40;                    // 8-column groups per CTA (C <= 5120)
-constexpr int kWBlock = 2 * 9 * 128;              // per (group, k-step): 2 K-chunks x 9 row-groups
-constexpr int kWBytes = kMaxGroups * 2 * kWBlock; // 184,320
+constexpr int kStages = 8;                        // shared-memory ring depth
+static_assert(kStages % 2 == 0, "each ring slot must always belong to the same token-row group");
+constexpr int kCols = 16;                         // columns per stream per stage
+constexpr int kBoxBytes = kTile * kCols * 2;      // 4 KB: one stream of one stage
+constexpr int kXBytes = 4 * kBoxBytes;            // 16 KB of x per stage
+constexpr int kMaxGroups = 20;                    // stages per tile (C <= 5120)
+constexpr int kWBlock = 9 * 256;                  // per (stage, stream): 9 row-atoms of 8 x 32 B
+constexpr int kWStage = 4 * kWBlock;              // 9 KB of fn planes per stage
+constexpr int kSlotBytes = kXBytes + kWStage;     // 25 KB ring slot: x boxes, then fn blocks
 constexpr int kN = 80;                            // MMA N: 72 plane rows + 8 ignored
 constexpr int kPart = 26;                         // 24 dots, sum x^2, sum h^2
 constexpr int kFinTok = kTile / kCtas;            // tokens finalized per CTA per tile
-constexpr int kThreads = 224;
+constexpr int kRowWarps = 8;
+constexpr int kThreads = 32 * (2 + kRowWarps + 1);
+constexpr int kFinWarp = 2 + kRowWarps;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kDCol0 = 0, kDCol1 = 96, kHCol = 192;  // accumulators, parked h
+constexpr uint32_t kDCol0 = 0, kDCol1 = 96, kHCol = 192;  // accumulators, parked h (320 columns)
+constexpr uint32_t kSumCol = 80;                           // group 1's sum x^2, sum h^2 (free columns)
 
-constexpr int kOffStages = 0;
-constexpr int kOffW = kOffStages + kStages * kStageBytes;
-constexpr int kOffInbox = kOffW + kWBytes;                      // [16 src][8 tok][26]
-constexpr int kOffScale = kOffInbox + kCtas * kFinTok * kPart * 4;  // [128]
-constexpr int kOffFinred = kOffScale + kTile * 4;               // [8][26]
-constexpr int kOffBars = kOffFinred + kFinTok * kPart * 4;
-constexpr int kNumBars = 2 * kStages + 2 + 2 + 1 + 1 + 1;       // full, empty, dfull, dempty, inbox, scale, drain
-constexpr int kOffMisc = kOffBars + kNumBars * 8;               // tmem base, abort flag
+constexpr int kOffStages = 0;                                        // 1 KB aligned
+// The last slot's ignored 10th B-operand atom reads 256 B past the ring: the
+// inbox follows it, so that read stays inside shared memory.
+constexpr int kOffInbox = kOffStages + kStages * kSlotBytes;         // [16 src][8 tok][26]
+constexpr int kOffScale = kOffInbox + kCtas * kFinTok * kPart * 4;   // [128]
+constexpr int kOffNormW = kOffScale + kTile * 4;                     // [C/16] bf16
+constexpr int kOffBars = kOffNormW + kMaxGroups * kCols * 2;      // after the norm_w slice
+constexpr int kNumBars = 2 * kStages + 2 + 2 + 1 + 1 + 1;           // full, empty, dfull, dempty, inbox, scale, drain
+constexpr int kOffMisc = kOffBars + kNumBars * 8;                    // tmem base, abort flag
 constexpr int kSmemBytes = kOffMisc + 16;
+static_assert(kOffNormW + kMaxGroups * kCols * 2 <= kOffBars, "norm_w slice overlaps the barriers");
+static_assert(kOffBars % 8 == 0, "mbarriers need 8-byte alignment");
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Args {
     const uint16_t* x;
@@ -85,14 +99,16 @@ struct Args {
     float* comb_out;
     uint16_t* layer_input;
     float* logits_out;
+    unsigned char* ws;  // fn planes, one region of ngroups x 9 KB per (cluster, rank)
     int ntiles;
 };
 
-// Byte offset of the 16-byte row (8 k-values) of plane row n for 8-column
-// group g, stream s, in the K-major no-swizzle B layout:
-// [group][k-step j = s/2][K-chunk kk = s%2][row-group n/8][row n%8][16 B].
-__device__ __forceinline__ int w_off(int g, int s, int n) {
-    return ((((g * 2 + (s >> 1)) * 2 + (s & 1)) * 9 + (n >> 3)) * 8 + (n & 7)) * 16;
+// Byte offset, inside a CTA's fn-plane region, of 16-byte chunk c (k =
+// 8c..8c+7 of the stage's 16 columns) of plane row n for stage g and stream
+// s: blocks [g][s] of 9 atoms x 256 B, row n in atom n/8, 32-byte swizzle in
+// the atom (the layout the MMA reads once the block sits in a ring slot).
+__device__ __forceinline__ int w_off(int g, int s, int n, int c) {
+    return (g * 4 + s) * kWBlock + (n >> 3) * 256 + sw32_off(n & 7, c);
 }
 
 __device__ __forceinline__ uint16_t bf16_bits_rn(float v) {
@@ -104,10 +120,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* stages = smem + kOffStages;
-    unsigned char* wsm = smem + kOffW;
     float* inbox = reinterpret_cast<float*>(smem + kOffInbox);
     float* scale = reinterpret_cast<float*>(smem + kOffScale);
-    float* finred = reinterpret_cast<float*>(smem + kOffFinred);
+    uint16_t* nw_s = reinterpret_cast<uint16_t*>(smem + kOffNormW);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
     uint64_t* full = bars;
     uint64_t* empty = bars + kStages;
@@ -122,17 +137,17 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_ctarank();
     const int cid = (int)cluster_id_x(), ncl = (int)ncluster_x();
-    const int C = a.C, K = 4 * C, slice = C / kCtas, ngroups = slice / 8, c0 = (int)rank * slice;
+    const int C = a.C, K = 4 * C, slice = C / kCtas, ngroups = slice / kCols, c0 = (int)rank * slice;
     const bool fold = a.norm_w != nullptr;
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 5);     // MMA commit + 4 token-row warps
+            mbar_init(&empty[s], 5);     // MMA commit + the stage's 4 token-row warps
         }
         for (int d = 0; d < 2; ++d) {
             mbar_init(&dfull[d], 1);
-            mbar_init(&dempty[d], 4);
+            mbar_init(&dempty[d], 4);    // group 0's 4 warps
         }
         mbar_init(inbox_full, kTile);    // one arrival per (source CTA, token) pair
         mbar_init(scale_full, kCtas);    // one arrival per finalizer CTA
@@ -142,35 +157,44 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
     }
     if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
 
-    // ---- fn K-slice -> three bf16 planes in shared memory (exact split)
+    // ---- fn K-slice -> three bf16 planes (exact split) in the operand layout,
+    //      written to this CTA's workspace region; read back stage by stage.
+    unsigned char* wreg = a.ws + (size_t)(cid * kCtas + (int)rank) * ngroups * kWStage;
     for (int idx = tid; idx < 24 * 4 * ngroups; idx += kThreads) {
-        const int g = idx % ngroups, rest = idx / ngroups, s = rest & 3, m = rest >> 2;
-        const float4* src = reinterpret_cast<const float4*>(a.fn + (int64_t)m * K + (int64_t)s * C + c0 + 8 * g);
-        const float4 u = __ldg(src), v = __ldg(src + 1);
-        const float w[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
-        uint32_t pk[3][4];
+        const int m = idx % 24, rest = idx / 24, s = rest & 3, g = rest >> 2;
+        const float4* src = reinterpret_cast<const float4*>(a.fn + (int64_t)m * K + (int64_t)s * C + c0 + kCols * g);
 #pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-            uint16_t b[3][2];
+        for (int c = 0; c < 2; ++c) {
+            const float4 u = __ldg(src + 2 * c), v = __ldg(src + 2 * c + 1);
+            const float w[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
+            uint32_t pk[3][4];
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const float w0 = w[e + q];
-                const uint16_t h1 = bf16_bits_rn(w0);
-                const float r1 = w0 - __uint_as_float((uint32_t)h1 << 16);
-                const uint16_t h2 = bf16_bits_rn(r1);
-                const float r2 = r1 - __uint_as_float((uint32_t)h2 << 16);
-                b[0][q] = h1;
-                b[1][q] = h2;
-                b[2][q] = bf16_bits_rn(r2);
+            for (int e = 0; e < 8; e += 2) {
+                uint16_t b[3][2];
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const float w0 = w[e + q];
+                    const uint16_t h1 = bf16_bits_rn(w0);
+                    const float r1 = w0 - __uint_as_float((uint32_t)h1 << 16);
+                    const uint16_t h2 = bf16_bits_rn(r1);
+                    const float r2 = r1 - __uint_as_float((uint32_t)h2 << 16);
+                    b[0][q] = h1;
+                    b[1][q] = h2;
+                    b[2][q] = bf16_bits_rn(r2);
+                }
+#pragma unroll
+                for (int p = 0; p < 3; ++p) pk[p][e >> 1] = (uint32_t)b[p][0] | ((uint32_t)b[p][1] << 16);
             }
 #pragma unroll
-            for (int p = 0; p < 3; ++p) pk[p][e >> 1] = (uint32_t)b[p][0] | ((uint32_t)b[p][1] << 16);
+            for (int p = 0; p < 3; ++p)
+                *reinterpret_cast<uint4*>(wreg + w_off(g, s, p * 24 + m, c)) =
+                    make_uint4(pk[p][0], pk[p][1], pk[p][2], pk[p][3]);
         }
-#pragma unroll
-        for (int p = 0; p < 3; ++p)
-            *reinterpret_cast<uint4*>(wsm + w_off(g, s, p * 24 + m)) = make_uint4(pk[p][0], pk[p][1], pk[p][2], pk[p][3]);
     }
-    fence_proxy_async_smem();  // generic-proxy writes of fn planes -> visible to the tensor core
+    if (fold)
+        for (int i = tid; i < slice / 8; i += kThreads)
+            reinterpret_cast<uint4*>(nw_s)[i] = __ldg(reinterpret_cast<const uint4*>(a.norm_w + c0) + i);
+    fence_proxy_async_global();  // this thread's fn-plane writes -> visible to the bulk copies
     tc_fence_before();
     __syncthreads();
     cluster_sync_all();        // barrier initialisation visible to the whole cluster
@@ -180,29 +204,19 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
     if (warp == 0) {
         // ================================================== TMA producer
         if (lane == 0) {
-            // L2 prefetch of the first kPrefetch stages; afterwards each issued
-            // stage prefetches the one kPrefetch later (the shared-memory ring
-            // holds only 32 KB, the L2 keeps HBM requests in flight).
-            auto prefetch = [&](uint32_t q) {
-                const int tile_q = cid + (int)(q / ngroups) * ncl;
-                if (tile_q >= a.ntiles) return;
-                const int grp_q = (int)(q % ngroups);
-#pragma unroll
-                for (int st = 0; st < 4; ++st) tma_prefetch_3d(&xmap, c0 + 8 * grp_q, st, tile_q * kTile);
-            };
-            for (uint32_t q = 0; q < (uint32_t)kPrefetch; ++q) prefetch(q);
+            const uint64_t pol_x = policy_evict_first(), pol_w = policy_evict_last();
             uint32_t g = 0;
             for (int tile = cid; tile < a.ntiles && !*abort; tile += ncl) {
                 for (int grp = 0; grp < ngroups; ++grp, ++g) {
-                    prefetch(g + kPrefetch);
                     const int s = g % kStages;
-                    const uint32_t ph = (g / kStages) & 1;
-                    mbar_wait(&empty[s], ph ^ 1, abort);
-                    mbar_arrive_expect_tx(&full[s], kStageBytes);
+                    mbar_wait(&empty[s], ((g / kStages) & 1) ^ 1, abort);
+                    unsigned char* slot = stages + s * kSlotBytes;
+                    mbar_arrive_expect_tx(&full[s], kSlotBytes);
 #pragma unroll
                     for (int st = 0; st < 4; ++st)
-                        tma_load_3d(stages + s * kStageBytes + st * (kTile * 16), &xmap, c0 + 8 * grp, st,
-                                    tile * kTile, &full[s]);
+                        tma_load_3d_hint(slot + st * kBoxBytes, &xmap, c0 + kCols * grp, st, tile * kTile, &full[s],
+                                         pol_x);
+                    bulk_load_hint(slot + kXBytes, wreg + grp * kWStage, kWStage, &full[s], pol_w);
                 }
             }
             // drain: the last load of every slot has landed before the CTA exits
@@ -214,7 +228,6 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
         // ================================================== MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(kTile, kN);
-            const uint32_t wbase = smem_u32(wsm);
             const uint32_t sbase = smem_u32(stages);
             uint32_t g = 0;
             int it = 0;
@@ -228,10 +241,11 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                     mbar_wait(&full[s], (g / kStages) & 1, abort);
                     tc_fence_after();
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        const uint64_t ad = smem_desc(sbase + s * kStageBytes + j * 2 * (kTile * 16), kTile * 16, 128);
-                        const uint64_t bd = smem_desc(wbase + (grp * 2 + j) * kWBlock, 9 * 128, 128);
-                        mma_bf16(dt, ad, bd, idesc, (grp | j) != 0);
+                    for (int st = 0; st < 4; ++st) {
+                        const uint32_t slot = sbase + s * kSlotBytes;
+                        const uint64_t ad = smem_desc(slot + st * kBoxBytes, 16, 256, kLayoutSwizzle32B);
+                        const uint64_t bd = smem_desc(slot + kXBytes + st * kWBlock, 16, 256, kLayoutSwizzle32B);
+                        mma_bf16(dt, ad, bd, idesc, (grp | st) != 0);
                     }
                     mma_commit(&empty[s]);
                 }
@@ -241,31 +255,40 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
             mbar_wait(drain, 0, abort);
         }
         __syncwarp();
-    } else if (warp < 6) {
+    } else if (warp < kFinWarp) {
         // ================================================== token rows
+        const int grpsel = (warp - 2) >> 2;   // 0 or 1: which stages this warp takes
         const int quad = warp & 3;
         const int trow = quad * 32 + lane;
         const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
         const int fin = trow / kFinTok, slot = trow % kFinTok;
         const uint32_t inbox_dst = mapa(smem_u32(inbox + ((int)rank * kFinTok + slot) * kPart), fin);
         const uint32_t inbox_bar = mapa(smem_u32(inbox_full), fin);
-        // The folded store of tile i is deferred into tile i+1's stage loop:
-        // at group grp the thread first reads back tile i's parked h for that
-        // group, scales, rounds and stores it, then parks tile i+1's new h in
-        // the same TMEM columns.  The last tile is flushed after the loop.
+        // byte offsets of this token's two 16-byte chunks in a 4 KB stream box
+        const int xo0 = (trow >> 3) * 256 + sw32_off(trow & 7, 0);
+        const int xo1 = (trow >> 3) * 256 + sw32_off(trow & 7, 1);
+        // The folded store of tile i is deferred into tile i+1's stages: at a
+        // stage the thread first reads back tile i's parked h of those 16
+        // columns, scales, rounds and stores it, then parks tile i+1's h.
         bool have_prev = false, valid_prev = false;
         int64_t t_prev = 0;
         float sc_prev = 1.f;
         auto store_folded = [&](int grp) {
-            uint32_t r[8];
-            tmem_ld8(tl + kHCol + 8 * grp, r);
+            uint32_t r[16];
+            tmem_ld16(tl + kHCol + kCols * grp, r);
             tmem_wait_ld();
             if (valid_prev) {
-                float wf[8], o[8];
-                unpack8(__ldg(reinterpret_cast<const uint4*>(a.norm_w + c0 + 8 * grp)), wf);
+                const uint4* wv = reinterpret_cast<const uint4*>(nw_s + kCols * grp);
+                uint4* dst = reinterpret_cast<uint4*>(a.layer_input + t_prev * C + c0 + kCols * grp);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = __fmul_rn(__fmul_rn(__uint_as_float(r[e]), sc_prev), wf[e]);
-                st_stream(reinterpret_cast<uint4*>(a.layer_input + t_prev * C + c0 + 8 * grp), pack8(o));
+                for (int c = 0; c < 2; ++c) {
+                    float wf[8], o[8];
+                    unpack8(wv[c], wf);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        o[e] = __fmul_rn(__fmul_rn(__uint_as_float(r[8 * c + e]), sc_prev), wf[e]);
+                    st_stream(dst + c, pack8(o));
+                }
             }
         };
         uint32_t g = 0;
@@ -280,17 +303,27 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
             }
             float sx = 0.f, sh = 0.f;
             for (int grp = 0; grp < ngroups; ++grp, ++g) {
-                const int s = g % kStages;
+                if ((int)(g & 1) != grpsel) continue;  // stages alternate between the two groups
+                const int s = g % kStages;                // (kStages is even: slot s -> group s % 2)
                 mbar_wait(&full[s], (g / kStages) & 1, abort);
-                const uint4* xb = reinterpret_cast<const uint4*>(stages + s * kStageBytes);
-                float xv[4][8];
+                const unsigned char* sb = stages + s * kSlotBytes;
+                float xv[4][16];
 #pragma unroll
-                for (int st = 0; st < 4; ++st) unpack8(xb[st * kTile + trow], xv[st]);
+                for (int st = 0; st < 4; ++st) {
+                    float lo[8], hi[8];
+                    unpack8(*reinterpret_cast<const uint4*>(sb + st * kBoxBytes + xo0), lo);
+                    unpack8(*reinterpret_cast<const uint4*>(sb + st * kBoxBytes + xo1), hi);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        xv[st][e] = lo[e];
+                        xv[st][8 + e] = hi[e];
+                    }
+                }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
-                float h[8];
+                float h[16];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
+                for (int e = 0; e < 16; ++e) {
                     float v = __fmul_rn(p[0], xv[0][e]);
                     v = __fadd_rn(v, __fmul_rn(p[1], xv[1][e]));
                     v = __fadd_rn(v, __fmul_rn(p[2], xv[2][e]));
@@ -302,40 +335,65 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
                 }
                 if (fold) {
                     if (have_prev) store_folded(grp);
-                    uint32_t hb[8];
+                    uint32_t hb[16];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) hb[e] = __float_as_uint(h[e]);
-                    tmem_st8(tl + kHCol + 8 * grp, hb);
+                    for (int e = 0; e < 16; ++e) hb[e] = __float_as_uint(h[e]);
+                    tmem_st16(tl + kHCol + kCols * grp, hb);
                 } else if (valid) {
-                    st_stream(reinterpret_cast<uint4*>(a.layer_input + t * C + c0 + 8 * grp), pack8(h));
+                    uint4* dst = reinterpret_cast<uint4*>(a.layer_input + t * C + c0 + kCols * grp);
+                    float h0[8], h1[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        h0[e] = h[e];
+                        h1[e] = h[8 + e];
+                    }
+                    st_stream(dst, pack8(h0));
+                    st_stream(dst + 1, pack8(h1));
                 }
             }
             if (fold) tmem_wait_st();
 
-            // accumulated projection of this CTA's K-slice for the token
-            const int d = it & 1;
-            mbar_wait(&dfull[d], (it >> 1) & 1, abort);
-            tc_fence_after();
-            float acc[72];
-#pragma unroll
-            for (int c = 0; c < 72; c += 8) {
-                uint32_t r[8];
-                tmem_ld8(tl + (d ? kDCol1 : kDCol0) + c, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[c + e] = __uint_as_float(r[e]);
+            // group 1 hands its sums to group 0 through two free TMEM columns
+            // of the token's lane (fixed order: group 0 + group 1)
+            if (grpsel == 1) {
+                const uint32_t v2[2] = {__float_as_uint(sx), __float_as_uint(sh)};
+                tmem_st2(tl + kSumCol, v2);
+                tmem_wait_st();
             }
             tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&dempty[d]);
-            float part[kPart];
+            named_bar_sync(1, 32 * kRowWarps);
+            tc_fence_after();
+            if (grpsel == 0) {
+                uint32_t v2[2];
+                tmem_ld2(tl + kSumCol, v2);
+                tmem_wait_ld();
+                sx += __uint_as_float(v2[0]);
+                sh += __uint_as_float(v2[1]);
+                // accumulated projection of this CTA's K-slice for the token
+                const int d = it & 1;
+                mbar_wait(&dfull[d], (it >> 1) & 1, abort);
+                tc_fence_after();
+                float acc[72];
 #pragma unroll
-            for (int m = 0; m < 24; ++m) part[m] = acc[m] + (acc[24 + m] + acc[48 + m]);
-            part[24] = sx;
-            part[25] = sh;
+                for (int c = 0; c < 72; c += 8) {
+                    uint32_t r[8];
+                    tmem_ld8(tl + (d ? kDCol1 : kDCol0) + c, r);
+                    tmem_wait_ld();
 #pragma unroll
-            for (int k = 0; k < kPart; k += 2) st_cluster_v2(inbox_dst + 4 * k, part[k], part[k + 1]);
-            mbar_arrive_remote(inbox_bar);
+                    for (int e = 0; e < 8; ++e) acc[c + e] = __uint_as_float(r[e]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&dempty[d]);
+                float part[kPart];
+#pragma unroll
+                for (int m = 0; m < 24; ++m) part[m] = acc[m] + (acc[24 + m] + acc[48 + m]);
+                part[24] = sx;
+                part[25] = sh;
+#pragma unroll
+                for (int k = 0; k < kPart; k += 2) st_cluster_v2(inbox_dst + 4 * k, part[k], part[k + 1]);
+                mbar_arrive_remote(inbox_bar);
+            }
 
             // this tile's fold scale from the finalizers (also: every finalizer
             // has read its inbox, so the next tile's partials may be pushed)
@@ -345,8 +403,10 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
             valid_prev = valid;
             have_prev = true;
         }
-        if (fold && have_prev)
-            for (int grp = 0; grp < ngroups; ++grp) store_folded(grp);
+        if (fold && have_prev) {
+            // flush the last tile: this warp's share of the column groups
+            for (int grp = grpsel; grp < ngroups; grp += 2) store_folded(grp);
+        }
     } else {
         // ================================================== finalizer
         const uint32_t scale_dst = mapa(smem_u32(scale + (int)rank * kFinTok), lane & (kCtas - 1));
@@ -354,16 +414,26 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
         int it = 0;
         for (int tile = cid; tile < a.ntiles; tile += ncl, ++it) {
             mbar_wait<true>(inbox_full, it & 1, abort);
+            // sum the 16 sources in rank order; the sum of (token, value) q is
+            // written back over source 0's copy (read by the same lane first)
             for (int q = lane; q < kFinTok * kPart; q += 32) {
                 const int sl = q / kPart, v = q - sl * kPart;
+                float vals[kCtas];
+#pragma unroll
+                for (int src = 0; src < kCtas; ++src) vals[src] = inbox[(src * kFinTok + sl) * kPart + v];
                 float s = 0.f;
 #pragma unroll
-                for (int src = 0; src < kCtas; ++src) s += inbox[(src * kFinTok + sl) * kPart + v];
-                finred[q] = s;
+                for (int src = 0; src < kCtas; ++src) s += vals[src];
+                inbox[sl * kPart + v] = s;
             }
             __syncwarp();
+            // every inbox read of this tile happens before the scale push below
             const int sl = lane & (kFinTok - 1);
-            const float sx = finred[sl * kPart + 24], sh = finred[sl * kPart + 25];
+            float tv[kPart];
+#pragma unroll
+            for (int m = 0; m < kPart; ++m) tv[m] = inbox[sl * kPart + m];
+            __syncwarp();
+            const float sx = tv[24], sh = tv[25];
             const float sfold = fold ? 1.0f / sqrtf(sh / (float)C + a.norm_eps) : 1.0f;
             float sv[kFinTok];
 #pragma unroll
@@ -381,7 +451,7 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
 #pragma unroll
                 for (int m = 0; m < kLogits; ++m) {
                     const float al = m < 4 ? al0 : (m < 8 ? al1 : al2);
-                    l[m] = (r * finred[lane * kPart + m]) * al + __ldg(a.bias + m);
+                    l[m] = (r * tv[m]) * al + __ldg(a.bias + m);
                 }
                 if (a.logits_out) {
                     float4* lo = reinterpret_cast<float4*>(a.logits_out + t * kLogits);
@@ -430,7 +500,15 @@ static PFN_encodeTiled encode_fn() {
     return fn;
 }
 
-bool pre_tc_supports(int C) { return C % (8 * tc::kCtas) == 0 && C / tc::kCtas <= 8 * tc::kMaxGroups; }
+size_t pre_tc_workspace_bytes(int64_t T, int C, int max_clusters) {
+    const int64_t tiles = (T + tc::kTile - 1) / tc::kTile;
+    const int64_t ncl = tiles < max_clusters ? tiles : max_clusters;
+    return (size_t)ncl * tc::kCtas * (size_t)(C / (tc::kCols * tc::kCtas)) * tc::kWStage;
+}
+
+bool pre_tc_supports(int C) {
+    return C % (tc::kCols * tc::kCtas) == 0 && C / tc::kCtas <= tc::kCols * tc::kMaxGroups;
+}
 int pre_tc_tile_tokens() { return tc::kTile; }
 
 // One-time set-up for the current device: cluster-size and shared-memory
@@ -459,18 +537,19 @@ int pre_tc_prepare() {
 cudaError_t launch_pre_tc(const uint16_t* x, const float* pre_in, const float* fn, const float* bias,
                           const float* alpha, const uint16_t* norm_w, int64_t T, int C, int iters,
                           float rms_eps, float norm_eps, float sk_eps, float* pre_out, float* post_out,
-                          float* comb_out, uint16_t* layer_input, float* logits_out, cudaStream_t stream,
-                          int max_clusters) {
+                          float* comb_out, uint16_t* layer_input, float* logits_out, void* workspace,
+                          cudaStream_t stream, int max_clusters) {
     PFN_encodeTiled enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
-    // x viewed as [T][4][C] bf16; box = 8 columns x 1 stream x 128 tokens.
+    // x viewed as [T][4][C] bf16; box = 16 columns (32 B) x 1 stream x 128
+    // tokens, written to shared memory with the 32-byte swizzle the MMA reads.
     alignas(64) CUtensorMap map;
     const cuuint64_t dims[3] = {(cuuint64_t)C, 4, (cuuint64_t)T};
     const cuuint64_t strides[2] = {(cuuint64_t)C * 2, (cuuint64_t)C * 8};
-    const cuuint32_t box[3] = {8, 1, (cuuint32_t)tc::kTile};
+    const cuuint32_t box[3] = {(cuuint32_t)tc::kCols, 1, (cuuint32_t)tc::kTile};
     const cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(x), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     tc::Args a;
@@ -479,6 +558,7 @@ cudaError_t launch_pre_tc(const uint16_t* x, const float* pre_in, const float* f
     a.rms_eps = rms_eps; a.norm_eps = norm_eps; a.sk_eps = sk_eps;
     a.pre_out = pre_out; a.post_out = post_out; a.comb_out = comb_out;
     a.layer_input = layer_input; a.logits_out = logits_out;
+    a.ws = static_cast<unsigned char*>(workspace);
     a.ntiles = (int)((T + tc::kTile - 1) / tc::kTile);
     const int nclusters = a.ntiles < max_clusters ? a.ntiles : max_clusters;
     cudaLaunchConfig_t cfg = {};

@@ -53,7 +53,8 @@ def _pre(lib, **kw):
     args = dict(x=A, pre_in=A + 0x100000, fn=A + 0x200000, bias=A + 0x3000000, alpha=A + 0x3001000,
                 norm_weight=None, T=16, n=4, C=5120, iters=20, rms_eps=1e-6, norm_eps=1e-6,
                 sk_eps=1e-6, pre_out=A + 0x4000000, post_out=A + 0x4100000, comb_out=A + 0x4200000,
-                layer_input=A + 0x4300000, logits_out=None, stream=None)
+                layer_input=A + 0x4300000, logits_out=None, workspace=None, workspace_bytes=0,
+                stream=None)
     args.update(kw)
     return lib.mhc_pre_delayed(*args.values())
 
@@ -88,6 +89,16 @@ def test_pre_rejects_null_misaligned_and_overlapping(lib):
     assert _pre(lib, layer_input=A + 0x1000) == INVALID
     # two outputs overlapping
     assert _pre(lib, post_out=A + 0x4000010) == INVALID
+    # workspace overlapping an input or an output
+    assert _pre(lib, workspace=A + 0x10, workspace_bytes=1 << 20) == INVALID
+    assert _pre(lib, workspace=A + 0x4300000, workspace_bytes=64) == INVALID
+
+
+def test_workspace_bytes_host_only(lib):
+    # no GPU in this process: every shape reports 0 (the tensor-core plan, and
+    # with it the workspace, is sized on the device); bad shapes report 0
+    assert lib.mhc_pre_workspace_bytes(16, 4, 5120) == 0
+    assert lib.mhc_pre_workspace_bytes(16, 3, 5120) == 0
 
 
 def _post(lib, **kw):

@@ -34,6 +34,7 @@ def _gpu_pre(g, **kw):
     out = mhc.pre_delayed(g["x"], g["pre_in"], g["fn"], g["bias"], g["alpha"], g["norm_w"],
                           return_logits=True, **kw)
     torch.cuda.synchronize()
+    assert mhc.device_status() == 0, "a bounded in-kernel wait timed out"
     return {k: v.cpu() for k, v in out.items()}
 
 
@@ -94,13 +95,14 @@ def test_token_and_hidden_sweep(T, C, fold):
 
 
 @pytest.mark.parametrize("T,C,fold", [
-    (256, 5120, True), (257, 5120, False), (300, 128, True), (512, 4096, True),
-    (640, 2048, False), (1383, 5120, True), (4096, 5120, False),
+    (256, 5120, True), (257, 5120, False), (300, 256, True), (512, 4096, True),
+    (640, 2048, False), (1383, 5120, True), (4096, 5120, False), (700, 768, True),
 ])
 def test_tensor_core_path(T, C, fold):
     """Shapes that take the tensor-core kernel (128-token tiles, fn split in
-    three bf16 planes): ragged last tiles, one 8-column group per CTA
-    (C = 128), other slice widths, more tiles than co-resident clusters."""
+    three bf16 planes): ragged last tiles, one 16-column stage per CTA
+    (C = 256), an odd number of stages per tile (C = 768), other slice
+    widths, more tiles than co-resident clusters."""
     assert mhc.pre_plan(T, 4, C)["kernel"] == 2
     d = seam_inputs(T, C=C, seed=700 + T, fold=fold)
     g = _gpu_pre(_to_dev(d))
@@ -115,7 +117,8 @@ def test_kernel_choice():
     assert mhc.pre_plan(256)["kernel"] == 2
     assert mhc.pre_plan(16384)["kernel"] == 2
     assert mhc.pre_plan(4096, 4, 6144)["kernel"] == 1      # slice too wide for the TMEM park
-    assert mhc.pre_plan(4096, 4, 1000)["kernel"] == 1      # C not a multiple of 128
+    assert mhc.pre_plan(4096, 4, 1000)["kernel"] == 1      # C not a multiple of 256
+    assert mhc.pre_plan(4096, 4, 640)["kernel"] == 1
     p = mhc.pre_plan(16384)
     assert p["cluster"] == 16 and p["tokens_per_tile"] == 128 and p["grid"] % 16 == 0
 
