@@ -60,27 +60,32 @@ constexpr int kWBlock = 9 * 256;                  // per (stage, stream): 9 row-
 constexpr int kWStage = 4 * kWBlock;              // 9 KB of fn planes per stage
 constexpr int kSlotBytes = kXBytes + kWStage;     // 25 KB ring slot: x boxes, then fn blocks
 constexpr int kN = 80;                            // MMA N: 72 plane rows + 8 ignored
-constexpr int kPart = 26;                         // 24 dots, sum x^2, sum h^2
+constexpr int kDots = 24;                         // projection dot products per token
 constexpr int kFinTok = kTile / kCtas;            // tokens finalized per CTA per tile
 constexpr int kRowWarps = 8;
 constexpr int kThreads = 32 * (2 + kRowWarps + 1);
 constexpr int kFinWarp = 2 + kRowWarps;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDCol0 = 0, kDCol1 = 96, kHCol = 192;  // accumulators, parked h (320 columns)
-constexpr uint32_t kSumCol = 80;                           // group 1's sum x^2, sum h^2 (free columns)
 
-constexpr int kOffStages = 0;                                        // 1 KB aligned
+constexpr int kOffStages = 0;                                         // 1 KB aligned
 // The last slot's ignored 10th B-operand atom reads 256 B past the ring: the
-// inbox follows it, so that read stays inside shared memory.
-constexpr int kOffInbox = kOffStages + kStages * kSlotBytes;         // [16 src][8 tok][26]
-constexpr int kOffScale = kOffInbox + kCtas * kFinTok * kPart * 4;   // [128]
-constexpr int kOffNormW = kOffScale + kTile * 4;                     // [C/16] bf16
-constexpr int kOffBars = kOffNormW + kMaxGroups * kCols * 2;      // after the norm_w slice
-constexpr int kNumBars = 2 * kStages + 2 + 2 + 1 + 1 + 1;           // full, empty, dfull, dempty, inbox, scale, drain
-constexpr int kOffMisc = kOffBars + kNumBars * 8;                    // tmem base, abort flag
+// dots inbox follows it, so that read stays inside shared memory.
+constexpr int kOffDots = kOffStages + kStages * kSlotBytes;           // [16 src][8 tok][24] dots
+constexpr int kOffSq = kOffDots + kCtas * kFinTok * kDots * 4;        // [16 src][8 tok][2 grp][2] sums
+constexpr int kOffScale = kOffSq + kCtas * kFinTok * 2 * 2 * 4;       // [128] fold scales
+constexpr int kOffNormW = kOffScale + kTile * 4;                      // [C/16] bf16
+// [8 row warps][32 tok][16 col] bf16 staging tiles, 32-byte swizzled: the
+// swizzle pattern follows address bit 7, so each tile starts 1 KB aligned
+constexpr int kOffOut = (kOffNormW + kMaxGroups * kCols * 2 + 1023) / 1024 * 1024;
+constexpr int kOffBars = kOffOut + kRowWarps * 32 * kCols * 2;
+// full[8], empty[8], dfull[2], dempty[2], sq_full, dots_full, scale_full, dots_free, drain
+constexpr int kNumBars = 2 * kStages + 2 + 2 + 5;
+constexpr int kOffMisc = kOffBars + kNumBars * 8;                     // tmem base, abort flag
 constexpr int kSmemBytes = kOffMisc + 16;
-static_assert(kOffNormW + kMaxGroups * kCols * 2 <= kOffBars, "norm_w slice overlaps the barriers");
 static_assert(kOffBars % 8 == 0, "mbarriers need 8-byte alignment");
+static_assert(kSlotBytes % 1024 == 0 && kBoxBytes % 1024 == 0 && kXBytes % 256 == 0 && kWBlock % 256 == 0,
+              "swizzled TMA boxes and MMA operand atoms must stay 256-byte aligned");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Args {
@@ -116,11 +121,33 @@ __device__ __forceinline__ uint16_t bf16_bits_rn(float v) {
     return *reinterpret_cast<uint16_t*>(&b);
 }
 
+// fn -> three bf16 planes (hi, mid, lo): an exact split of the fp32 value.
+__device__ __forceinline__ void split3(const float (&w)[8], uint32_t (&pk)[3][4]) {
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+        uint16_t b[3][2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const float w0 = w[e + q];
+            const uint16_t h1 = bf16_bits_rn(w0);
+            const float r1 = w0 - __uint_as_float((uint32_t)h1 << 16);
+            const uint16_t h2 = bf16_bits_rn(r1);
+            const float r2 = r1 - __uint_as_float((uint32_t)h2 << 16);
+            b[0][q] = h1;
+            b[1][q] = h2;
+            b[2][q] = bf16_bits_rn(r2);
+        }
+#pragma unroll
+        for (int p = 0; p < 3; ++p) pk[p][e >> 1] = (uint32_t)b[p][0] | ((uint32_t)b[p][1] << 16);
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
+pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap omap, const Args a) {
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* stages = smem + kOffStages;
-    float* inbox = reinterpret_cast<float*>(smem + kOffInbox);
+    float* dots_in = reinterpret_cast<float*>(smem + kOffDots);
+    float* sq_in = reinterpret_cast<float*>(smem + kOffSq);
     float* scale = reinterpret_cast<float*>(smem + kOffScale);
     uint16_t* nw_s = reinterpret_cast<uint16_t*>(smem + kOffNormW);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
@@ -128,9 +155,11 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
     uint64_t* empty = bars + kStages;
     uint64_t* dfull = bars + 2 * kStages;
     uint64_t* dempty = dfull + 2;
-    uint64_t* inbox_full = dempty + 2;
-    uint64_t* scale_full = inbox_full + 1;
-    uint64_t* drain = scale_full + 1;
+    uint64_t* sq_full = dempty + 2;       // this CTA's finalizer: Σx², Σh² of its 8 tokens arrived
+    uint64_t* dots_full = sq_full + 1;    // ... their dot products arrived
+    uint64_t* scale_full = dots_full + 1; // this CTA's 128 fold scales arrived
+    uint64_t* dots_free = scale_full + 1; // every finalizer has read this CTA's previous dots
+    uint64_t* drain = dots_free + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
 
@@ -139,6 +168,11 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
     const int cid = (int)cluster_id_x(), ncl = (int)ncluster_x();
     const int C = a.C, K = 4 * C, slice = C / kCtas, ngroups = slice / kCols, c0 = (int)rank * slice;
     const bool fold = a.norm_w != nullptr;
+    unsigned char* wreg = a.ws + (size_t)(cid * kCtas + (int)rank) * ngroups * kWStage;
+    // stages of this CTA in the whole launch, and those issued before the fn planes are ready
+    const int my_tiles = cid < a.ntiles ? (a.ntiles - 1 - cid) / ncl + 1 : 0;
+    const uint32_t total_stages = (uint32_t)my_tiles * ngroups;
+    const uint32_t early = total_stages < (uint32_t)kStages ? total_stages : (uint32_t)kStages;
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -149,46 +183,67 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
             mbar_init(&dfull[d], 1);
             mbar_init(&dempty[d], 4);    // group 0's 4 warps
         }
-        mbar_init(inbox_full, kTile);    // one arrival per (source CTA, token) pair
-        mbar_init(scale_full, kCtas);    // one arrival per finalizer CTA
+        // the three cluster exchanges complete by bytes (st.async); each has
+        // one local arrival per phase that arms the expected byte count
+        mbar_init(sq_full, 1);           // + 16 CTAs x 8 tokens x 2 groups x 8 B
+        mbar_init(dots_full, 1);         // + 16 CTAs x 8 tokens x 96 B
+        mbar_init(scale_full, 1);        // + 16 finalizers x 32 B
+        mbar_init(dots_free, kCtas);     // one arrival per finalizer CTA
         mbar_init(drain, 1);
         *abort = 0;
         fence_mbar_init_cluster();
+        fence_proxy_async_smem();
+        // the first ring slots' x boxes do not depend on fn: start them now
+        const uint64_t pol_x = policy_evict_first();
+        for (uint32_t q = 0; q < early; ++q) {
+            const int tile = cid + (int)(q / ngroups) * ncl, grp = (int)(q % ngroups);
+            mbar_arrive_expect_tx(&full[q], kSlotBytes);
+#pragma unroll
+            for (int st = 0; st < 4; ++st)
+                tma_load_3d_hint(stages + q * kSlotBytes + st * kBoxBytes, &xmap, c0 + kCols * grp, st,
+                                 tile * kTile, &full[q], pol_x);
+        }
     }
     if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
 
-    // ---- fn K-slice -> three bf16 planes (exact split) in the operand layout,
-    //      written to this CTA's workspace region; read back stage by stage.
-    unsigned char* wreg = a.ws + (size_t)(cid * kCtas + (int)rank) * ngroups * kWStage;
-    for (int idx = tid; idx < 24 * 4 * ngroups; idx += kThreads) {
-        const int m = idx % 24, rest = idx / 24, s = rest & 3, g = rest >> 2;
-        const float4* src = reinterpret_cast<const float4*>(a.fn + (int64_t)m * K + (int64_t)s * C + c0 + kCols * g);
+    // ---- fn K-slice -> three bf16 planes in the operand layout, written to
+    //      this CTA's workspace region; every thread first loads all of its
+    //      items (one latency), then splits and stores them.
+    {
+        constexpr int kItemsMax = 6;   // ceil(24 * 4 * 20 / 352)
+        float w[kItemsMax][2][8];
+        int nitems = 0;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            const float4 u = __ldg(src + 2 * c), v = __ldg(src + 2 * c + 1);
-            const float w[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
-            uint32_t pk[3][4];
+        for (int j = 0; j < kItemsMax; ++j) {
+            const int idx = tid + j * kThreads;
+            if (idx < 24 * 4 * ngroups) {
+                const int m = idx % 24, rest = idx / 24, s = rest & 3, g = rest >> 2;
+                const float4* src = reinterpret_cast<const float4*>(a.fn + (int64_t)m * K + (int64_t)s * C +
+                                                                    c0 + kCols * g);
 #pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-                uint16_t b[3][2];
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const float w0 = w[e + q];
-                    const uint16_t h1 = bf16_bits_rn(w0);
-                    const float r1 = w0 - __uint_as_float((uint32_t)h1 << 16);
-                    const uint16_t h2 = bf16_bits_rn(r1);
-                    const float r2 = r1 - __uint_as_float((uint32_t)h2 << 16);
-                    b[0][q] = h1;
-                    b[1][q] = h2;
-                    b[2][q] = bf16_bits_rn(r2);
+                for (int c = 0; c < 2; ++c) {
+                    const float4 u = __ldg(src + 2 * c), v = __ldg(src + 2 * c + 1);
+                    w[j][c][0] = u.x; w[j][c][1] = u.y; w[j][c][2] = u.z; w[j][c][3] = u.w;
+                    w[j][c][4] = v.x; w[j][c][5] = v.y; w[j][c][6] = v.z; w[j][c][7] = v.w;
                 }
-#pragma unroll
-                for (int p = 0; p < 3; ++p) pk[p][e >> 1] = (uint32_t)b[p][0] | ((uint32_t)b[p][1] << 16);
+                nitems = j + 1;
             }
+        }
 #pragma unroll
-            for (int p = 0; p < 3; ++p)
-                *reinterpret_cast<uint4*>(wreg + w_off(g, s, p * 24 + m, c)) =
-                    make_uint4(pk[p][0], pk[p][1], pk[p][2], pk[p][3]);
+        for (int j = 0; j < kItemsMax; ++j) {
+            if (j < nitems) {
+                const int idx = tid + j * kThreads;
+                const int m = idx % 24, rest = idx / 24, s = rest & 3, g = rest >> 2;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t pk[3][4];
+                    split3(w[j][c], pk);
+#pragma unroll
+                    for (int p = 0; p < 3; ++p)
+                        *reinterpret_cast<uint4*>(wreg + w_off(g, s, p * 24 + m, c)) =
+                            make_uint4(pk[p][0], pk[p][1], pk[p][2], pk[p][3]);
+                }
+            }
         }
     }
     if (fold)
@@ -197,7 +252,7 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
     fence_proxy_async_global();  // this thread's fn-plane writes -> visible to the bulk copies
     tc_fence_before();
     __syncthreads();
-    cluster_sync_all();        // barrier initialisation visible to the whole cluster
+    cluster_sync_all();          // barrier initialisation visible to the whole cluster
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
@@ -205,19 +260,21 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
         // ================================================== TMA producer
         if (lane == 0) {
             const uint64_t pol_x = policy_evict_first(), pol_w = policy_evict_last();
-            uint32_t g = 0;
-            for (int tile = cid; tile < a.ntiles && !*abort; tile += ncl) {
-                for (int grp = 0; grp < ngroups; ++grp, ++g) {
-                    const int s = g % kStages;
-                    mbar_wait(&empty[s], ((g / kStages) & 1) ^ 1, abort);
-                    unsigned char* slot = stages + s * kSlotBytes;
-                    mbar_arrive_expect_tx(&full[s], kSlotBytes);
+            for (uint32_t q = 0; q < early; ++q)   // fn blocks of the slots started before the planes existed
+                bulk_load_hint(stages + q * kSlotBytes + kXBytes, wreg + (q % ngroups) * kWStage, kWStage,
+                               &full[q], pol_w);
+            uint32_t g = early;
+            for (; g < total_stages && !*abort; ++g) {
+                const int tile = cid + (int)(g / ngroups) * ncl, grp = (int)(g % ngroups);
+                const int s = g % kStages;
+                mbar_wait(&empty[s], ((g / kStages) & 1) ^ 1, abort);
+                unsigned char* slot = stages + s * kSlotBytes;
+                mbar_arrive_expect_tx(&full[s], kSlotBytes);
 #pragma unroll
-                    for (int st = 0; st < 4; ++st)
-                        tma_load_3d_hint(slot + st * kBoxBytes, &xmap, c0 + kCols * grp, st, tile * kTile, &full[s],
-                                         pol_x);
-                    bulk_load_hint(slot + kXBytes, wreg + grp * kWStage, kWStage, &full[s], pol_w);
-                }
+                for (int st = 0; st < 4; ++st)
+                    tma_load_3d_hint(slot + st * kBoxBytes, &xmap, c0 + kCols * grp, st, tile * kTile, &full[s],
+                                     pol_x);
+                bulk_load_hint(slot + kXBytes, wreg + grp * kWStage, kWStage, &full[s], pol_w);
             }
             // drain: the last load of every slot has landed before the CTA exits
             for (uint32_t k = (g > (uint32_t)kStages ? g - kStages : 0); k < g; ++k)
@@ -262,40 +319,68 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
         const int trow = quad * 32 + lane;
         const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
         const int fin = trow / kFinTok, slot = trow % kFinTok;
-        const uint32_t inbox_dst = mapa(smem_u32(inbox + ((int)rank * kFinTok + slot) * kPart), fin);
-        const uint32_t inbox_bar = mapa(smem_u32(inbox_full), fin);
+        const uint32_t sq_dst = mapa(smem_u32(sq_in + (((int)rank * kFinTok + slot) * 2 + grpsel) * 2), fin);
+        const uint32_t sq_bar = mapa(smem_u32(sq_full), fin);
+        const uint32_t dots_dst = mapa(smem_u32(dots_in + ((int)rank * kFinTok + slot) * kDots), fin);
+        const uint32_t dots_bar = mapa(smem_u32(dots_full), fin);
+        const bool armer = (warp == 2 && lane == 0);   // arms this CTA's scale_full each tile
         // byte offsets of this token's two 16-byte chunks in a 4 KB stream box
         const int xo0 = (trow >> 3) * 256 + sw32_off(trow & 7, 0);
         const int xo1 = (trow >> 3) * 256 + sw32_off(trow & 7, 1);
+        // layer_input leaves through a per-warp 32-token x 16-column staging
+        // tile (32-byte swizzle) and one TMA tensor store per warp and stage:
+        // full 32-byte sectors instead of 32 scattered 16-byte stores per
+        // instruction; rows past T are clipped by the store.
+        unsigned char* ostage = smem + kOffOut + (warp - 2) * (32 * kCols * 2);
+        const int oo0 = (lane >> 3) * 256 + sw32_off(lane & 7, 0);
+        const int oo1 = (lane >> 3) * 256 + sw32_off(lane & 7, 1);
+        auto store_out = [&](const float (&o)[16], int col, int64_t row0) {
+            if (lane == 0) bulk_wait_read_all();   // the previous store has read the tile
+            __syncwarp();
+            float a0[8], a1[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                a0[e] = o[e];
+                a1[e] = o[8 + e];
+            }
+            *reinterpret_cast<uint4*>(ostage + oo0) = pack8(a0);
+            *reinterpret_cast<uint4*>(ostage + oo1) = pack8(a1);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && row0 < a.T) {
+                tma_store_2d(&omap, ostage, col, (int)row0);
+                bulk_commit_group();
+            }
+        };
         // The folded store of tile i is deferred into tile i+1's stages: at a
         // stage the thread first reads back tile i's parked h of those 16
         // columns, scales, rounds and stores it, then parks tile i+1's h.
-        bool have_prev = false, valid_prev = false;
+        bool have_prev = false;
         int64_t t_prev = 0;
         float sc_prev = 1.f;
         auto store_folded = [&](int grp) {
             uint32_t r[16];
             tmem_ld16(tl + kHCol + kCols * grp, r);
             tmem_wait_ld();
-            if (valid_prev) {
-                const uint4* wv = reinterpret_cast<const uint4*>(nw_s + kCols * grp);
-                uint4* dst = reinterpret_cast<uint4*>(a.layer_input + t_prev * C + c0 + kCols * grp);
+            tmem_regs_ready(r);
+            const uint4* wv = reinterpret_cast<const uint4*>(nw_s + kCols * grp);
+            float o[16];
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    float wf[8], o[8];
-                    unpack8(wv[c], wf);
+            for (int c = 0; c < 2; ++c) {
+                float wf[8];
+                unpack8(wv[c], wf);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        o[e] = __fmul_rn(__fmul_rn(__uint_as_float(r[8 * c + e]), sc_prev), wf[e]);
-                    st_stream(dst + c, pack8(o));
-                }
+                for (int e = 0; e < 8; ++e)
+                    o[8 * c + e] = __fmul_rn(__fmul_rn(__uint_as_float(r[8 * c + e]), sc_prev), wf[e]);
             }
+            store_out(o, c0 + kCols * grp, t_prev - lane);
         };
         uint32_t g = 0;
         int it = 0;
         for (int tile = cid; tile < a.ntiles; tile += ncl, ++it) {
             const int64_t t = (int64_t)tile * kTile + trow;
             const bool valid = t < a.T;
+            if (armer) mbar_arrive_expect_tx(scale_full, kCtas * kFinTok * 4);
             float p[4] = {0.f, 0.f, 0.f, 0.f};
             if (valid) {
                 const float4 pv = __ldg(reinterpret_cast<const float4*>(a.pre_in) + t);
@@ -339,110 +424,115 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
 #pragma unroll
                     for (int e = 0; e < 16; ++e) hb[e] = __float_as_uint(h[e]);
                     tmem_st16(tl + kHCol + kCols * grp, hb);
-                } else if (valid) {
-                    uint4* dst = reinterpret_cast<uint4*>(a.layer_input + t * C + c0 + kCols * grp);
-                    float h0[8], h1[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        h0[e] = h[e];
-                        h1[e] = h[8 + e];
-                    }
-                    st_stream(dst, pack8(h0));
-                    st_stream(dst + 1, pack8(h1));
+                } else {
+                    store_out(h, c0 + kCols * grp, t - lane);
                 }
             }
+            // this group's sums go out first: the finalizer needs only Σh² for
+            // the fold scale, which gates every CTA's next tile
+            st_async_v2(sq_dst, sx, sh, sq_bar);
             if (fold) tmem_wait_st();
 
-            // group 1 hands its sums to group 0 through two free TMEM columns
-            // of the token's lane (fixed order: group 0 + group 1)
-            if (grpsel == 1) {
-                const uint32_t v2[2] = {__float_as_uint(sx), __float_as_uint(sh)};
-                tmem_st2(tl + kSumCol, v2);
-                tmem_wait_st();
-            }
-            tc_fence_before();
-            named_bar_sync(1, 32 * kRowWarps);
-            tc_fence_after();
             if (grpsel == 0) {
-                uint32_t v2[2];
-                tmem_ld2(tl + kSumCol, v2);
-                tmem_wait_ld();
-                sx += __uint_as_float(v2[0]);
-                sh += __uint_as_float(v2[1]);
                 // accumulated projection of this CTA's K-slice for the token
                 const int d = it & 1;
                 mbar_wait(&dfull[d], (it >> 1) & 1, abort);
                 tc_fence_after();
+                uint32_t raw[9][8];
+#pragma unroll
+                for (int c = 0; c < 9; ++c) tmem_ld8(tl + (d ? kDCol1 : kDCol0) + 8 * c, raw[c]);
+                tmem_wait_ld();
                 float acc[72];
 #pragma unroll
-                for (int c = 0; c < 72; c += 8) {
-                    uint32_t r[8];
-                    tmem_ld8(tl + (d ? kDCol1 : kDCol0) + c, r);
-                    tmem_wait_ld();
+                for (int c = 0; c < 9; ++c) {
+                    tmem_regs_ready(raw[c]);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[c + e] = __uint_as_float(r[e]);
+                    for (int e = 0; e < 8; ++e) acc[8 * c + e] = __uint_as_float(raw[c][e]);
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&dempty[d]);
-                float part[kPart];
+                float dots[kDots];
 #pragma unroll
-                for (int m = 0; m < 24; ++m) part[m] = acc[m] + (acc[24 + m] + acc[48 + m]);
-                part[24] = sx;
-                part[25] = sh;
+                for (int m = 0; m < kDots; ++m) dots[m] = acc[m] + (acc[24 + m] + acc[48 + m]);
+                // the finalizers have read this CTA's previous dots
+                mbar_wait<true>(dots_free, (it & 1) ^ 1, abort);
 #pragma unroll
-                for (int k = 0; k < kPart; k += 2) st_cluster_v2(inbox_dst + 4 * k, part[k], part[k + 1]);
-                mbar_arrive_remote(inbox_bar);
+                for (int k = 0; k < kDots; k += 4)
+                    st_async_v4(dots_dst + 4 * k, dots[k], dots[k + 1], dots[k + 2], dots[k + 3], dots_bar);
             }
 
-            // this tile's fold scale from the finalizers (also: every finalizer
-            // has read its inbox, so the next tile's partials may be pushed)
+            // this tile's fold scale from the finalizers
             mbar_wait<true>(scale_full, it & 1, abort);
             sc_prev = scale[trow];
             t_prev = t;
-            valid_prev = valid;
             have_prev = true;
+            // both groups' parked h is complete before the other group reads it
+            // in the next tile (stage parity can change between tiles)
+            tc_fence_before();
+            named_bar_sync(1, 32 * kRowWarps);
+            tc_fence_after();
         }
         if (fold && have_prev) {
             // flush the last tile: this warp's share of the column groups
             for (int grp = grpsel; grp < ngroups; grp += 2) store_folded(grp);
         }
+        if (lane == 0) bulk_wait_all();   // stores complete before the CTA exits
     } else {
         // ================================================== finalizer
-        const uint32_t scale_dst = mapa(smem_u32(scale + (int)rank * kFinTok), lane & (kCtas - 1));
-        const uint32_t scale_bar = mapa(smem_u32(scale_full), lane & (kCtas - 1));
+        const uint32_t peer = (uint32_t)(lane & (kCtas - 1));
+        const uint32_t scale_dst = mapa(smem_u32(scale + (int)rank * kFinTok), peer);
+        const uint32_t scale_bar = mapa(smem_u32(scale_full), peer);
+        const uint32_t free_bar = mapa(smem_u32(dots_free), peer);
         int it = 0;
         for (int tile = cid; tile < a.ntiles; tile += ncl, ++it) {
-            mbar_wait<true>(inbox_full, it & 1, abort);
-            // sum the 16 sources in rank order; the sum of (token, value) q is
-            // written back over source 0's copy (read by the same lane first)
-            for (int q = lane; q < kFinTok * kPart; q += 32) {
-                const int sl = q / kPart, v = q - sl * kPart;
-                float vals[kCtas];
-#pragma unroll
-                for (int src = 0; src < kCtas; ++src) vals[src] = inbox[(src * kFinTok + sl) * kPart + v];
-                float s = 0.f;
-#pragma unroll
-                for (int src = 0; src < kCtas; ++src) s += vals[src];
-                inbox[sl * kPart + v] = s;
+            // (1) Σx², Σh² of the 8 tokens: lane (tok, value) sums 16 sources x
+            //     2 groups in fixed order; the scale goes out right away
+            if (lane == 0) {
+                mbar_arrive_expect_tx(sq_full, kCtas * kFinTok * 2 * 8);
+                mbar_arrive_expect_tx(dots_full, kCtas * kFinTok * kDots * 4);
             }
-            __syncwarp();
-            // every inbox read of this tile happens before the scale push below
-            const int sl = lane & (kFinTok - 1);
-            float tv[kPart];
+            mbar_wait<true>(sq_full, it & 1, abort);
+            float sum = 0.f;
+            if (lane < 2 * kFinTok) {
+                const int tk = lane & (kFinTok - 1), v = lane >> 3;
+                float vals[2 * kCtas];
 #pragma unroll
-            for (int m = 0; m < kPart; ++m) tv[m] = inbox[sl * kPart + m];
-            __syncwarp();
-            const float sx = tv[24], sh = tv[25];
+                for (int q = 0; q < 2 * kCtas; ++q) vals[q] = sq_in[(((q >> 1) * kFinTok + tk) * 2 + (q & 1)) * 2 + v];
+#pragma unroll
+                for (int q = 0; q < 2 * kCtas; ++q) sum += vals[q];
+            }
+            const float sx = __shfl_sync(0xffffffffu, sum, lane & (kFinTok - 1));
+            const float sh = __shfl_sync(0xffffffffu, sum, kFinTok + (lane & (kFinTok - 1)));
             const float sfold = fold ? 1.0f / sqrtf(sh / (float)C + a.norm_eps) : 1.0f;
             float sv[kFinTok];
 #pragma unroll
             for (int k = 0; k < kFinTok; ++k) sv[k] = __shfl_sync(0xffffffffu, sfold, k);
             if (lane < kCtas) {
-                st_cluster_v4(scale_dst, sv[0], sv[1], sv[2], sv[3]);
-                st_cluster_v4(scale_dst + 16, sv[4], sv[5], sv[6], sv[7]);
-                mbar_arrive_remote(scale_bar);
+                st_async_v4(scale_dst, sv[0], sv[1], sv[2], sv[3], scale_bar);
+                st_async_v4(scale_dst + 16, sv[4], sv[5], sv[6], sv[7], scale_bar);
             }
+            // (2) the dot products, off the tiles' critical path
+            mbar_wait<true>(dots_full, it & 1, abort);
+            float dsum[kDots];
+#pragma unroll
+            for (int m = 0; m < kDots; ++m) dsum[m] = 0.f;
+            if (lane < kFinTok) {
+#pragma unroll 4
+                for (int src = 0; src < kCtas; ++src) {
+                    const float4* row = reinterpret_cast<const float4*>(dots_in + (src * kFinTok + lane) * kDots);
+#pragma unroll
+                    for (int k = 0; k < kDots / 4; ++k) {
+                        const float4 v4 = row[k];
+                        dsum[4 * k] += v4.x;
+                        dsum[4 * k + 1] += v4.y;
+                        dsum[4 * k + 2] += v4.z;
+                        dsum[4 * k + 3] += v4.w;
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane < kCtas) mbar_arrive_remote(free_bar);   // inbox read: sources may push again
             const int64_t t = (int64_t)tile * kTile + (int)rank * kFinTok + lane;
             if (lane < kFinTok && t < a.T) {
                 const float r = 1.0f / sqrtf(sx / (float)K + a.rms_eps);
@@ -451,7 +541,7 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
 #pragma unroll
                 for (int m = 0; m < kLogits; ++m) {
                     const float al = m < 4 ? al0 : (m < 8 ? al1 : al2);
-                    l[m] = (r * tv[m]) * al + __ldg(a.bias + m);
+                    l[m] = (r * dsum[m]) * al + __ldg(a.bias + m);
                 }
                 if (a.logits_out) {
                     float4* lo = reinterpret_cast<float4*>(a.logits_out + t * kLogits);
@@ -552,6 +642,16 @@ cudaError_t launch_pre_tc(const uint16_t* x, const float* pre_in, const float* f
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    // layer_input [T][C] bf16; box = 16 columns x 32 tokens (one warp's rows)
+    alignas(64) CUtensorMap omap;
+    const cuuint64_t odims[2] = {(cuuint64_t)C, (cuuint64_t)T};
+    const cuuint64_t ostrides[1] = {(cuuint64_t)C * 2};
+    const cuuint32_t obox[2] = {(cuuint32_t)tc::kCols, 32};
+    const cuuint32_t oestr[2] = {1, 1};
+    r = enc(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, layer_input, odims, ostrides, obox, oestr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     tc::Args a;
     a.x = x; a.pre_in = pre_in; a.fn = fn; a.bias = bias; a.alpha = alpha; a.norm_w = norm_w;
     a.T = T; a.C = C; a.iters = iters;
@@ -573,7 +673,7 @@ cudaError_t launch_pre_tc(const uint16_t* x, const float* pre_in, const float* f
     cfg.gridDim = dim3((unsigned)(nclusters * tc::kCtas), 1, 1);
     cfg.dynamicSmemBytes = tc::kSmemBytes;
     cfg.stream = stream;
-    return cudaLaunchKernelEx(&cfg, tc::pre_tc_kernel, map, a);
+    return cudaLaunchKernelEx(&cfg, tc::pre_tc_kernel, map, omap, a);
 }
 
 // Host read-and-clear of the device status word (synchronous).
