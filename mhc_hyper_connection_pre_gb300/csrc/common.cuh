@@ -36,6 +36,42 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
     return v;
 }
 
+// Two fp32 lanes in one 64-bit register for the packed .f32x2 instructions
+// (each lane is rounded on its own, exactly like the scalar instruction).
+struct f32x2 {
+    unsigned long long v;
+};
+__device__ __forceinline__ f32x2 make_f32x2(float lo, float hi) {
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void split_f32x2(f32x2 a, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+}
+__device__ __forceinline__ f32x2 mul_rn2(f32x2 a, f32x2 b) {
+    f32x2 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+    return r;
+}
+__device__ __forceinline__ f32x2 add_rn2(f32x2 a, f32x2 b) {
+    f32x2 r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+    return r;
+}
+__device__ __forceinline__ f32x2 fma_rn2(f32x2 a, f32x2 b, f32x2 c) {
+    f32x2 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.v) : "l"(a.v), "l"(b.v), "l"(c.v));
+    return r;
+}
+// bf16 pair (low column in the low half) -> packed fp32 pair.
+__device__ __forceinline__ f32x2 bf16x2_to_f32x2(uint32_t w) { return make_f32x2(bf16lo(w), bf16hi(w)); }
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(f32x2 a) {
+    float lo, hi;
+    split_f32x2(a, lo, hi);
+    return pack_bf16x2(lo, hi);
+}
+
 // Streaming 16-byte global load / store (data touched once).
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
 __device__ __forceinline__ void st_stream(uint4* p, const uint4& v) { __stcs(p, v); }

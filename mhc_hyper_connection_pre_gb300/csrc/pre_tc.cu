@@ -334,17 +334,13 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
         unsigned char* ostage = smem + kOffOut + (warp - 2) * (32 * kCols * 2);
         const int oo0 = (lane >> 3) * 256 + sw32_off(lane & 7, 0);
         const int oo1 = (lane >> 3) * 256 + sw32_off(lane & 7, 1);
-        auto store_out = [&](const float (&o)[16], int col, int64_t row0) {
+        auto store_out = [&](const f32x2 (&o)[8], int col, int64_t row0) {
             if (lane == 0) bulk_wait_read_all();   // the previous store has read the tile
             __syncwarp();
-            float a0[8], a1[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                a0[e] = o[e];
-                a1[e] = o[8 + e];
-            }
-            *reinterpret_cast<uint4*>(ostage + oo0) = pack8(a0);
-            *reinterpret_cast<uint4*>(ostage + oo1) = pack8(a1);
+            *reinterpret_cast<uint4*>(ostage + oo0) = make_uint4(f32x2_to_bf16x2(o[0]), f32x2_to_bf16x2(o[1]),
+                                                                 f32x2_to_bf16x2(o[2]), f32x2_to_bf16x2(o[3]));
+            *reinterpret_cast<uint4*>(ostage + oo1) = make_uint4(f32x2_to_bf16x2(o[4]), f32x2_to_bf16x2(o[5]),
+                                                                 f32x2_to_bf16x2(o[6]), f32x2_to_bf16x2(o[7]));
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0 && row0 < a.T) {
@@ -364,14 +360,17 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
             tmem_wait_ld();
             tmem_regs_ready(r);
             const uint4* wv = reinterpret_cast<const uint4*>(nw_s + kCols * grp);
-            float o[16];
+            const f32x2 sc2 = make_f32x2(sc_prev, sc_prev);
+            f32x2 o[8];
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-                float wf[8];
-                unpack8(wv[c], wf);
+                const uint4 w4 = wv[c];
+                const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    o[8 * c + e] = __fmul_rn(__fmul_rn(__uint_as_float(r[8 * c + e]), sc_prev), wf[e]);
+                for (int e = 0; e < 4; ++e) {
+                    const f32x2 hv = make_f32x2(__uint_as_float(r[8 * c + 2 * e]), __uint_as_float(r[8 * c + 2 * e + 1]));
+                    o[4 * c + e] = mul_rn2(mul_rn2(hv, sc2), bf16x2_to_f32x2(ww[e]));   // (h * s) * w
+                }
             }
             store_out(o, c0 + kCols * grp, t_prev - lane);
         };
@@ -386,47 +385,71 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
                 const float4 pv = __ldg(reinterpret_cast<const float4*>(a.pre_in) + t);
                 p[0] = pv.x; p[1] = pv.y; p[2] = pv.z; p[3] = pv.w;
             }
-            float sx = 0.f, sh = 0.f;
+            f32x2 sx2 = make_f32x2(0.f, 0.f), sh2 = make_f32x2(0.f, 0.f);
             for (int grp = 0; grp < ngroups; ++grp, ++g) {
                 if ((int)(g & 1) != grpsel) continue;  // stages alternate between the two groups
                 const int s = g % kStages;                // (kStages is even: slot s -> group s % 2)
                 mbar_wait(&full[s], (g / kStages) & 1, abort);
                 const unsigned char* sb = stages + s * kSlotBytes;
-                float xv[4][16];
+                // x of the token: 4 streams x 16 columns as 8 column pairs each
+                f32x2 xv[4][8];
 #pragma unroll
                 for (int st = 0; st < 4; ++st) {
-                    float lo[8], hi[8];
-                    unpack8(*reinterpret_cast<const uint4*>(sb + st * kBoxBytes + xo0), lo);
-                    unpack8(*reinterpret_cast<const uint4*>(sb + st * kBoxBytes + xo1), hi);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        xv[st][e] = lo[e];
-                        xv[st][8 + e] = hi[e];
-                    }
+                    const uint4 lo = *reinterpret_cast<const uint4*>(sb + st * kBoxBytes + xo0);
+                    const uint4 hi = *reinterpret_cast<const uint4*>(sb + st * kBoxBytes + xo1);
+                    xv[st][0] = bf16x2_to_f32x2(lo.x); xv[st][1] = bf16x2_to_f32x2(lo.y);
+                    xv[st][2] = bf16x2_to_f32x2(lo.z); xv[st][3] = bf16x2_to_f32x2(lo.w);
+                    xv[st][4] = bf16x2_to_f32x2(hi.x); xv[st][5] = bf16x2_to_f32x2(hi.y);
+                    xv[st][6] = bf16x2_to_f32x2(hi.z); xv[st][7] = bf16x2_to_f32x2(hi.w);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
-                float h[16];
+                // collapse in scalar fp32, every product and sum rounded on its
+                // own, stream order (the bit-exact reference order); the sums
+                // of squares use the packed pipe in a fixed order
+                f32x2 h[8];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float v = __fmul_rn(p[0], xv[0][e]);
-                    v = __fadd_rn(v, __fmul_rn(p[1], xv[1][e]));
-                    v = __fadd_rn(v, __fmul_rn(p[2], xv[2][e]));
-                    v = __fadd_rn(v, __fmul_rn(p[3], xv[3][e]));
+                for (int e = 0; e < 8; ++e) {
+                    float x0l, x0h, x1l, x1h, x2l, x2h, x3l, x3h;
+                    split_f32x2(xv[0][e], x0l, x0h);
+                    split_f32x2(xv[1][e], x1l, x1h);
+                    split_f32x2(xv[2][e], x2l, x2h);
+                    split_f32x2(xv[3][e], x3l, x3h);
+                    float vl = __fmul_rn(p[0], x0l), vh = __fmul_rn(p[0], x0h);
+                    vl = __fadd_rn(vl, __fmul_rn(p[1], x1l));
+                    vh = __fadd_rn(vh, __fmul_rn(p[1], x1h));
+                    vl = __fadd_rn(vl, __fmul_rn(p[2], x2l));
+                    vh = __fadd_rn(vh, __fmul_rn(p[2], x2h));
+                    vl = __fadd_rn(vl, __fmul_rn(p[3], x3l));
+                    vh = __fadd_rn(vh, __fmul_rn(p[3], x3h));
+                    const f32x2 v = make_f32x2(vl, vh);
                     h[e] = v;
-                    sh = fmaf(v, v, sh);
+                    sh2 = fma_rn2(v, v, sh2);
 #pragma unroll
-                    for (int st = 0; st < 4; ++st) sx = fmaf(xv[st][e], xv[st][e], sx);
+                    for (int st = 0; st < 4; ++st) sx2 = fma_rn2(xv[st][e], xv[st][e], sx2);
                 }
                 if (fold) {
                     if (have_prev) store_folded(grp);
                     uint32_t hb[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) hb[e] = __float_as_uint(h[e]);
+                    for (int e = 0; e < 8; ++e) {
+                        float lo, hi;
+                        split_f32x2(h[e], lo, hi);
+                        hb[2 * e] = __float_as_uint(lo);
+                        hb[2 * e + 1] = __float_as_uint(hi);
+                    }
                     tmem_st16(tl + kHCol + kCols * grp, hb);
                 } else {
                     store_out(h, c0 + kCols * grp, t - lane);
                 }
+            }
+            float sx, sh;
+            {
+                float a0, a1;
+                split_f32x2(sx2, a0, a1);
+                sx = a0 + a1;
+                split_f32x2(sh2, a0, a1);
+                sh = a0 + a1;
             }
             // this group's sums go out first: the finalizer needs only Σh² for
             // the fold scale, which gates every CTA's next tile
