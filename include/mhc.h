@@ -101,6 +101,53 @@ mhc_status mhc_pre_delayed(const uint16_t *x, const float *pre_in, const float *
  */
 size_t mhc_pre_workspace_bytes(int64_t T, int n, int C);
 
+/*
+ * mhc_pre_delayed_noalloc -- mhc_pre_delayed for callers that cannot
+ * allocate device memory, and so cannot pass a workspace: for example a
+ * serving engine that reserves all free device memory for its caches up front
+ * and forbids later allocations, a plugin that only receives tensors from its
+ * host application, or a latency-critical path that cannot afford
+ * cudaMalloc's implicit device synchronisation.  (The pages describe no such
+ * entry point; it has no counterpart there.)
+ *
+ * Same arguments, meaning, layouts and results as mhc_pre_delayed, minus the
+ * workspace.  It always runs the tensor-core kernel, with its scratch in a
+ * fixed device array of MHC_NOALLOC_SCRATCH_BYTES that the library holds on
+ * every GPU that loads it, until the process exits; it never calls
+ * cudaMalloc, cudaFree or any allocating routine.  The array fits at most two
+ * 16-CTA clusters, so the kernel uses at most 32 SMs: correct for every T,
+ * but slower than mhc_pre_delayed for large T.
+ *  C            multiple of 256, 256 <= C <= 5120 (else MHC_ERR_UNSUPPORTED)
+ * First call on a device: resolves the array's device address and sets the
+ * kernel up for that device (no allocation); make that first call outside any
+ * stream capture.  Nothing in the array needs to start at zero: each call
+ * rewrites the part it reads before reading it.  Every call shares the one
+ * array: calls whose kernels can overlap on the GPU (different streams, or
+ * graphs replayed concurrently) race on it and must be serialised by the
+ * caller.  Errors as mhc_pre_delayed.
+ */
+#define MHC_NOALLOC_SCRATCH_BYTES 5898240u
+mhc_status mhc_pre_delayed_noalloc(const uint16_t *x, const float *pre_in, const float *fn,
+                                   const float *bias, const float *alpha,
+                                   const uint16_t *norm_weight, int64_t T, int n, int C,
+                                   int sinkhorn_iters, float rms_eps, float norm_eps,
+                                   float sinkhorn_eps, float *pre_out, float *post_out,
+                                   float *comb_out, uint16_t *layer_input, float *logits_out,
+                                   void *stream);
+
+/*
+ * mhc_post -- the mHC post block ([A] "Result": the mhc_post call sites go
+ * through MHCPostOp; the post mixes the residual streams through comb and
+ * adds the post-gated sublayer output):
+ *   x_new[t][j][c] = bf16( sum_i comb[t][i][j] * x[t][i][c] + post[t][j] * y[t][c] )
+ * accumulated in fp32, rounded once.
+ *  x     [T, n, C] bf16;  y [T, C] bf16 (sublayer output)
+ *  comb  [T, n, n] fp32;  post [T, n] fp32 (from mhc_pre_delayed)
+ *  x_new [T, n, C] bf16; may be exactly x (in place); must not otherwise
+ *        overlap an input.
+ *  n == 4; C multiple of 8; T >= 0.  Errors as mhc_pre_delayed.
+ *  One kernel launch per call.
+ */
 mhc_status mhc_post(const uint16_t *x, const uint16_t *y, const float *comb,
                     const float *post, int64_t T, int n, int C, uint16_t *x_new,
                     void *stream);

@@ -18,8 +18,8 @@ import threading
 
 import torch
 
-__all__ = ["pre_delayed", "post", "pre_plan", "device_status", "workspace_for", "library_path",
-           "load_library", "MhcError", "SINKHORN_ITERS"]
+__all__ = ["pre_delayed", "pre_delayed_noalloc", "post", "pre_plan", "device_status", "workspace_for",
+           "library_path", "load_library", "MhcError", "SINKHORN_ITERS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "_build", "libmhc.so")
@@ -57,6 +57,8 @@ def load_library():
         lib.mhc_pre_delayed.argtypes = [P, P, P, P, P, P, I64, I, I, I, F, F, F, P, P, P, P, P,
                                          P, ctypes.c_size_t, P]
         lib.mhc_pre_delayed.restype = I
+        lib.mhc_pre_delayed_noalloc.argtypes = [P, P, P, P, P, P, I64, I, I, I, F, F, F, P, P, P, P, P, P]
+        lib.mhc_pre_delayed_noalloc.restype = I
         lib.mhc_pre_workspace_bytes.argtypes = [I64, I, I]
         lib.mhc_pre_workspace_bytes.restype = ctypes.c_size_t
         lib.mhc_post.argtypes = [P, P, P, P, I64, I, I, P, P]
@@ -170,6 +172,37 @@ def pre_delayed(x: torch.Tensor, pre_in: torch.Tensor, fn: torch.Tensor, bias: t
                              float(sinkhorn_eps), *outs, ws_ptr, ws_bytes, _stream_ptr(stream, dev))
     _check("mhc_pre_delayed", st)
     return o
+
+
+def pre_delayed_noalloc(x: torch.Tensor, pre_in: torch.Tensor, fn: torch.Tensor, bias: torch.Tensor,
+                        alpha: torch.Tensor, norm_weight: torch.Tensor | None = None, *,
+                        sinkhorn_iters: int = SINKHORN_ITERS, rms_eps: float = 1e-6,
+                        norm_eps: float = 1e-6, sinkhorn_eps: float = 1e-6, out: dict,
+                        return_logits: bool = False, stream=None) -> dict:
+    """``mhc_pre_delayed_noalloc``: the delayed pre block for callers that
+    cannot allocate device memory (the library uses a fixed scratch array of
+    ``MHC_NOALLOC_SCRATCH_BYTES`` per GPU instead of a workspace).  ``out``
+    must hold preallocated "pre", "post", "comb", "layer_input" (and
+    "logits" when ``return_logits``); nothing is allocated here."""
+    lib = load_library()
+    if x.dim() != 3:
+        raise ValueError("x must be [T, n, C]")
+    T, n, C = x.shape
+    dev = x.device
+    args = [
+        _dev_ptr(x, "x", torch.bfloat16, dev), _dev_ptr(pre_in, "pre_in", torch.float32, dev),
+        _dev_ptr(fn, "fn", torch.float32, dev), _dev_ptr(bias, "bias", torch.float32, dev),
+        _dev_ptr(alpha, "alpha", torch.float32, dev),
+        _dev_ptr(norm_weight, "norm_weight", torch.bfloat16, dev),
+    ]
+    outs = [_dev_ptr(out["pre"], "pre", torch.float32, dev), _dev_ptr(out["post"], "post", torch.float32, dev),
+            _dev_ptr(out["comb"], "comb", torch.float32, dev),
+            _dev_ptr(out["layer_input"], "layer_input", torch.bfloat16, dev),
+            _dev_ptr(out.get("logits") if return_logits else None, "logits", torch.float32, dev)]
+    st = lib.mhc_pre_delayed_noalloc(*args, T, n, C, int(sinkhorn_iters), float(rms_eps), float(norm_eps),
+                                     float(sinkhorn_eps), *outs, _stream_ptr(stream, dev))
+    _check("mhc_pre_delayed_noalloc", st)
+    return out
 
 
 def post(x: torch.Tensor, y: torch.Tensor, comb: torch.Tensor, post_gate: torch.Tensor, *,

@@ -1,0 +1,119 @@
+// pre_noalloc.cu -- mhc_pre_delayed_noalloc: the delayed pre block for
+// callers that cannot allocate device memory.
+//
+// Who needs this: mhc_pre_delayed takes a caller-provided workspace (the
+// per-call copy of fn split into three bf16 planes that the tensor-core
+// kernel streams from).  Some callers have no way to provide one: a serving
+// engine that reserves all free device memory for its caches up front and
+// forbids any later cudaMalloc, a plugin that only receives tensors from its
+// host application and owns no allocator, or a latency-critical path where
+// cudaMalloc's implicit device synchronisation is not acceptable.  This entry
+// point runs the same tensor-core kernel with its scratch in a fixed array
+// that lives in this file; it never calls cudaMalloc, cudaFree or any
+// allocating routine.
+//
+// Limit: the array holds the fn planes for at most kNoAllocClusters 16-CTA
+// clusters (2 x 16 x 20 x 9 KB = 5,898,240 bytes for C = 5120), so the kernel
+// runs on at most 32 SMs here: correct for any token count, slower for large
+// ones than mhc_pre_delayed on the whole GPU.  Every GPU that loads the
+// library holds the array until the process exits.
+#include "../../include/mhc.h"
+
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+namespace mhc {
+bool pre_tc_supports(int C);
+int pre_tc_prepare();
+size_t pre_tc_workspace_bytes(int64_t T, int C, int max_clusters);
+cudaError_t launch_pre_tc(const uint16_t* x, const float* pre_in, const float* fn, const float* bias,
+                          const float* alpha, const uint16_t* norm_w, int64_t T, int C, int iters,
+                          float rms_eps, float norm_eps, float sk_eps, float* pre_out, float* post_out,
+                          float* comb_out, uint16_t* layer_input, float* logits_out, void* workspace,
+                          cudaStream_t stream, int max_clusters);
+}  // namespace mhc
+
+namespace {
+
+constexpr int kNoAllocClusters = 2;
+constexpr size_t kNoAllocBytes = MHC_NOALLOC_SCRATCH_BYTES;
+
+// The scratch itself.  Its name is a host-side stand-in in host code, not a
+// device address: host code uses the address cudaGetSymbolAddress returns.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+int g_clusters[kMaxDevices] = {};   // co-resident tensor-core clusters; 0 = not set up
+
+// Once per device, with that device current: resolve the array's device
+// address and set up the kernel (attributes, occupancy).  No allocation.
+bool setup(int dev, void** scratch, int* clusters) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return false;
+        const int n = mhc::pre_tc_prepare();
+        if (n <= 0) return false;
+        g_clusters[dev] = n < kNoAllocClusters ? n : kNoAllocClusters;
+        g_scratch_ptr[dev] = p;
+    }
+    *scratch = g_scratch_ptr[dev];
+    *clusters = g_clusters[dev];
+    return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
+    if (!a || !b || an == 0 || bn == 0) return false;
+    uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + bn && b0 < a0 + an;
+}
+
+}  // namespace
+
+extern "C" mhc_status mhc_pre_delayed_noalloc(const uint16_t* x, const float* pre_in, const float* fn,
+                                              const float* bias, const float* alpha,
+                                              const uint16_t* norm_weight, int64_t T, int n, int C,
+                                              int sinkhorn_iters, float rms_eps, float norm_eps,
+                                              float sinkhorn_eps, float* pre_out, float* post_out,
+                                              float* comb_out, uint16_t* layer_input, float* logits_out,
+                                              void* stream) {
+    if (T < 0 || n < 1 || C < 1 || sinkhorn_iters < 1) return MHC_ERR_INVALID_ARGUMENT;
+    if (n != 4 || !mhc::pre_tc_supports(C)) return MHC_ERR_UNSUPPORTED;
+    if (!(rms_eps >= 0.f) || !(norm_eps >= 0.f) || !(sinkhorn_eps >= 0.f)) return MHC_ERR_INVALID_ARGUMENT;
+    if (T == 0) return MHC_OK;
+    if (T > ((int64_t)1 << 40) / ((int64_t)n * C)) return MHC_ERR_UNSUPPORTED;
+    const void* req[] = {x, pre_in, fn, bias, alpha, pre_out, post_out, comb_out, layer_input};
+    for (const void* p : req)
+        if (!p || !aligned16(p)) return MHC_ERR_INVALID_ARGUMENT;
+    if ((norm_weight && !aligned16(norm_weight)) || (logits_out && !aligned16(logits_out)))
+        return MHC_ERR_INVALID_ARGUMENT;
+    const int M = 2 * n + n * n;
+    const size_t xb = (size_t)T * n * C * 2, pb = (size_t)T * n * 4, cb = (size_t)T * n * n * 4;
+    const size_t lib = (size_t)T * C * 2, lob = (size_t)T * M * 4;
+    const size_t fnb = (size_t)M * n * C * 4, bb = (size_t)M * 4, ab = 12, nwb = (size_t)C * 2;
+    struct R { const void* p; size_t n; };
+    const R ins[] = {{x, xb}, {pre_in, pb}, {fn, fnb}, {bias, bb}, {alpha, ab}, {norm_weight, nwb}};
+    const R outs[] = {{pre_out, pb}, {post_out, pb}, {comb_out, cb}, {layer_input, lib}, {logits_out, lob}};
+    for (const R& o : outs) {
+        for (const R& i : ins)
+            if (overlaps(o.p, o.n, i.p, i.n)) return MHC_ERR_INVALID_ARGUMENT;
+        for (const R& o2 : outs)
+            if (&o != &o2 && overlaps(o.p, o.n, o2.p, o2.n)) return MHC_ERR_INVALID_ARGUMENT;
+    }
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MHC_ERR_CUDA;
+    void* scratch = nullptr;
+    int clusters = 0;
+    if (!setup(dev, &scratch, &clusters)) return MHC_ERR_CUDA;
+    // the shapes above always fit; the check keeps the stated limit explicit
+    if (mhc::pre_tc_workspace_bytes(T, C, clusters) > kNoAllocBytes) return MHC_ERR_UNSUPPORTED;
+    cudaError_t e = mhc::launch_pre_tc(x, pre_in, fn, bias, alpha, norm_weight, T, C, sinkhorn_iters, rms_eps,
+                                       norm_eps, sinkhorn_eps, pre_out, post_out, comb_out, layer_input,
+                                       logits_out, scratch, static_cast<cudaStream_t>(stream), clusters);
+    return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA;
+}
