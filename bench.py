@@ -86,27 +86,36 @@ def load_peaks():
     return 6800.0, "fallback"
 
 
-def kernel_source_hash():
+# sources each kernel is built from: a committed ncu traffic figure is used
+# only while these files are unchanged
+KERNEL_SOURCES = {
+    "mhc_pre_delayed": ("pre_tc.cu", "sm100.cuh", "common.cuh"),
+    "mhc_post": ("post.cu", "common.cuh"),
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mhc_hyper_connection_pre_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    for fn in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, or
-    None when the kernels changed since that capture."""
+    """DRAM bytes (read + write) per launch of `kernel` at the benchmark's
+    size, from the committed ncu summary; None when that kernel's sources
+    changed since the capture."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    if d.get("source_hash") != kernel_source_hash():
-        return None
     k = d.get("kernels", {}).get(kernel)
-    return None if k is None else k.get("dram_bytes_per_launch_full_size")
+    if k is None or k.get("source_hash") != kernel_source_hash(kernel):
+        return None
+    return k.get("dram_bytes_per_launch")
 
 
 class ClockSampler:
