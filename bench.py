@@ -5,9 +5,9 @@ C = 5120, 20 Sinkhorn iterations, fused RMSNorm fold on; one step = one
 mhc_pre_delayed + one mhc_post over the batch (every step of the seam).
 `value` = tokens/s (whole job, all ranks).  Inputs (x 671 MB) are larger than
 L2 (129 MB), so no explicit flush is needed between steps.  Secondary keys
-carry the decode sweep (graph-captured mhc_pre_delayed, T = 1..128, median of
-5 x 200 replays), the 80-seam decode chain (one graph) and per-kernel HBM
-roofline figures.
+carry the decode sweep (T = 1..128: a graph of 20 back-to-back calls, as in a
+model step, median of 5 x 50 replays, per call), the 80-seam decode chain (one
+graph) and per-kernel HBM roofline figures.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--skip-decode] [--skip-cpu]
@@ -36,6 +36,7 @@ METRIC = "mHC seam µs/call T=1–128 (graph); tokens/s + HBM GB/s vs peak at T=
 T_PREFILL, N_STREAMS, HIDDEN, ITERS = 16384, 4, 5120, 20
 DECODE_T = (1, 2, 4, 8, 16, 32, 64, 128)
 CHAIN_SEAMS, CHAIN_T = 80, 4
+DECODE_REPS = 20   # calls per captured graph in the decode sweep
 
 # algorithmic bytes (what the method must move; fn counted once per call)
 PRE_BYTES_PER_TOKEN = 40960 + 10240 + 16 + 16 + 16 + 64   # x, layer_input, pre_in, pre, post, comb
@@ -337,24 +338,29 @@ def run_ours(args, rank, world, local):
             xn = torch.empty_like(dd["x"])
             torch.cuda.synchronize()
             res = {}
-            for name, fn_ in (
-                ("pre", lambda st: mhc.pre_delayed(dd["x"], dd["pre_in"], dd["fn"], dd["bias"],
-                                                   dd["alpha"], dd["norm_w"], out=o, stream=st)),
-                ("seam", lambda st: (mhc.pre_delayed(dd["x"], dd["pre_in"], dd["fn"], dd["bias"],
-                                                     dd["alpha"], dd["norm_w"], out=o, stream=st),
-                                     mhc.post(dd["x"], dd["y"], o["comb"], o["post"], out=xn, stream=st)))):
-                g = SeamGraph(fn_, s)
-                g.replay(20)
+            def pre_call(st):
+                mhc.pre_delayed(dd["x"], dd["pre_in"], dd["fn"], dd["bias"], dd["alpha"], dd["norm_w"],
+                                out=o, stream=st)
+
+            def seam_call(st):
+                pre_call(st)
+                mhc.post(dd["x"], dd["y"], o["comb"], o["post"], out=xn, stream=st)
+
+            for name, one in (("pre", pre_call), ("seam", seam_call)):
+                # DECODE_REPS calls back to back in one graph: the GPU time per
+                # call, not the host's graph-launch rate
+                g = SeamGraph(lambda st, one=one: [one(st) for _ in range(DECODE_REPS)], s)
+                g.replay(5)
                 meds = []
                 for _ in range(5):
                     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     a.record(s)
-                    g.replay(200)
+                    g.replay(50)
                     b.record(s)
                     s.synchronize()
-                    meds.append(a.elapsed_time(b) * 1e3 / 200)
+                    meds.append(a.elapsed_time(b) * 1e3 / (50 * DECODE_REPS))
                 res[name + "_us"] = round(statistics.median(meds), 3)
-                res[name + "_launches"] = g.kernel_nodes
+                res[name + "_launches"] = g.kernel_nodes / DECODE_REPS
                 g.close()
             decode[str(Td)] = res
         # 80 seams, each with its own weights, pre-mix carried seam to seam

@@ -166,10 +166,13 @@ mhc_status mhc_device_status(void);
 
 /*
  * Launch plan of mhc_pre_delayed for a shape, without launching (host only,
- * no device needed for the shape checks).  kernel: 1 = CUDA-core cluster
- * kernel (8-token tiles), 2 = tensor-core kernel (128-token tiles, used from
- * 256 tokens on when C is a multiple of 256 and at most 5120); grid/cluster:
- * CTAs launched and CTAs per cluster; tokens_per_tile.
+ * no device needed for the shape checks).  kernel: 1 = cluster kernel
+ * (warp-level MMA, one tile of up to 32 tokens per 16-CTA cluster, the tokens
+ * spread evenly over the co-resident clusters), 2 = tensor-core kernel
+ * (128-token tiles, used from 256 tokens on when C is a multiple of 256 and at
+ * most 5120); grid/cluster: CTAs launched and CTAs per cluster (grid 0 when no
+ * device is current); tokens_per_tile (for kernel 1 without a current device:
+ * min(T, 32)).
  * Returns the status mhc_pre_delayed would return for the shape checks.
  * Any output pointer may be NULL.
  */

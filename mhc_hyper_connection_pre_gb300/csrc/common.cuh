@@ -76,14 +76,46 @@ __device__ __forceinline__ uint32_t f32x2_to_bf16x2(f32x2 a) {
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
 __device__ __forceinline__ void st_stream(uint4* p, const uint4& v) { __stcs(p, v); }
 
+// Hardware reciprocal (PTX rcp.approx.ftz: about 1 ulp, one instruction).
+// The sums it inverts here are at least 4 * eps > 0, far from the
+// subnormal range, so flushing subnormals changes nothing.
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// Sinkhorn on a 4x4 row-major matrix that already holds iteration 1's row
+// softmax plus eps: iteration 1 finishes with a column normalisation,
+// iterations 2..iters normalise rows then columns.  One thread; the chain of
+// 2*iters dependent normalisations is the latency, so each one multiplies by
+// one reciprocal of the sum.
+__device__ __forceinline__ void sinkhorn_iterations(float (&P)[16], int iters) {
+    for (int it = 0; it < iters; ++it) {
+        if (it > 0) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float inv = rcp_approx(((P[4 * i] + P[4 * i + 1]) + P[4 * i + 2]) + P[4 * i + 3]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) P[4 * i + j] *= inv;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float inv = rcp_approx(((P[j] + P[4 + j]) + P[8 + j]) + P[12 + j]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) P[4 * i + j] *= inv;
+        }
+    }
+}
+
 // Per-token gates and comb from the 2n+n^2 logits, in fp32, by one thread.
 // pre = sigmoid(l[0:4]), post = 2 sigmoid(l[4:8]); comb = Sinkhorn on the
 // 4x4 row-major comb logits l[8:24]: iteration 1 is the row softmax (max
 // subtracted per row) plus eps on every entry, then a column normalisation;
 // iterations 2..iters normalise rows then columns.  Normalisations multiply
-// by the hardware reciprocal of the sum (__fdividef): a relative error of a
-// few fp32 ulps per step, far inside the 2e-5 gate tolerance, and no IEEE
-// division subroutine on the latency-critical path.
+// by the hardware reciprocal of the sum: a relative error of a few fp32 ulps
+// per step, far inside the 2e-5 gate tolerance.
 __device__ __forceinline__ void gates_and_comb(const float (&l)[kLogits], int iters, float eps,
                                                float (&pre)[4], float (&post)[4],
                                                float (&P)[16]) {
@@ -97,28 +129,13 @@ __device__ __forceinline__ void gates_and_comb(const float (&l)[kLogits], int it
         float mx = fmaxf(fmaxf(l[8 + 4 * i], l[9 + 4 * i]), fmaxf(l[10 + 4 * i], l[11 + 4 * i]));
         float e0 = expf(l[8 + 4 * i] - mx), e1 = expf(l[9 + 4 * i] - mx);
         float e2 = expf(l[10 + 4 * i] - mx), e3 = expf(l[11 + 4 * i] - mx);
-        float inv = __fdividef(1.0f, ((e0 + e1) + e2) + e3);
+        float inv = rcp_approx(((e0 + e1) + e2) + e3);
         P[4 * i + 0] = e0 * inv + eps;
         P[4 * i + 1] = e1 * inv + eps;
         P[4 * i + 2] = e2 * inv + eps;
         P[4 * i + 3] = e3 * inv + eps;
     }
-    for (int it = 0; it < iters; ++it) {
-        if (it > 0) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float inv = __fdividef(1.0f, ((P[4 * i] + P[4 * i + 1]) + P[4 * i + 2]) + P[4 * i + 3]);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) P[4 * i + j] *= inv;
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            float inv = __fdividef(1.0f, ((P[j] + P[4 + j]) + P[8 + j]) + P[12 + j]);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) P[4 * i + j] *= inv;
-        }
-    }
+    sinkhorn_iterations(P, iters);
 }
 
 }  // namespace mhc

@@ -16,7 +16,8 @@ cudaError_t launch_pre_cluster(const uint16_t* x, const float* pre_in, const flo
                                float sk_eps, float* pre_out, float* post_out, float* comb_out,
                                uint16_t* layer_input, float* logits_out, cudaStream_t stream,
                                int max_clusters);
-int pre_cluster_tile_tokens();
+int pre_cluster_tile_tokens(int64_t T, int max_clusters);
+int pre_cluster_max_tile();
 int pre_cluster_ctas();
 int pre_cluster_prepare(int C);
 bool pre_tc_supports(int C);
@@ -29,6 +30,7 @@ cudaError_t launch_pre_tc(const uint16_t* x, const float* pre_in, const float* f
                           float* comb_out, uint16_t* layer_input, float* logits_out, void* workspace,
                           cudaStream_t stream, int max_clusters);
 cudaError_t read_device_status(unsigned int* status);
+cudaError_t read_decode_status(unsigned int* status);
 }  // namespace mhc
 
 namespace {
@@ -36,7 +38,8 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int kMaxC = 6144;
 // From this many tokens on, the tensor-core kernel (128-token tiles) runs the
-// pre block; below it the CUDA-core kernel (8-token tiles) has lower latency.
+// pre block; below it the cluster kernel (tiles of up to 32 tokens, one per
+// cluster, warp-level MMA) has lower latency.
 constexpr int64_t kTcMinTokens = 256;
 
 // Per-device cache: SM count, and the cluster kernel's set-up result per
@@ -129,9 +132,10 @@ int mhc_version(void) { return (0 << 16) | 2; }
 
 mhc_status mhc_device_status(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return MHC_ERR_CUDA;
-    unsigned int v = 0;
+    unsigned int v = 0, w = 0;
     if (mhc::read_device_status(&v) != cudaSuccess) return MHC_ERR_CUDA;
-    return v ? MHC_ERR_TIMEOUT : MHC_OK;
+    if (mhc::read_decode_status(&w) != cudaSuccess) return MHC_ERR_CUDA;
+    return (v | w) ? MHC_ERR_TIMEOUT : MHC_OK;
 }
 
 mhc_status mhc_pre_delayed_plan(int64_t T, int n, int C, int* kernel, int* grid, int* cluster,
@@ -139,17 +143,19 @@ mhc_status mhc_pre_delayed_plan(int64_t T, int n, int C, int* kernel, int* grid,
     mhc_status st = check_pre_shape(T, n, C, 1);
     if (st != MHC_OK) return st;
     const bool tc = use_tc(T, C);
-    const int tt = tc ? mhc::pre_tc_tile_tokens() : mhc::pre_cluster_tile_tokens();
     if (kernel) *kernel = tc ? 2 : 1;
     if (cluster) *cluster = mhc::pre_cluster_ctas();
+    int dev = T > 0 && (grid || tokens_per_tile) ? current_device() : -1;
+    int mc = dev < 0 ? 0 : (tc ? tc_clusters(dev) : max_clusters(dev, C));
+    int tt = tc ? mhc::pre_tc_tile_tokens()
+                : (mc > 0 ? mhc::pre_cluster_tile_tokens(T, mc)
+                          : (int)(T < mhc::pre_cluster_max_tile() ? (T > 0 ? T : 1) : mhc::pre_cluster_max_tile()));
     if (tokens_per_tile) *tokens_per_tile = tt;
     if (grid) {
         *grid = 0;
-        if (T > 0) {
-            int dev = current_device();
-            int mc = dev < 0 ? 0 : (tc ? tc_clusters(dev) : max_clusters(dev, C));
+        if (T > 0 && mc > 0) {
             int64_t tiles = (T + tt - 1) / tt;
-            if (mc > 0) *grid = (int)((tiles < mc ? tiles : mc) * mhc::pre_cluster_ctas());
+            *grid = (int)((tiles < mc ? tiles : mc) * mhc::pre_cluster_ctas());
         }
     }
     return MHC_OK;

@@ -1,5 +1,6 @@
-// pre_cluster.cu -- delayed mHC pre block on CUDA cores, one cluster of 16
-// CTAs per token tile (sm_103a).
+// pre_cluster.cu -- delayed mHC pre block for small token counts (decode and
+// short prefill): one cluster of 16 CTAs per tile of up to 32 tokens, the
+// projection on the tensor cores through warp-level MMA (sm_103a).
 //
 // What it computes (vLLM page "Use AITER mHC for the delayed pre block":
 // commit message, sections "Why V4.1 cannot just reuse MHCPreOp", "Approach"
@@ -10,39 +11,49 @@
 //   h = fp32 collapse of x with the INCOMING pre-mix; layer_input = bf16(h)
 //   or bf16(h * rsqrt(mean h^2 + eps) * w).
 //
-// Decomposition.  A cluster of 16 CTAs owns a tile of 8 tokens; CTA r owns a
-// slice of C/16 columns of all four streams (so it can collapse them) and
-// keeps the matching K-slice of fn in registers for the whole launch:
-// warp w holds logits 2w and 2w+1, lane l holds 8-column groups
-// q = l, l+32, ... of the slice.  Per tile:
-//   1. the tile's x slice (and pre_in) arrives by cp.async, double-buffered
-//      one tile ahead;
-//   2. each warp forms its two partial dot products for the 8 tokens and
-//      reduces them across lanes (a reduce-scatter butterfly, fixed order);
-//      each thread collapses one (token, 8-column) item, keeping h in
-//      registers, and forms its sum x^2 and sum h^2;
-//   3. cluster barrier; CTA r < 8 sums the 16 CTAs' partials of token r over
-//      distributed shared memory in rank order, computes r, the logits, the
-//      gates and the Sinkhorn comb in one thread, writes them, and writes the
-//      token's fold scale into every CTA of the cluster;
-//   4. cluster barrier; every CTA writes its layer_input slice.
-// No global scratch memory, no atomics, no spin waits: the only waits are
-// hardware cluster barriers, and every reduction has a fixed order, so the
-// results are deterministic.
+// Decomposition.  CTA r of a cluster owns a slice of the columns (8-column
+// groups spread as evenly as possible over the 16 CTAs) of all four streams:
+// its K_r = 4 x ncols entries of x_flat, in 32-wide chunks.  Chunk q belongs
+// to warp q mod 12, which keeps the 24 x 32 block of fn for it in registers
+// (fp32) for the whole launch.  Per tile of TT tokens:
+//   1. the tile's x slice and pre_in arrive by cp.async (the next tile's load
+//      is issued as soon as this one's MMA is done);
+//   2. warps 2..11 collapse one token at a time (h to shared memory, or
+//      straight to layer_input without the fold) and push the token's
+//      partial sum x^2 and sum h^2 to the CTA that finalises it;
+//   3. every warp multiplies its chunks on the tensor cores:
+//      mma.sync m16n8k8 with tf32 inputs and fp32 accumulation, tokens as M,
+//      the 24 logits as three n-tiles of 8.  x (bf16) is exact in tf32; fn is
+//      split into hi = tf32(fn) and lo = fn - hi (exact in fp32), two MMAs per
+//      block, which leaves a relative error below 2^-21 on each product;
+//   4. the 12 warps' partial dot products are summed in shared memory in a
+//      fixed order and pushed to the finalising CTA;
+//   5. CTA r finalises tokens r and r + 16 of the tile (warps 0 and 1): it
+//      sums the 16 CTAs' partials in rank order, sends the fold scale to every
+//      CTA at once, then forms r, the logits, the gates and the Sinkhorn comb;
+//   6. warps 2..11 fold h with the scale and store layer_input.
+// Every push is an st.async into the receiver's shared memory that completes
+// bytes on the receiver's mbarrier, so no CTA waits at a cluster barrier for
+// the slowest one inside a tile; all waits are bounded (a timeout sets the
+// device status word).  Every reduction has a fixed order: results are
+// deterministic.
 #include "common.cuh"
-
-#include <cooperative_groups.h>
-
-namespace cg = cooperative_groups;
+#include "sm100.cuh"
 
 namespace mhc {
+namespace dec {
 
-constexpr int kClusterCtas = 16;   // CTAs per cluster = column slices of C
-constexpr int kPreThreads = 384;   // 12 warps x 2 logits = 24 logits
-constexpr int kTileTokens = 8;     // tokens per cluster tile
-constexpr int kPartStride = 26;    // 24 dot products, sum x^2, sum h^2
+constexpr int kCtas = 16;                  // CTAs per cluster = column slices
+constexpr int kWarps = 12;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kMaxTile = 32;               // tokens per cluster tile
+constexpr int kSlots = kMaxTile / kCtas;   // tokens each CTA finalises per tile
+constexpr int kRowWarp0 = kSlots;          // warps kRowWarp0.. collapse and fold
+constexpr int kRowWarps = kWarps - kRowWarp0;
+constexpr int kSqBytes = kCtas * 2 * 4;            // per token: 16 x (sum x^2, sum h^2)
+constexpr int kDotsBytes = kCtas * kLogits * 4;    // per token: 16 x 24 partial dots
 
-struct PreArgs {
+struct Args {
     const uint16_t* x;
     const float* pre_in;
     const float* fn;
@@ -59,313 +70,437 @@ struct PreArgs {
     uint16_t* layer_input;
     float* logits_out;
     int64_t ntiles;
-    int lcmax;  // max 8-column groups per CTA slice
+    int tile;      // tokens per tile (1..kMaxTile)
+    int lcmax;     // max 8-column groups per CTA slice
+    int xstride;   // bytes per token row of the x tile in shared memory
 };
 
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
-    uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
-    int n = valid ? 16 : 0;  // 0 bytes read: the 16 destination bytes are zero-filled
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(n)
-                 : "memory");
+// Shared-memory carve-up (bytes), in this order.
+struct Layout {
+    int xs, hs, red, pin, nw, sq, dots, scale, bars, abort_flag, total;
+};
+__host__ __device__ inline int dec_xstride(int lcmax) {
+    // 64 bytes per group (4 streams x 8 bf16); rows an odd multiple of 64
+    // bytes apart so that the MMA's row loads of 8 tokens hit distinct banks
+    return ((64 * lcmax + 127) / 128) * 128 + 64;
+}
+__host__ __device__ inline Layout dec_layout(int lcmax) {
+    Layout L;
+    int o = 0;
+    L.xs = o;    o += kMaxTile * dec_xstride(lcmax);
+    L.hs = o;    o += kMaxTile * 8 * lcmax * 4;
+    L.red = o;   o += kWarps * kMaxTile * kLogits * 4;
+    L.pin = o;   o += kMaxTile * 16;
+    L.nw = o;    o += ((8 * lcmax * 2 + 15) / 16) * 16;
+    L.sq = o;    o += kSlots * kCtas * 2 * 4;
+    L.dots = o;  o += 2 * kSlots * kCtas * kLogits * 4;
+    L.scale = o; o += kMaxTile * 4;
+    L.bars = o;  o += 8 * 8;
+    L.abort_flag = o; o += 16;
+    L.total = o;
+    return L;
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
 
-// Reduce 16 per-lane values over the 32 lanes of a warp.  After the call
-// lane l holds in v[0] the full sum of value index (l >> 1) & 15.
-__device__ __forceinline__ void warp_reduce_scatter16(float (&v)[16], int lane) {
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-        const int half = 8 >> s, bit = 16 >> s;
-        const bool upper = (lane & bit) != 0;
-#pragma unroll
-        for (int i = 0; i < half; ++i) {
-            float send = upper ? v[i] : v[i + half];
-            float keep = upper ? v[i + half] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
-        }
-    }
-    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+__device__ __forceinline__ uint32_t tf32_rna(float v) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
+    return r;
+}
+// D += A (16x8, tf32, row) * B (8x8, tf32, col); fp32 accumulators.
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 template <int JMAX>
-__global__ void __launch_bounds__(kPreThreads, 1) pre_cluster_kernel(const PreArgs a) {
-    cg::cluster_group cluster = cg::this_cluster();
-    const int rank = (int)cluster.block_rank();
-    const int64_t cluster_id = blockIdx.x / kClusterCtas;
-    const int64_t nclusters = gridDim.x / kClusterCtas;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+__global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
+    const int rank = (int)cluster_ctarank();
+    const int64_t cid = cluster_id_x();
+    const int64_t ncl = ncluster_x();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, t4 = lane & 3;
     const int C = a.C, K = 4 * C, nch = C >> 3;
-    const int ch0 = rank * nch / kClusterCtas;
-    const int lc = (rank + 1) * nch / kClusterCtas - ch0;  // 8-column groups of this CTA
-    const int qn = 4 * lc;                                  // (stream, group) pairs
+    const int ch0 = rank * nch / kCtas;
+    const int lc = (rank + 1) * nch / kCtas - ch0;   // 8-column groups of this CTA
+    const int ncols = 8 * lc;
+    const int c0 = 8 * ch0;
     const bool fold = a.norm_w != nullptr;
+    const int TT = a.tile;
 
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    const int qstride = 4 * a.lcmax;
-    uint4* xs = reinterpret_cast<uint4*>(smem_raw);                       // [2][TT][qstride]
-    float* pin = reinterpret_cast<float*>(xs + 2 * kTileTokens * qstride);  // [2][TT][4]
-    float* part = pin + 2 * kTileTokens * 4;                                // [TT][26]
-    float* scale = part + kTileTokens * kPartStride;                        // [TT]
-    float* red = scale + kTileTokens;                                       // [2][TT][lcmax]
+    extern __shared__ __align__(128) unsigned char smem[];
+    const Layout L = dec_layout(a.lcmax);
+    unsigned char* xs = smem + L.xs;
+    float* hs = reinterpret_cast<float*>(smem + L.hs);
+    float* red = reinterpret_cast<float*>(smem + L.red);
+    float* pin = reinterpret_cast<float*>(smem + L.pin);
+    uint16_t* nw = reinterpret_cast<uint16_t*>(smem + L.nw);
+    float* inbox_sq = reinterpret_cast<float*>(smem + L.sq);      // [slot][src][2]
+    float* inbox_dots = reinterpret_cast<float*>(smem + L.dots);  // [parity][slot][src][24]
+    float* scale_in = reinterpret_cast<float*>(smem + L.scale);   // [token]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+    uint64_t* sq_full = bars;              // [slot]
+    uint64_t* dots_full = bars + kSlots;   // [parity][slot]
+    uint64_t* scale_full = bars + 3 * kSlots;
+    volatile int* abort = reinterpret_cast<volatile int*>(smem + L.abort_flag);
+    const int hstride = 8 * a.lcmax;       // floats per token row of h
 
-    // ---- this warp's two rows of fn over this CTA's K-slice, in registers
-    const int m0 = 2 * warp;
-    float w[JMAX][2][8];
+    auto tile_tokens = [&](int64_t tile) -> int {
+        const int64_t left = a.T - tile * TT;
+        return (int)(left < TT ? left : TT);
+    };
+
+    // ---- set-up: barriers armed for the first tile
+    int64_t tile = cid;
+    int nv = tile_tokens(tile);
+    if (tid == 0) {
+        for (int i = 0; i < 3 * kSlots + 1; ++i) mbar_init(&bars[i], 1);
+        *abort = 0;
+        fence_mbar_init_cluster();
+        for (int s = 0; s < kSlots; ++s)
+            if (kCtas * s + rank < nv) {
+                mbar_arrive_expect_tx(&sq_full[s], kSqBytes);
+                mbar_arrive_expect_tx(&dots_full[s], kDotsBytes);
+            }
+        mbar_arrive_expect_tx(scale_full, 4 * nv);
+    }
+
+    // ---- this warp's fn blocks, fp32 in registers: chunk q = warp + 12 j,
+    //      n-tile nt (logits 8 nt .. 8 nt + 7), lane (g, t4) holds logit
+    //      8 nt + g at local K 32 q + 8 t4 .. + 7
+    float b[JMAX][3][8];
 #pragma unroll
     for (int j = 0; j < JMAX; ++j) {
-        const int q = lane + 32 * j;
-        if (q < qn) {
-            const int i = q / lc, cc = q - i * lc;
-            const int64_t k = (int64_t)i * C + (int64_t)(ch0 + cc) * 8;
+        const int q = warp + kWarps * j;
+        if (q < lc) {
+            const int kl = 32 * q + 8 * t4;
+            const int i = kl / ncols, cc = kl - i * ncols;
+            const float* src = a.fn + (int64_t)i * C + c0 + cc;
 #pragma unroll
-            for (int mm = 0; mm < 2; ++mm) {
-                const float4* src = reinterpret_cast<const float4*>(a.fn + (int64_t)(m0 + mm) * K + k);
-                float4 u = __ldg(src), v = __ldg(src + 1);
-                w[j][mm][0] = u.x; w[j][mm][1] = u.y; w[j][mm][2] = u.z; w[j][mm][3] = u.w;
-                w[j][mm][4] = v.x; w[j][mm][5] = v.y; w[j][mm][6] = v.z; w[j][mm][7] = v.w;
+            for (int nt = 0; nt < 3; ++nt) {
+                const float4* p = reinterpret_cast<const float4*>(src + (int64_t)(8 * nt + g) * K);
+                const float4 u = __ldg(p), v = __ldg(p + 1);
+                b[j][nt][0] = u.x; b[j][nt][1] = u.y; b[j][nt][2] = u.z; b[j][nt][3] = u.w;
+                b[j][nt][4] = v.x; b[j][nt][5] = v.y; b[j][nt][6] = v.z; b[j][nt][7] = v.w;
             }
         } else {
 #pragma unroll
-            for (int mm = 0; mm < 2; ++mm)
+            for (int nt = 0; nt < 3; ++nt)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) w[j][mm][e] = 0.f;
+                for (int e = 0; e < 8; ++e) b[j][nt][e] = 0.f;
         }
     }
 
-    auto issue_tile = [&](int64_t tile, int buf) {
-        const int64_t t0 = tile * kTileTokens;
-        for (int idx = threadIdx.x; idx < kTileTokens * qn; idx += kPreThreads) {
-            const int tt = idx / qn, q = idx - tt * qn;
-            const int i = q / lc, cc = q - i * lc;
-            const int64_t t = t0 + tt;
-            const bool ok = t < a.T;
-            const uint16_t* src = a.x + ((ok ? t : 0) * 4 + i) * (int64_t)C + (int64_t)(ch0 + cc) * 8;
-            cp_async16(xs + (buf * kTileTokens + tt) * qstride + q, src, ok);
+    // x tile (and pre_in) of a tile into shared memory: row tt, local K order
+    // (stream, column) so that local k = i * ncols + column
+    auto issue_tile = [&](int64_t tl, int n) {
+        const int64_t t0 = tl * TT;
+        const int items = n * 4 * lc;
+        for (int idx = tid; idx < items; idx += kThreads) {
+            const int tt = idx / (4 * lc), r2 = idx - tt * 4 * lc;
+            const int i = r2 / lc, cc = r2 - i * lc;
+            const uint16_t* src = a.x + ((t0 + tt) * 4 + i) * (int64_t)C + c0 + 8 * cc;
+            cp_async16(smem_u32(xs + tt * a.xstride + (i * ncols + 8 * cc) * 2), src);
         }
-        if (threadIdx.x < kTileTokens) {
-            const int64_t t = t0 + threadIdx.x;
-            const bool ok = t < a.T;
-            cp_async16(pin + (buf * kTileTokens + threadIdx.x) * 4, a.pre_in + (ok ? t : 0) * 4, ok);
-        }
+        if (tid < n) cp_async16(smem_u32(pin + 4 * tid), a.pre_in + (t0 + tid) * 4);
     };
-
-    int64_t tile = cluster_id;
-    int buf = 0;
-    issue_tile(tile, 0);
+    issue_tile(tile, nv);
+    if (fold)
+        for (int cc = tid; cc < lc; cc += kThreads) cp_async16(smem_u32(nw + 8 * cc), a.norm_w + c0 + 8 * cc);
     cp_async_commit();
 
-    for (; tile < a.ntiles; tile += nclusters, buf ^= 1) {
-        const int64_t t0 = tile * kTileTokens;
-        const int64_t next = tile + nclusters;
-        if (next < a.ntiles) issue_tile(next, buf ^ 1);
-        cp_async_commit();
-        cp_async_wait<1>();  // this tile's group has landed (the next may be in flight)
+    // finalising warps keep bias and alpha of their lane's logit
+    float bias_l = 0.f, alpha_l = 0.f;
+    if (warp < kSlots && lane < kLogits) {
+        bias_l = __ldg(a.bias + lane);
+        alpha_l = __ldg(a.alpha + (lane < 4 ? 0 : (lane < 8 ? 1 : 2)));
+    }
+
+    cluster_sync_all();  // every CTA's barriers are initialised before any push
+
+    bool arrived = false;  // this thread's arrival at the final cluster barrier
+    for (int round = 0; tile < a.ntiles; ++round, tile += ncl) {
+        const int64_t t0 = tile * TT;
+        nv = tile_tokens(tile);
+        const bool last = tile + ncl >= a.ntiles;
+        const int nv_next = last ? 0 : tile_tokens(tile + ncl);
+        const int par = round & 1;
+        cp_async_wait_all();
         __syncthreads();
 
-        const uint4* xb = xs + buf * kTileTokens * qstride;
-
-        // ---- 2a. partial dot products of logits m0, m0+1 for the 8 tokens
-        float acc[16];
+        // ---- 2. collapse (warps 2..11), one token per warp at a time
+        if (warp >= kRowWarp0) {
+            for (int tt = warp - kRowWarp0; tt < nv; tt += kRowWarps) {
+                const float p0 = pin[4 * tt], p1 = pin[4 * tt + 1], p2 = pin[4 * tt + 2], p3 = pin[4 * tt + 3];
+                float sx = 0.f, sh = 0.f;
+                for (int cc = lane; cc < lc; cc += 32) {
+                    float xv[4][8], h[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-#pragma unroll
-        for (int tt = 0; tt < kTileTokens; ++tt) {
-#pragma unroll
-            for (int j = 0; j < JMAX; ++j) {
-                const int q = lane + 32 * j;
-                if (q < qn) {
-                    float f[8];
-                    unpack8(xb[tt * qstride + q], f);
+                    for (int i = 0; i < 4; ++i)
+                        unpack8(*reinterpret_cast<const uint4*>(xs + tt * a.xstride + (i * ncols + 8 * cc) * 2), xv[i]);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        acc[2 * tt + 0] = fmaf(w[j][0][e], f[e], acc[2 * tt + 0]);
-                        acc[2 * tt + 1] = fmaf(w[j][1][e], f[e], acc[2 * tt + 1]);
+                        float v = __fmul_rn(p0, xv[0][e]);
+                        v = __fadd_rn(v, __fmul_rn(p1, xv[1][e]));
+                        v = __fadd_rn(v, __fmul_rn(p2, xv[2][e]));
+                        v = __fadd_rn(v, __fmul_rn(p3, xv[3][e]));
+                        h[e] = v;
+                        sh = fmaf(v, v, sh);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) sx = fmaf(xv[i][e], xv[i][e], sx);
+                    }
+                    if (fold) {
+                        float4* hp = reinterpret_cast<float4*>(hs + tt * hstride + 8 * cc);
+                        hp[0] = make_float4(h[0], h[1], h[2], h[3]);
+                        hp[1] = make_float4(h[4], h[5], h[6], h[7]);
+                    } else {
+                        st_stream(reinterpret_cast<uint4*>(a.layer_input + (t0 + tt) * C + c0 + 8 * cc), pack8(h));
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    sx += __shfl_xor_sync(0xffffffffu, sx, o);
+                    sh += __shfl_xor_sync(0xffffffffu, sh, o);
+                }
+                if (lane == 0) {
+                    const uint32_t f = (uint32_t)(tt % kCtas), s = (uint32_t)(tt / kCtas);
+                    st_async_v2(mapa(smem_u32(inbox_sq + (s * kCtas + rank) * 2), f), sx, sh,
+                                mapa(smem_u32(&sq_full[s]), f));
+                }
+            }
+        }
+
+        // ---- 3. projection on the tensor cores, one 16-token m-tile at a time
+        const int nm = (nv + 15) >> 4;
+        for (int mt = 0; mt < nm; ++mt) {
+            float dh[3][4], dl[3][4];
+#pragma unroll
+            for (int nt = 0; nt < 3; ++nt)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) dh[nt][k] = dl[nt][k] = 0.f;
+#pragma unroll
+            for (int j = 0; j < JMAX; ++j) {
+                const int q = warp + kWarps * j;
+                if (q < lc) {
+                    const unsigned char* r0 = xs + (16 * mt + g) * a.xstride + (32 * q + 8 * t4) * 2;
+                    const uint4 x0 = *reinterpret_cast<const uint4*>(r0);
+                    const uint4 x1 = *reinterpret_cast<const uint4*>(r0 + 8 * a.xstride);
+                    const uint32_t w0[4] = {x0.x, x0.y, x0.z, x0.w}, w1[4] = {x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                    for (int blk = 0; blk < 4; ++blk) {
+                        // block blk: logical k = t4 <-> local 32q + 8 t4 + 2 blk,
+                        // logical k = t4 + 4 <-> the next column
+                        const uint32_t af[4] = {w0[blk] << 16, w1[blk] << 16, w0[blk] & 0xffff0000u,
+                                                w1[blk] & 0xffff0000u};
+#pragma unroll
+                        for (int nt = 0; nt < 3; ++nt) {
+                            const float v0 = b[j][nt][2 * blk], v1 = b[j][nt][2 * blk + 1];
+                            const uint32_t h0 = tf32_rna(v0), h1 = tf32_rna(v1);
+                            const uint32_t l0 = __float_as_uint(v0 - __uint_as_float(h0));
+                            const uint32_t l1 = __float_as_uint(v1 - __uint_as_float(h1));
+                            mma_tf32(dh[nt], af, h0, h1);
+                            mma_tf32(dl[nt], af, l0, l1);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < 3; ++nt) {
+                float* rr = red + (warp * kMaxTile + 16 * mt + g) * kLogits + 8 * nt + 2 * t4;
+                *reinterpret_cast<float2*>(rr) = make_float2(dh[nt][0] + dl[nt][0], dh[nt][1] + dl[nt][1]);
+                *reinterpret_cast<float2*>(rr + 8 * kLogits) =
+                    make_float2(dh[nt][2] + dl[nt][2], dh[nt][3] + dl[nt][3]);
+            }
+        }
+        __syncthreads();  // partials complete; the x tile and pre_in are free
+
+        if (!last) {
+            issue_tile(tile + ncl, nv_next);
+            cp_async_commit();
+        }
+
+        // ---- 4. sum the 12 warps' partials, push them to the finalising CTA
+        for (int pidx = tid; pidx < nv * kLogits; pidx += kThreads) {
+            const int tok = pidx / kLogits, m = pidx - tok * kLogits;
+            float s = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) s += red[(w * kMaxTile + tok) * kLogits + m];
+            const uint32_t f = (uint32_t)(tok % kCtas), slot = (uint32_t)(tok / kCtas);
+            st_async_f32(mapa(smem_u32(inbox_dots + ((par * kSlots + slot) * kCtas + rank) * kLogits + m), f), s,
+                         mapa(smem_u32(&dots_full[par * kSlots + slot]), f));
+        }
+
+        // ---- 5. finalise token 16 * warp + rank (warps 0, 1)
+        if (warp < kSlots) {
+            const int slot = warp;
+            const int tok = kCtas * slot + rank;
+            if (tok < nv) {
+                const int64_t t = t0 + tok;
+                bool ok = mbar_wait<true>(&sq_full[slot], par, abort);
+                // Arm the next tile's phases of this slot now, before this
+                // tile's scales leave: every push of the next tile happens
+                // after its sender received them, so no byte can reach a
+                // phase before its expect_tx (and the previous phase of the
+                // other dots buffer completed a tile ago).
+                __syncwarp();
+                if (lane == 0 && nv_next > tok) {
+                    mbar_arrive_expect_tx(&sq_full[slot], kSqBytes);
+                    mbar_arrive_expect_tx(&dots_full[(par ^ 1) * kSlots + slot], kDotsBytes);
+                }
+                float sx = 0.f, sh = 0.f;
+                if (lane < kCtas) {
+                    sx = inbox_sq[(slot * kCtas + lane) * 2];
+                    sh = inbox_sq[(slot * kCtas + lane) * 2 + 1];
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {  // lanes 16..31 add zeros: every lane ends with the sums
+                    sx += __shfl_xor_sync(0xffffffffu, sx, o);
+                    sh += __shfl_xor_sync(0xffffffffu, sh, o);
+                }
+                const float scale = 1.0f / sqrtf(sh / (float)C + a.norm_eps);
+                if (ok && lane < kCtas)
+                    st_async_f32(mapa(smem_u32(scale_in + tok), lane), scale, mapa(smem_u32(scale_full), lane));
+                if (last) {
+                    cluster_arrive_release();
+                    arrived = true;
+                }
+                ok = ok && mbar_wait<true>(&dots_full[par * kSlots + slot], (round >> 1) & 1, abort);
+                if (ok) {
+                    float l = 0.f;
+                    if (lane < kLogits) {
+                        const float* src = inbox_dots + (par * kSlots + slot) * kCtas * kLogits + lane;
+#pragma unroll
+                        for (int s = 0; s < kCtas; ++s) l += src[s * kLogits];
+                        const float r = 1.0f / sqrtf(sx / (float)K + a.rms_eps);
+                        l = (r * l) * alpha_l + bias_l;
+                        if (a.logits_out) a.logits_out[t * kLogits + lane] = l;
+                    }
+                    // gates: lanes 0..3 pre, 4..7 post
+                    if (lane < 4) a.pre_out[t * 4 + lane] = __fdividef(1.0f, 1.0f + expf(-l));
+                    else if (lane < 8) a.post_out[t * 4 + lane - 4] = __fdividef(2.0f, 1.0f + expf(-l));
+                    // comb: lanes 8..23 hold the 4x4 logits row-major; row softmax
+                    // across each group of 4 lanes, plus eps
+                    float mx = fmaxf(l, __shfl_xor_sync(0xffffffffu, l, 1));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                    const float e = expf(l - mx);
+                    const float e01 = e + __shfl_xor_sync(0xffffffffu, e, 1);
+                    const float sum = e01 + __shfl_xor_sync(0xffffffffu, e01, 2);
+                    const float p = e * rcp_approx(sum) + a.sk_eps;
+                    float P[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) P[k] = __shfl_sync(0xffffffffu, p, 8 + k);
+                    if (lane == 0) {
+                        sinkhorn_iterations(P, a.iters);
+                        float4* co = reinterpret_cast<float4*>(a.comb_out + t * 16);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) co[i] = make_float4(P[4 * i], P[4 * i + 1], P[4 * i + 2], P[4 * i + 3]);
                     }
                 }
             }
         }
-        warp_reduce_scatter16(acc, lane);
-        if ((lane & 1) == 0) {
-            const int idx = (lane >> 1) & 15;
-            part[(idx >> 1) * kPartStride + m0 + (idx & 1)] = acc[0];
+        if (last && !arrived) {
+            cluster_arrive_release();  // every push of this CTA has been issued
+            arrived = true;
         }
 
-        // ---- 2b. collapse one (token, 8-column) item per thread
-        float h[8];
-        const int item = threadIdx.x;
-        const bool has_item = item < kTileTokens * lc;
-        const int it_tt = has_item ? item / lc : 0;
-        const int it_cc = has_item ? item - it_tt * lc : 0;
-        if (has_item) {
-            const float* p = pin + (buf * kTileTokens + it_tt) * 4;
-            float xv[4][8];
+        // ---- 6. wait for the tile's fold scales; fold and store (warps 2..11)
+        if (warp >= kRowWarp0) {
+            const bool ok = mbar_wait<true>(scale_full, par, abort);
+            // next tile's phase: its scales need this CTA's next sq pushes,
+            // which follow the next tile's __syncthreads, so the arm is first
+            if (tid == 32 * kRowWarp0 && nv_next > 0) mbar_arrive_expect_tx(scale_full, 4 * nv_next);
+            if (fold && ok) {
+                for (int tt = warp - kRowWarp0; tt < nv; tt += kRowWarps) {
+                    const float s = scale_in[tt];
+                    for (int cc = lane; cc < lc; cc += 32) {
+                        const float4* hp = reinterpret_cast<const float4*>(hs + tt * hstride + 8 * cc);
+                        const float4 h0 = hp[0], h1 = hp[1];
+                        const float h[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+                        float wf[8], o[8];
+                        unpack8(*reinterpret_cast<const uint4*>(nw + 8 * cc), wf);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) unpack8(xb[it_tt * qstride + i * lc + it_cc], xv[i]);
-            float sx = 0.f, sh = 0.f;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                float v = __fmul_rn(p[0], xv[0][e]);
-                v = __fadd_rn(v, __fmul_rn(p[1], xv[1][e]));
-                v = __fadd_rn(v, __fmul_rn(p[2], xv[2][e]));
-                v = __fadd_rn(v, __fmul_rn(p[3], xv[3][e]));
-                h[e] = v;
-                sh = fmaf(v, v, sh);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) sx = fmaf(xv[i][e], xv[i][e], sx);
-            }
-            red[it_tt * a.lcmax + it_cc] = sx;
-            red[(kTileTokens + it_tt) * a.lcmax + it_cc] = sh;
-            const int64_t t = t0 + it_tt;
-            if (!fold && t < a.T) {
-                uint4* dst = reinterpret_cast<uint4*>(a.layer_input + t * C + (int64_t)(ch0 + it_cc) * 8);
-                st_stream(dst, pack8(h));
-            }
-        }
-        __syncthreads();
-
-        // ---- 2c. this CTA's sum x^2 and sum h^2 per token (warp tt, fixed order)
-        if (warp < kTileTokens) {
-            float sx = 0.f, sh = 0.f;
-            for (int cc = lane; cc < lc; cc += 32) {
-                sx += red[warp * a.lcmax + cc];
-                sh += red[(kTileTokens + warp) * a.lcmax + cc];
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                sx += __shfl_xor_sync(0xffffffffu, sx, o);
-                sh += __shfl_xor_sync(0xffffffffu, sh, o);
-            }
-            if (lane == 0) {
-                part[warp * kPartStride + 24] = sx;
-                part[warp * kPartStride + 25] = sh;
-            }
-        }
-        cluster.sync();  // A: every CTA's partials are visible cluster-wide
-
-        // ---- 3. finalize token t0 + rank in CTA rank (rank < 8), warp 0: the fold
-        //         scale is pushed first (it gates every CTA's stores), the gates and
-        //         the Sinkhorn comb follow while the other CTAs wait at barrier B
-        if (rank < kTileTokens && warp == 0) {
-            const int64_t t = t0 + rank;
-            float v = 0.f;
-            if (lane < kPartStride) {
-                float pv[kClusterCtas];
-#pragma unroll
-                for (int s = 0; s < kClusterCtas; ++s)
-                    pv[s] = cluster.map_shared_rank(part, s)[rank * kPartStride + lane];
-#pragma unroll
-                for (int s = 0; s < kClusterCtas; ++s) v += pv[s];
-            }
-            const float sh = __shfl_sync(0xffffffffu, v, 25);
-            if (fold && lane < kClusterCtas) {
-                float* rs = cluster.map_shared_rank(scale, lane);
-                rs[rank] = 1.0f / sqrtf(sh / (float)C + a.norm_eps);
-            }
-            float l[kLogits];
-#pragma unroll
-            for (int m = 0; m < kLogits; ++m) l[m] = __shfl_sync(0xffffffffu, v, m);
-            const float sx = __shfl_sync(0xffffffffu, v, 24);
-            if (lane == 0 && t < a.T) {
-                const float r = 1.0f / sqrtf(sx / (float)K + a.rms_eps);
-                const float al0 = __ldg(a.alpha), al1 = __ldg(a.alpha + 1), al2 = __ldg(a.alpha + 2);
-#pragma unroll
-                for (int m = 0; m < kLogits; ++m) {
-                    const float al = m < 4 ? al0 : (m < 8 ? al1 : al2);
-                    l[m] = (r * l[m]) * al + __ldg(a.bias + m);
+                        for (int e = 0; e < 8; ++e) o[e] = __fmul_rn(__fmul_rn(h[e], s), wf[e]);
+                        st_stream(reinterpret_cast<uint4*>(a.layer_input + (t0 + tt) * C + c0 + 8 * cc), pack8(o));
+                    }
                 }
-                if (a.logits_out) {
-                    float4* lo = reinterpret_cast<float4*>(a.logits_out + t * kLogits);
-#pragma unroll
-                    for (int m = 0; m < kLogits; m += 4) lo[m / 4] = make_float4(l[m], l[m + 1], l[m + 2], l[m + 3]);
-                }
-                float pre[4], post[4], P[16];
-                gates_and_comb(l, a.iters, a.sk_eps, pre, post, P);
-                reinterpret_cast<float4*>(a.pre_out)[t] = make_float4(pre[0], pre[1], pre[2], pre[3]);
-                reinterpret_cast<float4*>(a.post_out)[t] = make_float4(post[0], post[1], post[2], post[3]);
-                float4* co = reinterpret_cast<float4*>(a.comb_out + t * 16);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) co[i] = make_float4(P[4 * i], P[4 * i + 1], P[4 * i + 2], P[4 * i + 3]);
-            }
-        }
-        cluster.sync();  // B: fold scales are in place; partial buffers may be reused
-
-        // ---- 4. fold: scale h, round once, store this CTA's slice
-        if (fold && has_item) {
-            const int64_t t = t0 + it_tt;
-            if (t < a.T) {
-                const float s = scale[it_tt];
-                const uint4 wv = __ldg(reinterpret_cast<const uint4*>(a.norm_w + (int64_t)(ch0 + it_cc) * 8));
-                float wf[8], o[8];
-                unpack8(wv, wf);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = __fmul_rn(__fmul_rn(h[e], s), wf[e]);
-                uint4* dst = reinterpret_cast<uint4*>(a.layer_input + t * C + (int64_t)(ch0 + it_cc) * 8);
-                st_stream(dst, pack8(o));
             }
         }
     }
-    cp_async_wait<0>();
+    if (!arrived) cluster_arrive_release();  // (a CTA with no tile)
+    cp_async_wait_all();
+    cluster_wait_acquire();  // no CTA leaves while a peer may still push into it
 }
 
-static size_t pre_cluster_smem(int lcmax) {
-    return sizeof(uint4) * 2 * kTileTokens * 4 * lcmax + sizeof(float) * 2 * kTileTokens * 4 +
-           sizeof(float) * kTileTokens * kPartStride + sizeof(float) * kTileTokens +
-           sizeof(float) * 2 * kTileTokens * lcmax;
+int lcmax_of(int C) { return (C / 8 + kCtas - 1) / kCtas; }
+
+int jmax_of(int C) {
+    const int j = (lcmax_of(C) + kWarps - 1) / kWarps;
+    if (j <= 1) return 1;
+    if (j <= 2) return 2;
+    if (j <= 4) return 4;
+    return 0;
 }
 
-static cudaLaunchConfig_t cluster_config(cudaLaunchAttribute* attr, size_t smem, cudaStream_t stream) {
+cudaLaunchConfig_t cluster_config(cudaLaunchAttribute* attr, size_t smem, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kClusterCtas;
+    attr[0].val.clusterDim.x = kCtas;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cfg.blockDim = dim3(kPreThreads, 1, 1);
-    cfg.gridDim = dim3(kClusterCtas, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.gridDim = dim3(kCtas, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     return cfg;
 }
 
-static int lcmax_of(int C) { return (C / 8 + kClusterCtas - 1) / kClusterCtas; }
+}  // namespace dec
 
-int pre_cluster_jmax(int C) {
-    const int j = (4 * lcmax_of(C) + 31) / 32;
-    if (j <= 2) return 2;
-    if (j <= 4) return 4;
-    if (j <= 5) return 5;
-    if (j <= 6) return 6;
-    return 0;
+int pre_cluster_ctas() { return dec::kCtas; }
+int pre_cluster_max_tile() { return dec::kMaxTile; }
+
+// Tokens per tile for T tokens and `max_clusters` co-resident clusters: the
+// tokens spread evenly over the clusters, at most 32 per tile.
+int pre_cluster_tile_tokens(int64_t T, int max_clusters) {
+    if (T <= 0 || max_clusters <= 0) return 1;
+    int64_t tt = (T + max_clusters - 1) / max_clusters;
+    return (int)(tt < dec::kMaxTile ? tt : dec::kMaxTile);
 }
 
-int pre_cluster_tile_tokens() { return kTileTokens; }
-int pre_cluster_ctas() { return kClusterCtas; }
-
 // One-time set-up for the current device and hidden size C: allows the
-// non-portable cluster size and the dynamic shared memory of the kernel
-// instance C uses, then returns the maximum number of co-resident clusters
-// (the launch grid is min(tiles, that) clusters).  Returns 0 on error.
-// Must run before any stream capture that records the kernel.
+// non-portable cluster size and the kernel's dynamic shared memory, then
+// returns the maximum number of co-resident clusters (0 on error).  Must run
+// before any stream capture that records the kernel.
 int pre_cluster_prepare(int C) {
-    const size_t smem = pre_cluster_smem(lcmax_of(C));
+    const size_t smem = (size_t)dec::dec_layout(dec::lcmax_of(C)).total;
+    // the attribute belongs to the kernel instance, which several hidden
+    // sizes share: allow the largest slice that instance takes
+    const int jmax = dec::jmax_of(C);
+    const size_t smem_cap = (size_t)dec::dec_layout(dec::kWarps * jmax).total;
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = cluster_config(attr, smem, nullptr);
+    cudaLaunchConfig_t cfg = dec::cluster_config(attr, smem, nullptr);
     int n = 0;
     cudaError_t e = cudaSuccess;
     auto setup = [&](auto kern) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_cap);
         if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
     };
-    switch (pre_cluster_jmax(C)) {
-        case 2: setup(pre_cluster_kernel<2>); break;
-        case 4: setup(pre_cluster_kernel<4>); break;
-        case 5: setup(pre_cluster_kernel<5>); break;
-        case 6: setup(pre_cluster_kernel<6>); break;
+    switch (jmax) {
+        case 1: setup(dec::pre_decode_kernel<1>); break;
+        case 2: setup(dec::pre_decode_kernel<2>); break;
+        case 4: setup(dec::pre_decode_kernel<4>); break;
         default: return 0;
     }
     return e == cudaSuccess ? n : 0;
@@ -377,25 +512,36 @@ cudaError_t launch_pre_cluster(const uint16_t* x, const float* pre_in, const flo
                                float sk_eps, float* pre_out, float* post_out, float* comb_out,
                                uint16_t* layer_input, float* logits_out, cudaStream_t stream,
                                int max_clusters) {
-    PreArgs a;
+    dec::Args a;
     a.x = x; a.pre_in = pre_in; a.fn = fn; a.bias = bias; a.alpha = alpha; a.norm_w = norm_w;
     a.T = T; a.C = C; a.iters = iters;
     a.rms_eps = rms_eps; a.norm_eps = norm_eps; a.sk_eps = sk_eps;
     a.pre_out = pre_out; a.post_out = post_out; a.comb_out = comb_out;
     a.layer_input = layer_input; a.logits_out = logits_out;
-    a.ntiles = (T + kTileTokens - 1) / kTileTokens;
-    a.lcmax = lcmax_of(C);
+    a.tile = pre_cluster_tile_tokens(T, max_clusters);
+    a.ntiles = (T + a.tile - 1) / a.tile;
+    a.lcmax = dec::lcmax_of(C);
+    a.xstride = dec::dec_xstride(a.lcmax);
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = cluster_config(attr, pre_cluster_smem(a.lcmax), stream);
+    cudaLaunchConfig_t cfg = dec::cluster_config(attr, (size_t)dec::dec_layout(a.lcmax).total, stream);
     const int64_t nclusters = a.ntiles < max_clusters ? a.ntiles : max_clusters;
-    cfg.gridDim = dim3((unsigned)(nclusters * kClusterCtas), 1, 1);
-    switch (pre_cluster_jmax(C)) {
-        case 2: return cudaLaunchKernelEx(&cfg, pre_cluster_kernel<2>, a);
-        case 4: return cudaLaunchKernelEx(&cfg, pre_cluster_kernel<4>, a);
-        case 5: return cudaLaunchKernelEx(&cfg, pre_cluster_kernel<5>, a);
-        case 6: return cudaLaunchKernelEx(&cfg, pre_cluster_kernel<6>, a);
+    cfg.gridDim = dim3((unsigned)(nclusters * dec::kCtas), 1, 1);
+    switch (dec::jmax_of(C)) {
+        case 1: return cudaLaunchKernelEx(&cfg, dec::pre_decode_kernel<1>, a);
+        case 2: return cudaLaunchKernelEx(&cfg, dec::pre_decode_kernel<2>, a);
+        case 4: return cudaLaunchKernelEx(&cfg, dec::pre_decode_kernel<4>, a);
         default: return cudaErrorInvalidValue;
     }
+}
+
+// Read and clear this kernel's device status word (bit 0: a bounded wait
+// gave up).
+cudaError_t read_decode_status(unsigned int* status) {
+    unsigned int v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_status, sizeof v);
+    if (e == cudaSuccess && v) e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof zero);
+    *status = v;
+    return e;
 }
 
 }  // namespace mhc

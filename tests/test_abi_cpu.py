@@ -124,7 +124,9 @@ def test_plan_shape_checks(lib):
     st = lib.mhc_pre_delayed_plan(16, 4, 5120, ctypes.byref(kernel), ctypes.byref(grid),
                                   ctypes.byref(cluster), ctypes.byref(tt))
     assert st == OK
-    assert kernel.value == 1 and cluster.value == 16 and tt.value == 8
+    assert kernel.value == 1 and cluster.value == 16 and tt.value == 16
+    st = lib.mhc_pre_delayed_plan(100, 4, 5120, None, None, None, ctypes.byref(tt))
+    assert st == OK and tt.value == 32
     assert lib.mhc_pre_delayed_plan(16, 4, 5121, None, None, None, None) == UNSUPPORTED
 
 

@@ -83,11 +83,14 @@ def test_config1_decode_sweep(T):
     (1, 8, False), (3, 8, True), (7, 136, True), (31, 1000, False), (9, 2056, True),
     (127, 5120, False), (129, 5120, True), (17, 6144, True), (64, 6144, False),
     (1000, 5120, True), (33, 4096, False), (5, 128, True), (2, 2048, True),
+    (300, 1000, True), (500, 6144, False), (225, 136, False),
 ])
 def test_token_and_hidden_sweep(T, C, fold):
-    """Ragged token tails (not multiples of the 8-token tile), hidden sizes
-    whose 8-column groups do not split evenly over the 16 CTA slices, and
-    slices with no columns at all (C = 8)."""
+    """Ragged token tails (tile sizes that do not divide T), hidden sizes
+    whose 8-column groups do not split evenly over the 16 CTA slices, slices
+    with no columns at all (C = 8), and cluster-kernel shapes with more tiles
+    than co-resident clusters (several rounds per cluster: T = 225..500 at
+    hidden sizes the tensor-core kernel does not take)."""
     d = seam_inputs(T, C=C, seed=100 + T + C, fold=fold)
     g = _gpu_pre(_to_dev(d))
     o, xb = _oracle_pre(d)
