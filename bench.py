@@ -346,7 +346,9 @@ def run_ours(args, rank, world, local):
                 pre_call(st)
                 mhc.post(dd["x"], dd["y"], o["comb"], o["post"], out=xn, stream=st)
 
-            for name, one in (("pre", pre_call), ("seam", seam_call)):
+            for name, one, ov in (("pre", pre_call, False), ("seam", seam_call, False),
+                                  ("pre_overlap", pre_call, True), ("seam_overlap", seam_call, True)):
+                mhc.set_launch_overlap(ov)
                 # DECODE_REPS calls back to back in one graph: the GPU time per
                 # call, not the host's graph-launch rate
                 g = SeamGraph(lambda st, one=one: [one(st) for _ in range(DECODE_REPS)], s)
@@ -362,6 +364,7 @@ def run_ours(args, rank, world, local):
                 res[name + "_us"] = round(statistics.median(meds), 3)
                 res[name + "_launches"] = g.kernel_nodes / DECODE_REPS
                 g.close()
+            mhc.set_launch_overlap(False)
             decode[str(Td)] = res
         # 80 seams, each with its own weights, pre-mix carried seam to seam
         params = [chain_seam_params(si, device=f"cuda:{local}") for si in range(CHAIN_SEAMS)]
@@ -382,22 +385,29 @@ def run_ours(args, rank, world, local):
                     torch.add(co["layer_input"], deltas[si], out=cy)   # synthetic sublayer
                 mhc.post(cx, cy, co["comb"], co["post"], out=cx, stream=st)
 
-        with torch.cuda.stream(s):
-            chain_step(s)
-        s.synchronize()
-        g = SeamGraph(chain_step, s)
-        g.replay(3)
-        meds = []
-        for _ in range(5):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(s)
-            g.replay(200)
-            b.record(s)
+        chain_us = {}
+        for ov in (False, True):
+            mhc.set_launch_overlap(ov)
+            with torch.cuda.stream(s):
+                chain_step(s)
             s.synchronize()
-            meds.append(a.elapsed_time(b) * 1e3 / 200)
-        chain = {"us_per_step": round(statistics.median(meds), 2), "seams": CHAIN_SEAMS, "T": CHAIN_T,
-                 "kernel_nodes": g.kernel_nodes,
-                 "launches_per_seam": (g.kernel_nodes - CHAIN_SEAMS) / CHAIN_SEAMS,
+            g = SeamGraph(chain_step, s)
+            g.replay(3)
+            meds = []
+            for _ in range(5):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(s)
+                g.replay(200)
+                b.record(s)
+                s.synchronize()
+                meds.append(a.elapsed_time(b) * 1e3 / 200)
+            chain_us[ov] = round(statistics.median(meds), 2)
+            nodes = g.kernel_nodes
+            g.close()
+        mhc.set_launch_overlap(False)
+        chain = {"us_per_step": chain_us[False], "us_per_step_overlap": chain_us[True],
+                 "seams": CHAIN_SEAMS, "T": CHAIN_T, "kernel_nodes": nodes,
+                 "launches_per_seam": (nodes - CHAIN_SEAMS) / CHAIN_SEAMS,
                  "l2": "fn of 80 seams = 157 MB > L2"}
         g.close()
 

@@ -179,6 +179,26 @@ mhc_status mhc_device_status(void);
 mhc_status mhc_pre_delayed_plan(int64_t T, int n, int C, int *kernel, int *grid,
                                 int *cluster, int *tokens_per_tile);
 
+/*
+ * Launch overlap between consecutive seam kernels (programmatic dependent
+ * launch, a CUDA launch attribute; the pages' own kernels have no
+ * counterpart: this is a scheduling option of this library, it changes no
+ * result).  enable != 0: from then on mhc_post and mhc_pre_delayed's
+ * cluster kernel (the one used below 256 tokens and for hidden sizes the
+ * tensor-core kernel does not take) are launched so that they may start
+ * while the previous kernel in the stream is still running.  The pre kernel
+ * then loads fn, bias, alpha and norm_weight, and sets itself up, before it
+ * waits for that kernel; it reads x and pre_in, and mhc_post reads all of
+ * its inputs, only after the wait.
+ * Contract while enabled: fn, bias, alpha and norm_weight must not be
+ * written by the kernel (or copy) issued just before mhc_pre_delayed on the
+ * same stream; they are weights, written once, in a decode step.  Outputs
+ * are bit-identical with and without the overlap.  Works under stream
+ * capture (the graph keeps the programmatic edges).  Process-wide, off at
+ * load.  Returns the previous setting (0 or 1).
+ */
+int mhc_set_launch_overlap(int enable);
+
 /* Library version, (major << 16) | minor. */
 int mhc_version(void);
 

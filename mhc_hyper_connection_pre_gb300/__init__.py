@@ -71,6 +71,8 @@ def load_library():
         lib.mhc_version.restype = I
         lib.mhc_device_status.argtypes = []
         lib.mhc_device_status.restype = I
+        lib.mhc_set_launch_overlap.argtypes = [I]
+        lib.mhc_set_launch_overlap.restype = I
         _lib = lib
         return lib
 
@@ -232,6 +234,14 @@ def device_status() -> int:
     status word (``mhc_device_status``): 0 = OK, 4 = a bounded in-kernel wait
     timed out since the last check."""
     return load_library().mhc_device_status()
+
+
+def set_launch_overlap(enable: bool) -> bool:
+    """Turn programmatic dependent launch of the decode pre kernel and of
+    ``post`` on or off (``mhc_set_launch_overlap``); returns the previous
+    setting.  While on, fn, bias, alpha and norm_w must not be written by the
+    kernel issued just before ``pre_delayed`` on the same stream."""
+    return bool(load_library().mhc_set_launch_overlap(1 if enable else 0))
 
 
 def pre_plan(T: int, n: int = 4, C: int = 5120) -> dict:

@@ -72,6 +72,17 @@ __device__ __forceinline__ uint32_t f32x2_to_bf16x2(f32x2 a) {
     return pack_bf16x2(lo, hi);
 }
 
+// Programmatic dependent launch (PTX griddepcontrol).  A kernel launched
+// with the programmatic stream serialization attribute may start while the
+// previous kernel in the stream is still running: griddep_wait() blocks until
+// that kernel has completed and its writes are visible (without the
+// attribute it returns at once); griddep_launch_dependents() allows the next
+// such kernel to start before this one ends.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Streaming 16-byte global load / store (data touched once).
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
 __device__ __forceinline__ void st_stream(uint4* p, const uint4& v) { __stcs(p, v); }

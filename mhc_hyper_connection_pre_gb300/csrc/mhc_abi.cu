@@ -4,18 +4,19 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 namespace mhc {
 cudaError_t launch_post(const uint16_t* x, const uint16_t* y, const float* comb,
                         const float* post, int64_t T, int C, uint16_t* x_new,
-                        cudaStream_t stream, int num_sms);
+                        cudaStream_t stream, int num_sms, bool overlap);
 cudaError_t launch_pre_cluster(const uint16_t* x, const float* pre_in, const float* fn,
                                const float* bias, const float* alpha, const uint16_t* norm_w,
                                int64_t T, int C, int iters, float rms_eps, float norm_eps,
                                float sk_eps, float* pre_out, float* post_out, float* comb_out,
                                uint16_t* layer_input, float* logits_out, cudaStream_t stream,
-                               int max_clusters);
+                               int max_clusters, bool overlap);
 int pre_cluster_tile_tokens(int64_t T, int max_clusters);
 int pre_cluster_max_tile();
 int pre_cluster_ctas();
@@ -53,6 +54,9 @@ struct DeviceInfo {
 };
 
 std::mutex g_mutex;
+// Programmatic dependent launch for the decode pre kernel and the post kernel
+// (mhc_set_launch_overlap); off by default.
+std::atomic<int> g_launch_overlap{0};
 DeviceInfo g_dev[kMaxDevices];
 
 int current_device() {
@@ -128,7 +132,9 @@ const char* mhc_status_string(mhc_status s) {
     return "unknown mhc_status";
 }
 
-int mhc_version(void) { return (0 << 16) | 2; }
+int mhc_version(void) { return (0 << 16) | 3; }
+
+int mhc_set_launch_overlap(int enable) { return g_launch_overlap.exchange(enable ? 1 : 0); }
 
 mhc_status mhc_device_status(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return MHC_ERR_CUDA;
@@ -218,7 +224,7 @@ mhc_status mhc_pre_delayed(const uint16_t* x, const float* pre_in, const float* 
     cudaError_t e = mhc::launch_pre_cluster(
         x, pre_in, fn, bias, alpha, norm_weight, T, C, sinkhorn_iters, rms_eps, norm_eps,
         sinkhorn_eps, pre_out, post_out, comb_out, layer_input, logits_out,
-        static_cast<cudaStream_t>(stream), mc);
+        static_cast<cudaStream_t>(stream), mc, g_launch_overlap.load() != 0);
     return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA;
 }
 
@@ -239,7 +245,8 @@ mhc_status mhc_post(const uint16_t* x, const uint16_t* y, const float* comb, con
     if (dev < 0) return MHC_ERR_CUDA;
     int sms = num_sms(dev);
     if (sms <= 0) return MHC_ERR_CUDA;
-    cudaError_t e = mhc::launch_post(x, y, comb, post, T, C, x_new, static_cast<cudaStream_t>(stream), sms);
+    cudaError_t e = mhc::launch_post(x, y, comb, post, T, C, x_new, static_cast<cudaStream_t>(stream), sms,
+                                     g_launch_overlap.load() != 0);
     return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA;
 }
 

@@ -21,6 +21,8 @@ __global__ void __launch_bounds__(256)
 post_kernel(const uint4* x, const uint4* __restrict__ y,
             const float4* __restrict__ comb, const float4* __restrict__ post,
             int64_t items, int c8, uint4* x_new) {
+    griddep_launch_dependents();
+    griddep_wait();  // every input may come from the previous kernel
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; base < items;
          base += 2 * stride) {
@@ -75,7 +77,7 @@ post_kernel(const uint4* x, const uint4* __restrict__ y,
 
 cudaError_t launch_post(const uint16_t* x, const uint16_t* y, const float* comb,
                         const float* post, int64_t T, int C, uint16_t* x_new,
-                        cudaStream_t stream, int num_sms) {
+                        cudaStream_t stream, int num_sms, bool overlap) {
     const int c8 = C / 8;
     const int64_t items = T * (int64_t)c8;
     const int threads = 256;
@@ -83,10 +85,20 @@ cudaError_t launch_post(const uint16_t* x, const uint16_t* y, const float* comb,
     int64_t cap = (int64_t)num_sms * 8;
     int blocks = (int)(want < cap ? want : cap);
     if (blocks < 1) blocks = 1;
-    post_kernel<<<blocks, threads, 0, stream>>>(
-        reinterpret_cast<const uint4*>(x), reinterpret_cast<const uint4*>(y),
-        reinterpret_cast<const float4*>(comb), reinterpret_cast<const float4*>(post), items,
-        c8, reinterpret_cast<uint4*>(x_new));
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(blocks, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = overlap ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, post_kernel, reinterpret_cast<const uint4*>(x),
+                                       reinterpret_cast<const uint4*>(y), reinterpret_cast<const float4*>(comb),
+                                       reinterpret_cast<const float4*>(post), items, c8,
+                                       reinterpret_cast<uint4*>(x_new));
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -24,10 +24,12 @@
 //   3. every warp multiplies its chunks on the tensor cores:
 //      mma.sync m16n8k8 with tf32 inputs and fp32 accumulation, tokens as M,
 //      the 24 logits as three n-tiles of 8.  x (bf16) is exact in tf32; fn is
-//      split into hi = tf32(fn) and lo = fn - hi (exact in fp32), two MMAs per
-//      block, which leaves a relative error below 2^-21 on each product;
+//      split into hi = fn with the low 13 mantissa bits cleared (exactly a
+//      tf32 value) and lo = fn - hi (exact in fp32), two MMAs per block; the
+//      MMA keeps 10 mantissa bits of lo, so each product carries a relative
+//      error below 2^-20;
 //   4. the 12 warps' partial dot products are summed in shared memory in a
-//      fixed order and pushed to the finalising CTA;
+//      fixed order and pushed to the finalising CTA, four logits per store;
 //   5. CTA r finalises tokens r and r + 16 of the tile (warps 0 and 1): it
 //      sums the 16 CTAs' partials in rank order, sends the fold scale to every
 //      CTA at once, then forms r, the logits, the gates and the Sinkhorn comb;
@@ -107,10 +109,12 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
 
-__device__ __forceinline__ uint32_t tf32_rna(float v) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
-    return r;
+// fp32 -> (hi, lo) with hi + lo == v exactly: hi keeps sign, exponent and
+// the top 10 mantissa bits (a tf32 value as is), lo the rest.  (volatile: the
+// split is redone at each use rather than hoisted into 192 live registers.)
+__device__ __forceinline__ void split_tf32(float v, uint32_t& hi, uint32_t& lo) {
+    asm volatile("and.b32 %0, %1, 0xffffe000;" : "=r"(hi) : "r"(__float_as_uint(v)));
+    lo = __float_as_uint(v - __uint_as_float(hi));
 }
 // D += A (16x8, tf32, row) * B (8x8, tf32, col); fp32 accumulators.
 __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -158,6 +162,8 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
         return (int)(left < TT ? left : TT);
     };
 
+    griddep_launch_dependents();  // the next kernel may set itself up meanwhile
+
     // ---- set-up: barriers armed for the first tile
     int64_t tile = cid;
     int nv = tile_tokens(tile);
@@ -172,6 +178,9 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
             }
         mbar_arrive_expect_tx(scale_full, 4 * nv);
     }
+    // Relaxed: this arrival waits for none of the loads below.  The matching
+    // wait comes before the first push into another CTA.
+    cluster_arrive_relaxed();
 
     // ---- this warp's fn blocks, fp32 in registers: chunk q = warp + 12 j,
     //      n-tile nt (logits 8 nt .. 8 nt + 7), lane (g, t4) holds logit
@@ -212,10 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
         }
         if (tid < n) cp_async16(smem_u32(pin + 4 * tid), a.pre_in + (t0 + tid) * 4);
     };
-    issue_tile(tile, nv);
     if (fold)
         for (int cc = tid; cc < lc; cc += kThreads) cp_async16(smem_u32(nw + 8 * cc), a.norm_w + c0 + 8 * cc);
-    cp_async_commit();
 
     // finalising warps keep bias and alpha of their lane's logit
     float bias_l = 0.f, alpha_l = 0.f;
@@ -224,7 +231,13 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
         alpha_l = __ldg(a.alpha + (lane < 4 ? 0 : (lane < 8 ? 1 : 2)));
     }
 
-    cluster_sync_all();  // every CTA's barriers are initialised before any push
+    // Everything above reads only the weights (fn, bias, alpha, norm_w).
+    // Under programmatic dependent launch it overlaps the previous kernel;
+    // x and pre_in may be that kernel's output.
+    griddep_wait();
+    issue_tile(tile, nv);
+    cp_async_commit();
+    cluster_wait_acquire();  // every CTA's barriers are initialised before any push
 
     bool arrived = false;  // this thread's arrival at the final cluster barrier
     for (int round = 0; tile < a.ntiles; ++round, tile += ncl) {
@@ -302,10 +315,9 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
                                                 w1[blk] & 0xffff0000u};
 #pragma unroll
                         for (int nt = 0; nt < 3; ++nt) {
-                            const float v0 = b[j][nt][2 * blk], v1 = b[j][nt][2 * blk + 1];
-                            const uint32_t h0 = tf32_rna(v0), h1 = tf32_rna(v1);
-                            const uint32_t l0 = __float_as_uint(v0 - __uint_as_float(h0));
-                            const uint32_t l1 = __float_as_uint(v1 - __uint_as_float(h1));
+                            uint32_t h0, l0, h1, l1;
+                            split_tf32(b[j][nt][2 * blk], h0, l0);
+                            split_tf32(b[j][nt][2 * blk + 1], h1, l1);
                             mma_tf32(dh[nt], af, h0, h1);
                             mma_tf32(dl[nt], af, l0, l1);
                         }
@@ -327,15 +339,19 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
             cp_async_commit();
         }
 
-        // ---- 4. sum the 12 warps' partials, push them to the finalising CTA
-        for (int pidx = tid; pidx < nv * kLogits; pidx += kThreads) {
-            const int tok = pidx / kLogits, m = pidx - tok * kLogits;
-            float s = 0.f;
+        // ---- 4. sum the 12 warps' partials (warp order), push them to the
+        //         finalising CTA, four logits per 16-byte store
+        for (int pidx = tid; pidx < nv * (kLogits / 4); pidx += kThreads) {
+            const int tok = pidx / (kLogits / 4), m = 4 * (pidx - tok * (kLogits / 4));
+            float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) s += red[(w * kMaxTile + tok) * kLogits + m];
+            for (int w = 0; w < kWarps; ++w) {
+                const float4 v = *reinterpret_cast<const float4*>(red + (w * kMaxTile + tok) * kLogits + m);
+                s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+            }
             const uint32_t f = (uint32_t)(tok % kCtas), slot = (uint32_t)(tok / kCtas);
-            st_async_f32(mapa(smem_u32(inbox_dots + ((par * kSlots + slot) * kCtas + rank) * kLogits + m), f), s,
-                         mapa(smem_u32(&dots_full[par * kSlots + slot]), f));
+            st_async_v4(mapa(smem_u32(inbox_dots + ((par * kSlots + slot) * kCtas + rank) * kLogits + m), f),
+                        s.x, s.y, s.z, s.w, mapa(smem_u32(&dots_full[par * kSlots + slot]), f));
         }
 
         // ---- 5. finalise token 16 * warp + rank (warps 0, 1)
@@ -511,7 +527,7 @@ cudaError_t launch_pre_cluster(const uint16_t* x, const float* pre_in, const flo
                                int64_t T, int C, int iters, float rms_eps, float norm_eps,
                                float sk_eps, float* pre_out, float* post_out, float* comb_out,
                                uint16_t* layer_input, float* logits_out, cudaStream_t stream,
-                               int max_clusters) {
+                               int max_clusters, bool overlap) {
     dec::Args a;
     a.x = x; a.pre_in = pre_in; a.fn = fn; a.bias = bias; a.alpha = alpha; a.norm_w = norm_w;
     a.T = T; a.C = C; a.iters = iters;
@@ -522,8 +538,13 @@ cudaError_t launch_pre_cluster(const uint16_t* x, const float* pre_in, const flo
     a.ntiles = (T + a.tile - 1) / a.tile;
     a.lcmax = dec::lcmax_of(C);
     a.xstride = dec::dec_xstride(a.lcmax);
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = dec::cluster_config(attr, (size_t)dec::dec_layout(a.lcmax).total, stream);
+    if (overlap) {
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 2;
+    }
     const int64_t nclusters = a.ntiles < max_clusters ? a.ntiles : max_clusters;
     cfg.gridDim = dim3((unsigned)(nclusters * dec::kCtas), 1, 1);
     switch (dec::jmax_of(C)) {

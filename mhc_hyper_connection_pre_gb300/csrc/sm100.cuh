@@ -129,6 +129,9 @@ __device__ __forceinline__ void cluster_sync_all() {
 }
 // The two halves of a cluster barrier, for threads that reach them at
 // different points (each thread: one arrive, then one wait).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_arrive_release() {
     asm volatile("barrier.cluster.arrive.release;" ::: "memory");
 }

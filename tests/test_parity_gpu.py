@@ -10,7 +10,7 @@ import torch
 import oracle
 import mhc_hyper_connection_pre_gb300 as mhc
 from mhc_hyper_connection_pre_gb300.graphs import SeamGraph
-from workloads import seam_inputs, bf16_bits
+from workloads import seam_inputs, bf16_bits, chain_seam_params, chain_stub_delta
 from parity import (assert_gates, assert_bf16, assert_bitexact, assert_logits, logit_bound,
                     post_abs_scale)
 
@@ -237,6 +237,74 @@ def test_graph_seam_is_two_launches_and_replays_exactly():
         assert torch.equal(out[k], eager_pre[k]), k
     assert torch.equal(xn, eager_xn)
     g.close()
+
+
+def _chain_buffers(T, seams, C, dev):
+    return {"x": torch.empty(T, 4, C, dtype=torch.bfloat16, device=dev),
+            "pre": [torch.empty(T, 4, device=dev), torch.empty(T, 4, device=dev)],
+            "outs": [{"post": torch.empty(T, 4, device=dev), "comb": torch.empty(T, 4, 4, device=dev),
+                      "layer_input": torch.empty(T, C, dtype=torch.bfloat16, device=dev)}
+                     for _ in range(seams)]}
+
+
+def _seam_chain(b, params, ys, stream):
+    """(pre, post) per seam back to back on one stream, launches only: each
+    pre reads the x the previous post wrote and the pre-mix the previous pre
+    wrote."""
+    for si, o in enumerate(b["outs"]):
+        p = params[si]
+        out = dict(o, pre=b["pre"][(si + 1) & 1])
+        mhc.pre_delayed(b["x"], b["pre"][si & 1], p["fn"], p["bias"], p["alpha"], p["norm_w"], out=out,
+                        stream=stream)
+        mhc.post(b["x"], ys[si], o["comb"], o["post"], out=b["x"], stream=stream)
+
+
+def _chain_result(b):
+    return [b["x"].clone(), b["pre"][0].clone(), b["pre"][1].clone()] + \
+        [v.clone() for o in b["outs"] for v in o.values()]
+
+
+@pytest.mark.parametrize("T", [4, 100])
+def test_launch_overlap_is_bit_identical(T):
+    """With programmatic dependent launch on, a chain of seams whose kernels
+    each consume the previous kernel's output (eager and graph-captured) gives
+    the same bits as with it off."""
+    seams, C, dev = 6, 5120, "cuda"
+    params = [chain_seam_params(si, device=dev) for si in range(seams)]
+    ys = [chain_stub_delta(si, T=T, device=dev) for si in range(seams)]
+    d = seam_inputs(T, seed=900 + T, device=dev)
+    b = _chain_buffers(T, seams, C, dev)
+    s = torch.cuda.Stream()
+
+    def reset():
+        b["x"].copy_(d["x"])
+        b["pre"][0].copy_(d["pre_in"])
+        torch.cuda.synchronize()
+
+    prev = mhc.set_launch_overlap(False)
+    try:
+        reset()
+        _seam_chain(b, params, ys, s)
+        s.synchronize()
+        ref = _chain_result(b)
+        mhc.set_launch_overlap(True)
+        reset()
+        _seam_chain(b, params, ys, s)
+        s.synchronize()
+        assert mhc.device_status() == 0
+        for got, want in zip(_chain_result(b), ref):
+            assert torch.equal(got, want)
+        g = SeamGraph(lambda st: _seam_chain(b, params, ys, st), s)
+        assert g.kernel_nodes == 2 * seams, g.kernel_nodes
+        reset()
+        g.replay(1)
+        s.synchronize()
+        assert mhc.device_status() == 0
+        for got, want in zip(_chain_result(b), ref):
+            assert torch.equal(got, want)
+        g.close()
+    finally:
+        mhc.set_launch_overlap(prev)
 
 
 # ------------------------------------------------- stress and full sizes ---
