@@ -20,7 +20,7 @@
 //      is issued as soon as this one's MMA is done);
 //   2. warps 2..11 collapse one token at a time (h to shared memory, or
 //      straight to layer_input without the fold) and push the token's
-//      partial sum x^2 and sum h^2 to the CTA that finalises it;
+//      partial sum x^2 and sum h^2 to every CTA of the cluster;
 //   3. every warp multiplies its chunks on the tensor cores:
 //      mma.sync m16n8k8 with tf32 inputs and fp32 accumulation, tokens as M,
 //      the 24 logits as three n-tiles of 8.  x (bf16) is exact in tf32; fn is
@@ -31,9 +31,11 @@
 //   4. the 12 warps' partial dot products are summed in shared memory in a
 //      fixed order and pushed to the finalising CTA, four logits per store;
 //   5. CTA r finalises tokens r and r + 16 of the tile (warps 0 and 1): it
-//      sums the 16 CTAs' partials in rank order, sends the fold scale to every
-//      CTA at once, then forms r, the logits, the gates and the Sinkhorn comb;
-//   6. warps 2..11 fold h with the scale and store layer_input.
+//      sums the 16 CTAs' partials in rank order and forms r, the logits, the
+//      gates and the Sinkhorn comb;
+//   6. meanwhile warps 2..11 form each token's fold scale from the 16 sum h^2
+//      partials (the same sum, in rank order, in every CTA: the same bits),
+//      fold h and store layer_input.
 // Every push is an st.async into the receiver's shared memory that completes
 // bytes on the receiver's mbarrier, so no CTA waits at a cluster barrier for
 // the slowest one inside a tile; all waits are bounded (a timeout sets the
@@ -53,6 +55,7 @@ constexpr int kSlots = kMaxTile / kCtas;   // tokens each CTA finalises per tile
 constexpr int kRowWarp0 = kSlots;          // warps kRowWarp0.. collapse and fold
 constexpr int kRowWarps = kWarps - kRowWarp0;
 constexpr int kSqBytes = kCtas * 2 * 4;            // per token: 16 x (sum x^2, sum h^2)
+constexpr int kNumBars = 2 + 2 * kSlots;           // sq_full[parity], dots_full[parity][slot]
 constexpr int kDotsBytes = kCtas * kLogits * 4;    // per token: 16 x 24 partial dots
 
 struct Args {
@@ -79,7 +82,7 @@ struct Args {
 
 // Shared-memory carve-up (bytes), in this order.
 struct Layout {
-    int xs, hs, red, pin, nw, sq, dots, scale, bars, abort_flag, total;
+    int xs, hs, red, pin, nw, sq, dots, bars, abort_flag, total;
 };
 __host__ __device__ inline int dec_xstride(int lcmax) {
     // 64 bytes per group (4 streams x 8 bf16); rows an odd multiple of 64
@@ -94,10 +97,9 @@ __host__ __device__ inline Layout dec_layout(int lcmax) {
     L.red = o;   o += kWarps * kMaxTile * kLogits * 4;
     L.pin = o;   o += kMaxTile * 16;
     L.nw = o;    o += ((8 * lcmax * 2 + 15) / 16) * 16;
-    L.sq = o;    o += kSlots * kCtas * 2 * 4;
+    L.sq = o;    o += 2 * kMaxTile * kCtas * 2 * 4;
     L.dots = o;  o += 2 * kSlots * kCtas * kLogits * 4;
-    L.scale = o; o += kMaxTile * 4;
-    L.bars = o;  o += 8 * 8;
+    L.bars = o;  o += kNumBars * 8;
     L.abort_flag = o; o += 16;
     L.total = o;
     return L;
@@ -147,13 +149,11 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
     float* red = reinterpret_cast<float*>(smem + L.red);
     float* pin = reinterpret_cast<float*>(smem + L.pin);
     uint16_t* nw = reinterpret_cast<uint16_t*>(smem + L.nw);
-    float* inbox_sq = reinterpret_cast<float*>(smem + L.sq);      // [slot][src][2]
+    float* inbox_sq = reinterpret_cast<float*>(smem + L.sq);      // [parity][token][src][2]
     float* inbox_dots = reinterpret_cast<float*>(smem + L.dots);  // [parity][slot][src][24]
-    float* scale_in = reinterpret_cast<float*>(smem + L.scale);   // [token]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
-    uint64_t* sq_full = bars;              // [slot]
-    uint64_t* dots_full = bars + kSlots;   // [parity][slot]
-    uint64_t* scale_full = bars + 3 * kSlots;
+    uint64_t* sq_full = bars;              // [parity]
+    uint64_t* dots_full = bars + 2;        // [parity][slot]
     volatile int* abort = reinterpret_cast<volatile int*>(smem + L.abort_flag);
     const int hstride = 8 * a.lcmax;       // floats per token row of h
 
@@ -167,16 +167,22 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
     // ---- set-up: barriers armed for the first tile
     int64_t tile = cid;
     int nv = tile_tokens(tile);
+    // Phases of tile k: sq_full[k & 1] (every token's 16 partials) and
+    // dots_full[k & 1][slot] (the finalised tokens' 16 x 24 partials).  The
+    // first tile's are armed here, tile k + 1's at the start of tile k:
+    // before this CTA pushes tile k's dots, which every sender of tile
+    // k + 1 bytes must have received first, and after tile k - 1's phases of
+    // the same barriers completed.
+    auto arm = [&](int parity, int n) {
+        mbar_arrive_expect_tx(&sq_full[parity], kSqBytes * n);
+        for (int s = 0; s < kSlots; ++s)
+            if (kCtas * s + rank < n) mbar_arrive_expect_tx(&dots_full[parity * kSlots + s], kDotsBytes);
+    };
     if (tid == 0) {
-        for (int i = 0; i < 3 * kSlots + 1; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < kNumBars; ++i) mbar_init(&bars[i], 1);
         *abort = 0;
         fence_mbar_init_cluster();
-        for (int s = 0; s < kSlots; ++s)
-            if (kCtas * s + rank < nv) {
-                mbar_arrive_expect_tx(&sq_full[s], kSqBytes);
-                mbar_arrive_expect_tx(&dots_full[s], kDotsBytes);
-            }
-        mbar_arrive_expect_tx(scale_full, 4 * nv);
+        arm(0, nv);
     }
     // Relaxed: this arrival waits for none of the loads below.  The matching
     // wait comes before the first push into another CTA.
@@ -248,6 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
         const int par = round & 1;
         cp_async_wait_all();
         __syncthreads();
+        if (tid == 0 && nv_next > 0) arm(par ^ 1, nv_next);
 
         // ---- 2. collapse (warps 2..11), one token per warp at a time
         if (warp >= kRowWarp0) {
@@ -283,11 +290,9 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
                     sx += __shfl_xor_sync(0xffffffffu, sx, o);
                     sh += __shfl_xor_sync(0xffffffffu, sh, o);
                 }
-                if (lane == 0) {
-                    const uint32_t f = (uint32_t)(tt % kCtas), s = (uint32_t)(tt / kCtas);
-                    st_async_v2(mapa(smem_u32(inbox_sq + (s * kCtas + rank) * 2), f), sx, sh,
-                                mapa(smem_u32(&sq_full[s]), f));
-                }
+                if (lane < kCtas)   // every lane holds both sums; lane d sends them to CTA d
+                    st_async_v2(mapa(smem_u32(inbox_sq + ((par * kMaxTile + tt) * kCtas + rank) * 2), lane), sx, sh,
+                                mapa(smem_u32(&sq_full[par]), lane));
             }
         }
 
@@ -354,47 +359,33 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
                         s.x, s.y, s.z, s.w, mapa(smem_u32(&dots_full[par * kSlots + slot]), f));
         }
 
+        if (last) {
+            // every push of this CTA has been issued (relaxed: the receivers
+            // count the bytes on their barriers; this barrier only keeps a
+            // CTA from leaving while a peer may still push into it)
+            cluster_arrive_relaxed();
+            arrived = true;
+        }
+
         // ---- 5. finalise token 16 * warp + rank (warps 0, 1)
         if (warp < kSlots) {
             const int slot = warp;
             const int tok = kCtas * slot + rank;
             if (tok < nv) {
                 const int64_t t = t0 + tok;
-                bool ok = mbar_wait<true>(&sq_full[slot], par, abort);
-                // Arm the next tile's phases of this slot now, before this
-                // tile's scales leave: every push of the next tile happens
-                // after its sender received them, so no byte can reach a
-                // phase before its expect_tx (and the previous phase of the
-                // other dots buffer completed a tile ago).
-                __syncwarp();
-                if (lane == 0 && nv_next > tok) {
-                    mbar_arrive_expect_tx(&sq_full[slot], kSqBytes);
-                    mbar_arrive_expect_tx(&dots_full[(par ^ 1) * kSlots + slot], kDotsBytes);
-                }
-                float sx = 0.f, sh = 0.f;
-                if (lane < kCtas) {
-                    sx = inbox_sq[(slot * kCtas + lane) * 2];
-                    sh = inbox_sq[(slot * kCtas + lane) * 2 + 1];
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {  // lanes 16..31 add zeros: every lane ends with the sums
-                    sx += __shfl_xor_sync(0xffffffffu, sx, o);
-                    sh += __shfl_xor_sync(0xffffffffu, sh, o);
-                }
-                const float scale = 1.0f / sqrtf(sh / (float)C + a.norm_eps);
-                if (ok && lane < kCtas)
-                    st_async_f32(mapa(smem_u32(scale_in + tok), lane), scale, mapa(smem_u32(scale_full), lane));
-                if (last) {
-                    cluster_arrive_release();
-                    arrived = true;
-                }
-                ok = ok && mbar_wait<true>(&dots_full[par * kSlots + slot], (round >> 1) & 1, abort);
+                bool ok = mbar_wait<true>(&dots_full[par * kSlots + slot], (round >> 1) & 1, abort);
+                ok = ok && mbar_wait<true>(&sq_full[par], (round >> 1) & 1, abort);
                 if (ok) {
+                    // sum x^2 over the 16 slices, rank order (every lane)
+                    const float* sq = inbox_sq + (par * kMaxTile + tok) * kCtas * 2;
+                    float sx = 0.f;
+#pragma unroll
+                    for (int s2 = 0; s2 < kCtas; ++s2) sx += sq[2 * s2];
                     float l = 0.f;
                     if (lane < kLogits) {
                         const float* src = inbox_dots + (par * kSlots + slot) * kCtas * kLogits + lane;
 #pragma unroll
-                        for (int s = 0; s < kCtas; ++s) l += src[s * kLogits];
+                        for (int s2 = 0; s2 < kCtas; ++s2) l += src[s2 * kLogits];
                         const float r = 1.0f / sqrtf(sx / (float)K + a.rms_eps);
                         l = (r * l) * alpha_l + bias_l;
                         if (a.logits_out) a.logits_out[t * kLogits + lane] = l;
@@ -422,20 +413,17 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
                 }
             }
         }
-        if (last && !arrived) {
-            cluster_arrive_release();  // every push of this CTA has been issued
-            arrived = true;
-        }
-
-        // ---- 6. wait for the tile's fold scales; fold and store (warps 2..11)
+        // ---- 6. fold scales from the 16 sum h^2 partials; fold and store
+        //         (warps 2..11)
         if (warp >= kRowWarp0) {
-            const bool ok = mbar_wait<true>(scale_full, par, abort);
-            // next tile's phase: its scales need this CTA's next sq pushes,
-            // which follow the next tile's __syncthreads, so the arm is first
-            if (tid == 32 * kRowWarp0 && nv_next > 0) mbar_arrive_expect_tx(scale_full, 4 * nv_next);
+            const bool ok = mbar_wait<true>(&sq_full[par], (round >> 1) & 1, abort);
             if (fold && ok) {
                 for (int tt = warp - kRowWarp0; tt < nv; tt += kRowWarps) {
-                    const float s = scale_in[tt];
+                    const float* sq = inbox_sq + (par * kMaxTile + tt) * kCtas * 2;
+                    float sh = 0.f;
+#pragma unroll
+                    for (int s2 = 0; s2 < kCtas; ++s2) sh += sq[2 * s2 + 1];
+                    const float s = 1.0f / sqrtf(sh / (float)C + a.norm_eps);
                     for (int cc = lane; cc < lc; cc += 32) {
                         const float4* hp = reinterpret_cast<const float4*>(hs + tt * hstride + 8 * cc);
                         const float4 h0 = hp[0], h1 = hp[1];
@@ -450,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
             }
         }
     }
-    if (!arrived) cluster_arrive_release();  // (a CTA with no tile)
+    if (!arrived) cluster_arrive_relaxed();  // (a CTA with no tile)
     cp_async_wait_all();
     cluster_wait_acquire();  // no CTA leaves while a peer may still push into it
 }
