@@ -346,8 +346,15 @@ def run_ours(args, rank, world, local):
                 pre_call(st)
                 mhc.post(dd["x"], dd["y"], o["comb"], o["post"], out=xn, stream=st)
 
+            def fused_call(st):
+                # post of the previous seam (its gates: o) fused with this pre
+                mhc.post_pre_delayed(dd["x"], dd["y"], o["comb"], o["post"], dd["pre_in"], dd["fn"], dd["bias"],
+                                     dd["alpha"], dd["norm_w"], x_new=xn, out=o, stream=st)
+
             for name, one, ov in (("pre", pre_call, False), ("seam", seam_call, False),
-                                  ("pre_overlap", pre_call, True), ("seam_overlap", seam_call, True)):
+                                  ("fused_seam", fused_call, False),
+                                  ("pre_overlap", pre_call, True), ("seam_overlap", seam_call, True),
+                                  ("fused_seam_overlap", fused_call, True)):
                 mhc.set_launch_overlap(ov)
                 # DECODE_REPS calls back to back in one graph: the GPU time per
                 # call, not the host's graph-launch rate
@@ -385,13 +392,28 @@ def run_ours(args, rank, world, local):
                     torch.add(co["layer_input"], deltas[si], out=cy)   # synthetic sublayer
                 mhc.post(cx, cy, co["comb"], co["post"], out=cx, stream=st)
 
+        def chain_step_fused(st):
+            # the same step with post(s - 1) fused into pre(s)
+            for si in range(CHAIN_SEAMS):
+                p = params[si]
+                o = dict(co, pre=cp[(si + 1) & 1])
+                if si == 0:
+                    mhc.pre_delayed(cx, cp[0], p["fn"], p["bias"], p["alpha"], p["norm_w"], out=o, stream=st)
+                else:
+                    mhc.post_pre_delayed(cx, cy, co["comb"], co["post"], cp[si & 1], p["fn"], p["bias"],
+                                         p["alpha"], p["norm_w"], x_new=cx, out=o, stream=st)
+                with torch.cuda.stream(st):
+                    torch.add(co["layer_input"], deltas[si], out=cy)   # synthetic sublayer
+            mhc.post(cx, cy, co["comb"], co["post"], out=cx, stream=st)
+
         chain_us = {}
-        for ov in (False, True):
+        for fused, ov in ((False, False), (False, True), (True, False), (True, True)):
             mhc.set_launch_overlap(ov)
+            step_fn = chain_step_fused if fused else chain_step
             with torch.cuda.stream(s):
-                chain_step(s)
+                step_fn(s)
             s.synchronize()
-            g = SeamGraph(chain_step, s)
+            g = SeamGraph(step_fn, s)
             g.replay(3)
             meds = []
             for _ in range(5):
@@ -401,13 +423,18 @@ def run_ours(args, rank, world, local):
                 b.record(s)
                 s.synchronize()
                 meds.append(a.elapsed_time(b) * 1e3 / 200)
-            chain_us[ov] = round(statistics.median(meds), 2)
-            nodes = g.kernel_nodes
+            chain_us[(fused, ov)] = round(statistics.median(meds), 2)
+            if fused:
+                fused_nodes = g.kernel_nodes
+            else:
+                nodes = g.kernel_nodes
             g.close()
         mhc.set_launch_overlap(False)
-        chain = {"us_per_step": chain_us[False], "us_per_step_overlap": chain_us[True],
+        chain = {"us_per_step": chain_us[(False, False)], "us_per_step_overlap": chain_us[(False, True)],
+                 "us_per_step_fused": chain_us[(True, False)], "us_per_step_fused_overlap": chain_us[(True, True)],
                  "seams": CHAIN_SEAMS, "T": CHAIN_T, "kernel_nodes": nodes,
                  "launches_per_seam": (nodes - CHAIN_SEAMS) / CHAIN_SEAMS,
+                 "launches_per_seam_fused": (fused_nodes - CHAIN_SEAMS) / CHAIN_SEAMS,
                  "l2": "fn of 80 seams = 157 MB > L2"}
         g.close()
 

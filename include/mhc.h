@@ -152,6 +152,40 @@ mhc_status mhc_post(const uint16_t *x, const uint16_t *y, const float *comb,
                     const float *post, int64_t T, int n, int C, uint16_t *x_new,
                     void *stream);
 
+/*
+ * mhc_post_pre_delayed -- one seam boundary in a single call: the PREVIOUS
+ * seam's post (as mhc_post, on x, y, comb, post) followed by THIS seam's
+ * delayed pre (as mhc_pre_delayed) on its result x_new.  The survey of the
+ * pages ranks this fusion as the next step after the two blocks: a decoder
+ * runs ... pre(s) -> sublayer -> post(s) -> pre(s+1) ..., and post(s) and
+ * pre(s+1) meet at x_new ([A] "Result": the seam's launch count is the
+ * figure the pages track; the next seam's pre reads exactly the x_new the
+ * post writes).
+ *  x, y, comb, post, x_new  as mhc_post (comb/post: the previous seam's
+ *                            outputs); x_new is written.
+ *  all other arguments      as mhc_pre_delayed, with x_new in place of x.
+ * Results are bit-identical to mhc_post followed by mhc_pre_delayed on the
+ * same arguments.  Below 256 tokens (and for hidden sizes the tensor-core
+ * kernel does not take) this is ONE kernel: each CTA forms x_new for its
+ * column slice of the tile, writes it out and runs the pre block on it from
+ * shared memory (x is read once).  From 256 tokens on it is two launches,
+ * the post kernel then the tensor-core pre kernel; the workspace is then
+ * needed as for mhc_pre_delayed (mhc_pre_workspace_bytes).
+ * Aliasing: x_new may be exactly x; comb_out may be exactly comb and
+ * post_out exactly post (one gate buffer carried along a chain); pre_out
+ * must not overlap pre_in; nothing else may overlap.
+ * Errors as mhc_pre_delayed; additionally y, comb, post, x_new are
+ * required, 16-byte aligned.
+ */
+mhc_status mhc_post_pre_delayed(const uint16_t *x, const uint16_t *y, const float *comb,
+                                const float *post, uint16_t *x_new, const float *pre_in,
+                                const float *fn, const float *bias, const float *alpha,
+                                const uint16_t *norm_weight, int64_t T, int n, int C,
+                                int sinkhorn_iters, float rms_eps, float norm_eps,
+                                float sinkhorn_eps, float *pre_out, float *post_out,
+                                float *comb_out, uint16_t *layer_input, float *logits_out,
+                                void *workspace, size_t workspace_bytes, void *stream);
+
 /* Static description of the status code (never NULL). */
 const char *mhc_status_string(mhc_status status);
 

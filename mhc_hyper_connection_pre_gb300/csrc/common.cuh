@@ -83,6 +83,40 @@ __device__ __forceinline__ void griddep_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// mHC post on 8 columns of one token: out[j][e] = sum_i cw[i][j] x[i][e]
+// + pw[j] y[e] in fp32, the sum over i in order 0..3 (the first term a
+// product, then fused multiply-adds), then + post * y, one rounding to bf16
+// per output.  Taken one stream at a time (post_mix_first for i = 0,
+// post_mix_next for i = 1..3, post_mix_last); the post kernel and the fused
+// post + pre kernel both use these steps, so the two give the same bits.
+// cw / pw: the coefficients of the NJ outputs taken (comb row i from the
+// first of them, post of each).
+template <int NJ>
+__device__ __forceinline__ void post_mix_first(float (&acc)[NJ][8], const float (&x)[8], const float* cw) {
+#pragma unroll
+    for (int j = 0; j < NJ; ++j)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[j][e] = cw[j] * x[e];
+}
+template <int NJ>
+__device__ __forceinline__ void post_mix_next(float (&acc)[NJ][8], const float (&x)[8], const float* cw) {
+#pragma unroll
+    for (int j = 0; j < NJ; ++j)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[j][e] = fmaf(cw[j], x[e], acc[j][e]);
+}
+template <int NJ>
+__device__ __forceinline__ void post_mix_last(const float (&acc)[NJ][8], const float (&y)[8], const float* pw,
+                                              uint4 (&out)[NJ]) {
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+        float o[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = fmaf(pw[j], y[e], acc[j][e]);
+        out[j] = pack8(o);
+    }
+}
+
 // Streaming 16-byte global load / store (data touched once).
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
 __device__ __forceinline__ void st_stream(uint4* p, const uint4& v) { __stcs(p, v); }

@@ -16,7 +16,8 @@ cudaError_t launch_pre_cluster(const uint16_t* x, const float* pre_in, const flo
                                int64_t T, int C, int iters, float rms_eps, float norm_eps,
                                float sk_eps, float* pre_out, float* post_out, float* comb_out,
                                uint16_t* layer_input, float* logits_out, cudaStream_t stream,
-                               int max_clusters, bool overlap);
+                               int max_clusters, bool overlap, const uint16_t* y, const float* comb_prev,
+                               const float* post_prev, uint16_t* x_new);
 int pre_cluster_tile_tokens(int64_t T, int max_clusters);
 int pre_cluster_max_tile();
 int pre_cluster_ctas();
@@ -175,12 +176,21 @@ size_t mhc_pre_workspace_bytes(int64_t T, int n, int C) {
     return tcc > 0 ? mhc::pre_tc_workspace_bytes(T, C, tcc) : 0;
 }
 
-mhc_status mhc_pre_delayed(const uint16_t* x, const float* pre_in, const float* fn,
-                           const float* bias, const float* alpha, const uint16_t* norm_weight,
-                           int64_t T, int n, int C, int sinkhorn_iters, float rms_eps,
-                           float norm_eps, float sinkhorn_eps, float* pre_out, float* post_out,
-                           float* comb_out, uint16_t* layer_input, float* logits_out,
-                           void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+struct Span { const void* p; size_t n; };
+
+// Host-side checks shared by mhc_pre_delayed and mhc_post_pre_delayed, then
+// the launch(es).  fused: the previous seam's post runs first on x (into
+// x_new) and the pre block reads x_new.
+mhc_status pre_entry(const uint16_t* x, const float* pre_in, const float* fn, const float* bias,
+                     const float* alpha, const uint16_t* norm_weight, int64_t T, int n, int C,
+                     int sinkhorn_iters, float rms_eps, float norm_eps, float sinkhorn_eps, float* pre_out,
+                     float* post_out, float* comb_out, uint16_t* layer_input, float* logits_out, void* workspace,
+                     size_t workspace_bytes, void* stream, bool fused, const uint16_t* y, const float* comb_prev,
+                     const float* post_prev, uint16_t* x_new) {
     mhc_status st = check_pre_shape(T, n, C, sinkhorn_iters);
     if (st != MHC_OK) return st;
     if (!(rms_eps >= 0.f) || !(norm_eps >= 0.f) || !(sinkhorn_eps >= 0.f)) return MHC_ERR_INVALID_ARGUMENT;
@@ -188,44 +198,92 @@ mhc_status mhc_pre_delayed(const uint16_t* x, const float* pre_in, const float* 
     const void* req[] = {x, pre_in, fn, bias, alpha, pre_out, post_out, comb_out, layer_input};
     for (const void* p : req)
         if (!p || !aligned16(p)) return MHC_ERR_INVALID_ARGUMENT;
+    if (fused) {
+        const void* req2[] = {y, comb_prev, post_prev, x_new};
+        for (const void* p : req2)
+            if (!p || !aligned16(p)) return MHC_ERR_INVALID_ARGUMENT;
+    }
     if ((norm_weight && !aligned16(norm_weight)) || (logits_out && !aligned16(logits_out)))
         return MHC_ERR_INVALID_ARGUMENT;
     const int M = 2 * n + n * n;
     const size_t xb = (size_t)T * n * C * 2, pb = (size_t)T * n * 4, cb = (size_t)T * n * n * 4;
     const size_t lib = (size_t)T * C * 2, lob = (size_t)T * M * 4;
     const size_t fnb = (size_t)M * n * C * 4, bb = (size_t)M * 4, ab = 12, nwb = (size_t)C * 2;
-    struct R { const void* p; size_t n; };
-    const R ins[] = {{x, xb}, {pre_in, pb}, {fn, fnb}, {bias, bb}, {alpha, ab}, {norm_weight, nwb}};
-    const R outs[] = {{pre_out, pb}, {post_out, pb}, {comb_out, cb}, {layer_input, lib}, {logits_out, lob},
-                      {workspace, workspace_bytes}};
-    for (const R& o : outs) {
-        for (const R& i : ins)
-            if (overlaps(o.p, o.n, i.p, i.n)) return MHC_ERR_INVALID_ARGUMENT;
-        for (const R& o2 : outs)
+    // Exact aliases allowed when fused: x_new == x, comb_out == comb_prev,
+    // post_out == post_prev (each is read, for a token, before it is written).
+    const Span ins[] = {{x, xb}, {pre_in, pb}, {fn, fnb}, {bias, bb}, {alpha, ab}, {norm_weight, nwb},
+                        {fused ? y : nullptr, lib}, {fused ? comb_prev : nullptr, cb},
+                        {fused ? post_prev : nullptr, pb}};
+    const Span outs[] = {{pre_out, pb}, {post_out, pb}, {comb_out, cb}, {layer_input, lib}, {logits_out, lob},
+                         {workspace, workspace_bytes}, {fused ? x_new : nullptr, xb}};
+    for (const Span& o : outs) {
+        for (const Span& i : ins) {
+            const bool exact_alias = fused && o.p == i.p &&
+                                     ((o.p == x_new && i.p == x) || (o.p == comb_out && i.p == comb_prev) ||
+                                      (o.p == post_out && i.p == post_prev));
+            if (!exact_alias && overlaps(o.p, o.n, i.p, i.n)) return MHC_ERR_INVALID_ARGUMENT;
+        }
+        for (const Span& o2 : outs)
             if (&o != &o2 && overlaps(o.p, o.n, o2.p, o2.n)) return MHC_ERR_INVALID_ARGUMENT;
     }
     int dev = current_device();
     if (dev < 0) return MHC_ERR_CUDA;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool overlap = g_launch_overlap.load() != 0;
     if (use_tc(T, C)) {
         int tcc = tc_clusters(dev);
         if (tcc > 0) {
             const size_t need = mhc::pre_tc_workspace_bytes(T, C, tcc);
             if (workspace_bytes < need || (need && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))))
                 return MHC_ERR_INVALID_ARGUMENT;
-            cudaError_t e = mhc::launch_pre_tc(x, pre_in, fn, bias, alpha, norm_weight, T, C, sinkhorn_iters,
+            const uint16_t* xin = x;
+            if (fused) {   // large T: the post kernel, then the tensor-core pre on x_new
+                int sms = num_sms(dev);
+                if (sms <= 0) return MHC_ERR_CUDA;
+                if (mhc::launch_post(x, y, comb_prev, post_prev, T, C, x_new, s, sms, overlap) != cudaSuccess)
+                    return MHC_ERR_CUDA;
+                xin = x_new;
+            }
+            cudaError_t e = mhc::launch_pre_tc(xin, pre_in, fn, bias, alpha, norm_weight, T, C, sinkhorn_iters,
                                                rms_eps, norm_eps, sinkhorn_eps, pre_out, post_out, comb_out,
-                                               layer_input, logits_out, workspace,
-                                               static_cast<cudaStream_t>(stream), tcc);
+                                               layer_input, logits_out, workspace, s, tcc);
             return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA;
         }
     }
     int mc = max_clusters(dev, C);
     if (mc <= 0) return MHC_ERR_CUDA;
-    cudaError_t e = mhc::launch_pre_cluster(
-        x, pre_in, fn, bias, alpha, norm_weight, T, C, sinkhorn_iters, rms_eps, norm_eps,
-        sinkhorn_eps, pre_out, post_out, comb_out, layer_input, logits_out,
-        static_cast<cudaStream_t>(stream), mc, g_launch_overlap.load() != 0);
+    cudaError_t e = mhc::launch_pre_cluster(x, pre_in, fn, bias, alpha, norm_weight, T, C, sinkhorn_iters, rms_eps,
+                                            norm_eps, sinkhorn_eps, pre_out, post_out, comb_out, layer_input,
+                                            logits_out, s, mc, overlap, fused ? y : nullptr,
+                                            fused ? comb_prev : nullptr, fused ? post_prev : nullptr,
+                                            fused ? x_new : nullptr);
     return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+mhc_status mhc_pre_delayed(const uint16_t* x, const float* pre_in, const float* fn,
+                           const float* bias, const float* alpha, const uint16_t* norm_weight,
+                           int64_t T, int n, int C, int sinkhorn_iters, float rms_eps,
+                           float norm_eps, float sinkhorn_eps, float* pre_out, float* post_out,
+                           float* comb_out, uint16_t* layer_input, float* logits_out,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+    return pre_entry(x, pre_in, fn, bias, alpha, norm_weight, T, n, C, sinkhorn_iters, rms_eps, norm_eps,
+                     sinkhorn_eps, pre_out, post_out, comb_out, layer_input, logits_out, workspace, workspace_bytes,
+                     stream, false, nullptr, nullptr, nullptr, nullptr);
+}
+
+mhc_status mhc_post_pre_delayed(const uint16_t* x, const uint16_t* y, const float* comb, const float* post,
+                                uint16_t* x_new, const float* pre_in, const float* fn, const float* bias,
+                                const float* alpha, const uint16_t* norm_weight, int64_t T, int n, int C,
+                                int sinkhorn_iters, float rms_eps, float norm_eps, float sinkhorn_eps,
+                                float* pre_out, float* post_out, float* comb_out, uint16_t* layer_input,
+                                float* logits_out, void* workspace, size_t workspace_bytes, void* stream) {
+    return pre_entry(x, pre_in, fn, bias, alpha, norm_weight, T, n, C, sinkhorn_iters, rms_eps, norm_eps,
+                     sinkhorn_eps, pre_out, post_out, comb_out, layer_input, logits_out, workspace, workspace_bytes,
+                     stream, true, y, comb, post, x_new);
 }
 
 mhc_status mhc_post(const uint16_t* x, const uint16_t* y, const float* comb, const float* post,

@@ -57,20 +57,16 @@ post_kernel(const uint4* x, const uint4* __restrict__ y,
 #pragma unroll
             for (int i = 0; i < 4; ++i) unpack8(xv[u][i], xs[i]);
             unpack8(yv[u], ys);
+            float acc[4][8];
+            post_mix_first<4>(acc, xs[0], cw[0]);
+            post_mix_next<4>(acc, xs[1], cw[1]);
+            post_mix_next<4>(acc, xs[2], cw[2]);
+            post_mix_next<4>(acc, xs[3], cw[3]);
+            uint4 ov[4];
+            post_mix_last<4>(acc, ys, pw, ov);
             uint4* op = x_new + tok[u] * (4 * (int64_t)c8) + col[u];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float o[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    float acc = cw[0][j] * xs[0][e];
-                    acc = fmaf(cw[1][j], xs[1][e], acc);
-                    acc = fmaf(cw[2][j], xs[2][e], acc);
-                    acc = fmaf(cw[3][j], xs[3][e], acc);
-                    o[e] = fmaf(pw[j], ys[e], acc);
-                }
-                st_stream(op + (int64_t)j * c8, pack8(o));
-            }
+            for (int j = 0; j < 4; ++j) st_stream(op + (int64_t)j * c8, ov[j]);
         }
     }
 }

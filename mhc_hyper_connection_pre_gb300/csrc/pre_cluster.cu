@@ -36,6 +36,11 @@
 //   6. meanwhile warps 2..11 form each token's fold scale from the 16 sum h^2
 //      partials (the same sum, in rank order, in every CTA: the same bits),
 //      fold h and store layer_input.
+// Fused with the previous seam's post (y != nullptr): before step 2 every
+// thread turns its share of the tile's x slice into x_new = post(x, y, comb,
+// post) with the post kernel's arithmetic (the same bits), writes it out and
+// leaves it in shared memory, where the pre block reads it in place of x.
+//
 // Every push is an st.async into the receiver's shared memory that completes
 // bytes on the receiver's mbarrier, so no CTA waits at a cluster barrier for
 // the slowest one inside a tile; all waits are bounded (a timeout sets the
@@ -78,18 +83,23 @@ struct Args {
     int tile;      // tokens per tile (1..kMaxTile)
     int lcmax;     // max 8-column groups per CTA slice
     int xstride;   // bytes per token row of the x tile in shared memory
+    // previous seam's post, fused in front (y == nullptr: none)
+    const uint16_t* y;
+    const float* comb_prev;
+    const float* post_prev;
+    uint16_t* x_new;
 };
 
 // Shared-memory carve-up (bytes), in this order.
 struct Layout {
-    int xs, hs, red, pin, nw, sq, dots, bars, abort_flag, total;
+    int xs, hs, red, pin, nw, sq, dots, ys, gates, bars, abort_flag, total;
 };
 __host__ __device__ inline int dec_xstride(int lcmax) {
     // 64 bytes per group (4 streams x 8 bf16); rows an odd multiple of 64
     // bytes apart so that the MMA's row loads of 8 tokens hit distinct banks
     return ((64 * lcmax + 127) / 128) * 128 + 64;
 }
-__host__ __device__ inline Layout dec_layout(int lcmax) {
+__host__ __device__ inline Layout dec_layout(int lcmax, bool fused) {
     Layout L;
     int o = 0;
     L.xs = o;    o += kMaxTile * dec_xstride(lcmax);
@@ -99,6 +109,11 @@ __host__ __device__ inline Layout dec_layout(int lcmax) {
     L.nw = o;    o += ((8 * lcmax * 2 + 15) / 16) * 16;
     L.sq = o;    o += 2 * kMaxTile * kCtas * 2 * 4;
     L.dots = o;  o += 2 * kSlots * kCtas * kLogits * 4;
+    // fused post inputs share memory with buffers first written after the
+    // post step: the y slice with h, the gates with the warps' partials
+    L.ys = L.hs;     // kMaxTile x 8 lcmax bf16 <= the h buffer
+    L.gates = L.red; // kMaxTile x 20 fp32 <= the partials buffer
+    (void)fused;
     L.bars = o;  o += kNumBars * 8;
     L.abort_flag = o; o += 16;
     L.total = o;
@@ -127,7 +142,7 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-template <int JMAX>
+template <int JMAX, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
     const int rank = (int)cluster_ctarank();
     const int64_t cid = cluster_id_x();
@@ -140,10 +155,11 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
     const int ncols = 8 * lc;
     const int c0 = 8 * ch0;
     const bool fold = a.norm_w != nullptr;
+    constexpr bool fused = FUSED;   // the previous seam's post runs first
     const int TT = a.tile;
 
     extern __shared__ __align__(128) unsigned char smem[];
-    const Layout L = dec_layout(a.lcmax);
+    const Layout L = dec_layout(a.lcmax, FUSED);
     unsigned char* xs = smem + L.xs;
     float* hs = reinterpret_cast<float*>(smem + L.hs);
     float* red = reinterpret_cast<float*>(smem + L.red);
@@ -151,6 +167,8 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
     uint16_t* nw = reinterpret_cast<uint16_t*>(smem + L.nw);
     float* inbox_sq = reinterpret_cast<float*>(smem + L.sq);      // [parity][token][src][2]
     float* inbox_dots = reinterpret_cast<float*>(smem + L.dots);  // [parity][slot][src][24]
+    uint16_t* ys = reinterpret_cast<uint16_t*>(smem + L.ys);         // [token][8 lcmax]
+    float* gts = reinterpret_cast<float*>(smem + L.gates);          // [token][comb 16, post 4]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
     uint64_t* sq_full = bars;              // [parity]
     uint64_t* dots_full = bars + 2;        // [parity][slot]
@@ -227,6 +245,22 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
         }
         if (tid < n) cp_async16(smem_u32(pin + 4 * tid), a.pre_in + (t0 + tid) * 4);
     };
+    // y slice and gates of a tile (fused post).  Their buffers double as h and
+    // the partials later in a tile, so a later tile's are loaded at its start.
+    auto issue_post_inputs = [&](int64_t tl, int n) {
+        const int64_t t0 = tl * TT;
+        {
+            for (int idx = tid; idx < n * lc; idx += kThreads) {
+                const int tt = idx / lc, cc = idx - tt * lc;
+                cp_async16(smem_u32(ys + tt * 8 * a.lcmax + 8 * cc), a.y + (t0 + tt) * C + c0 + 8 * cc);
+            }
+            for (int idx = tid; idx < n * 5; idx += kThreads) {
+                const int tt = idx / 5, k = idx - tt * 5;
+                const float* src = k < 4 ? a.comb_prev + (t0 + tt) * 16 + 4 * k : a.post_prev + (t0 + tt) * 4;
+                cp_async16(smem_u32(gts + tt * 20 + 4 * k), src);
+            }
+        }
+    };
     if (fold)
         for (int cc = tid; cc < lc; cc += kThreads) cp_async16(smem_u32(nw + 8 * cc), a.norm_w + c0 + 8 * cc);
 
@@ -242,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
     // x and pre_in may be that kernel's output.
     griddep_wait();
     issue_tile(tile, nv);
+    if (fused) issue_post_inputs(tile, nv);
     cp_async_commit();
     cluster_wait_acquire();  // every CTA's barriers are initialised before any push
 
@@ -255,6 +290,51 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
         cp_async_wait_all();
         __syncthreads();
         if (tid == 0 && nv_next > 0) arm(par ^ 1, nv_next);
+        if (fused && round > 0) {   // h and the partials of the last tile are dead now
+            issue_post_inputs(tile, nv);
+            cp_async_commit();
+            cp_async_wait_all();
+            __syncthreads();
+        }
+
+        // ---- 1b. fused post of the previous seam: x_new for this CTA's
+        //          slice of the tile, written out and kept in place of x
+        if (fused) {
+            for (int it = tid; it < nv * lc; it += kThreads) {
+                const int tt = it / lc, cc = it - tt * lc;
+                const float* gt = gts + tt * 20;
+                // the item's four streams stay packed in registers, so each
+                // output can overwrite its stream in place at once
+                uint4 xp[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    xp[i] = *reinterpret_cast<const uint4*>(xs + tt * a.xstride + (i * ncols + 8 * cc) * 2);
+                const uint4 yp = *reinterpret_cast<const uint4*>(ys + tt * 8 * a.lcmax + 8 * cc);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float acc[1][8], v[8];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        unpack8(xp[i], v);
+                        if (i == 0) post_mix_first<1>(acc, v, gt + j);
+                        else post_mix_next<1>(acc, v, gt + 4 * i + j);
+                    }
+                    unpack8(yp, v);
+                    uint4 o[1];
+                    post_mix_last<1>(acc, v, gt + 16 + j, o);
+                    *reinterpret_cast<uint4*>(xs + tt * a.xstride + (j * ncols + 8 * cc) * 2) = o[0];
+                }
+            }
+            fence_proxy_async_smem();   // the tile's x_new is read by bulk copies below
+            __syncthreads();
+            // x_new out: one bulk copy per (token, stream) row of the slice
+            if (tid < 4 * nv && ncols > 0) {
+                const int tt = tid >> 2, i = tid & 3;
+                bulk_store(a.x_new + ((t0 + tt) * 4 + i) * (int64_t)C + c0, xs + tt * a.xstride + i * ncols * 2,
+                           (uint32_t)ncols * 2);
+                bulk_commit_group();
+            }
+        }
 
         // ---- 2. collapse (warps 2..11), one token per warp at a time
         if (warp >= kRowWarp0) {
@@ -337,6 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
                     make_float2(dh[nt][2] + dl[nt][2], dh[nt][3] + dl[nt][3]);
             }
         }
+        if (fused && tid < 4 * nv) bulk_wait_read_all();   // x_new copies done reading the x tile
         __syncthreads();  // partials complete; the x tile and pre_in are free
 
         if (!last) {
@@ -440,6 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
     }
     if (!arrived) cluster_arrive_relaxed();  // (a CTA with no tile)
     cp_async_wait_all();
+    if (fused) bulk_wait_all();   // x_new copies complete before the CTA leaves
     cluster_wait_acquire();  // no CTA leaves while a peer may still push into it
 }
 
@@ -486,28 +568,31 @@ int pre_cluster_tile_tokens(int64_t T, int max_clusters) {
 // returns the maximum number of co-resident clusters (0 on error).  Must run
 // before any stream capture that records the kernel.
 int pre_cluster_prepare(int C) {
-    const size_t smem = (size_t)dec::dec_layout(dec::lcmax_of(C)).total;
     // the attribute belongs to the kernel instance, which several hidden
-    // sizes share: allow the largest slice that instance takes
+    // sizes share: allow the largest slice that instance takes; the plan
+    // uses the smaller of the two instances' co-resident cluster counts
     const int jmax = dec::jmax_of(C);
-    const size_t smem_cap = (size_t)dec::dec_layout(dec::kWarps * jmax).total;
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = dec::cluster_config(attr, smem, nullptr);
-    int n = 0;
+    int n_min = 0;
     cudaError_t e = cudaSuccess;
-    auto setup = [&](auto kern) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    auto setup = [&](auto kern, bool fused) {
+        const size_t smem = (size_t)dec::dec_layout(dec::lcmax_of(C), fused).total;
+        const size_t smem_cap = (size_t)dec::dec_layout(dec::kWarps * jmax, fused).total;
+        cudaLaunchAttribute attr[1];
+        cudaLaunchConfig_t cfg = dec::cluster_config(attr, smem, nullptr);
+        int n = 0;
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_cap);
         if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        n_min = (n_min == 0 || n < n_min) ? n : n_min;
     };
     switch (jmax) {
-        case 1: setup(dec::pre_decode_kernel<1>); break;
-        case 2: setup(dec::pre_decode_kernel<2>); break;
-        case 4: setup(dec::pre_decode_kernel<4>); break;
+        case 1: setup(dec::pre_decode_kernel<1, false>, false); setup(dec::pre_decode_kernel<1, true>, true); break;
+        case 2: setup(dec::pre_decode_kernel<2, false>, false); setup(dec::pre_decode_kernel<2, true>, true); break;
+        case 4: setup(dec::pre_decode_kernel<4, false>, false); setup(dec::pre_decode_kernel<4, true>, true); break;
         default: return 0;
     }
-    return e == cudaSuccess ? n : 0;
+    return e == cudaSuccess ? n_min : 0;
 }
 
 cudaError_t launch_pre_cluster(const uint16_t* x, const float* pre_in, const float* fn,
@@ -515,8 +600,10 @@ cudaError_t launch_pre_cluster(const uint16_t* x, const float* pre_in, const flo
                                int64_t T, int C, int iters, float rms_eps, float norm_eps,
                                float sk_eps, float* pre_out, float* post_out, float* comb_out,
                                uint16_t* layer_input, float* logits_out, cudaStream_t stream,
-                               int max_clusters, bool overlap) {
+                               int max_clusters, bool overlap, const uint16_t* y, const float* comb_prev,
+                               const float* post_prev, uint16_t* x_new) {
     dec::Args a;
+    a.y = y; a.comb_prev = comb_prev; a.post_prev = post_prev; a.x_new = x_new;
     a.x = x; a.pre_in = pre_in; a.fn = fn; a.bias = bias; a.alpha = alpha; a.norm_w = norm_w;
     a.T = T; a.C = C; a.iters = iters;
     a.rms_eps = rms_eps; a.norm_eps = norm_eps; a.sk_eps = sk_eps;
@@ -527,7 +614,8 @@ cudaError_t launch_pre_cluster(const uint16_t* x, const float* pre_in, const flo
     a.lcmax = dec::lcmax_of(C);
     a.xstride = dec::dec_xstride(a.lcmax);
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = dec::cluster_config(attr, (size_t)dec::dec_layout(a.lcmax).total, stream);
+    const bool fused = y != nullptr;
+    cudaLaunchConfig_t cfg = dec::cluster_config(attr, (size_t)dec::dec_layout(a.lcmax, fused).total, stream);
     if (overlap) {
         attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[1].val.programmaticStreamSerializationAllowed = 1;
@@ -535,10 +623,13 @@ cudaError_t launch_pre_cluster(const uint16_t* x, const float* pre_in, const flo
     }
     const int64_t nclusters = a.ntiles < max_clusters ? a.ntiles : max_clusters;
     cfg.gridDim = dim3((unsigned)(nclusters * dec::kCtas), 1, 1);
-    switch (dec::jmax_of(C)) {
-        case 1: return cudaLaunchKernelEx(&cfg, dec::pre_decode_kernel<1>, a);
-        case 2: return cudaLaunchKernelEx(&cfg, dec::pre_decode_kernel<2>, a);
-        case 4: return cudaLaunchKernelEx(&cfg, dec::pre_decode_kernel<4>, a);
+    switch (dec::jmax_of(C) * 2 + (fused ? 1 : 0)) {
+        case 2: return cudaLaunchKernelEx(&cfg, dec::pre_decode_kernel<1, false>, a);
+        case 3: return cudaLaunchKernelEx(&cfg, dec::pre_decode_kernel<1, true>, a);
+        case 4: return cudaLaunchKernelEx(&cfg, dec::pre_decode_kernel<2, false>, a);
+        case 5: return cudaLaunchKernelEx(&cfg, dec::pre_decode_kernel<2, true>, a);
+        case 8: return cudaLaunchKernelEx(&cfg, dec::pre_decode_kernel<4, false>, a);
+        case 9: return cudaLaunchKernelEx(&cfg, dec::pre_decode_kernel<4, true>, a);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -192,6 +192,13 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, const void* src, 
                  "r"(c0), "r"(c1), "r"(smem_u32(src))
                  : "memory");
 }
+// Contiguous bulk copy from this CTA's shared memory to global memory
+// (16-byte aligned addresses, size a multiple of 16; bulk async-group).
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
+                 "r"(bytes)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until this thread's committed bulk stores have finished reading their
 // shared-memory source (the buffer may be rewritten) / have fully completed.

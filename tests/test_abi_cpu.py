@@ -136,3 +136,33 @@ def test_binding_refuses_cpu_tensors(lib):
     with pytest.raises(ValueError):
         mhc.post(x, torch.zeros(2, 64, dtype=torch.bfloat16), torch.zeros(2, 4, 4),
                  torch.zeros(2, 4))
+
+
+def _fused(lib, **kw):
+    args = dict(x=A, y=A + 0x1000000, comb=A + 0x2000000, post=A + 0x2100000, x_new=A + 0x6000000,
+                pre_in=A + 0x100000, fn=A + 0x200000, bias=A + 0x3000000, alpha=A + 0x3001000,
+                norm_weight=None, T=16, n=4, C=5120, iters=20, rms_eps=1e-6, norm_eps=1e-6, sk_eps=1e-6,
+                pre_out=A + 0x4000000, post_out=A + 0x4100000, comb_out=A + 0x4200000,
+                layer_input=A + 0x4300000, logits_out=None, workspace=None, workspace_bytes=0, stream=None)
+    args.update(kw)
+    return lib.mhc_post_pre_delayed(*args.values())
+
+
+def test_fused_rejects_on_the_host(lib):
+    # x (0x10000) spans 655,360 bytes at T = 16; y sits at +0x1000000 and so on
+    assert _fused(lib, y=None) == INVALID
+    assert _fused(lib, comb=A + 0x2000008) == INVALID            # misaligned
+    assert _fused(lib, x_new=A + 0x100) == INVALID                # partial overlap with x
+    assert _fused(lib, x_new=A + 0x1000000) == INVALID            # overlaps y
+    assert _fused(lib, comb_out=A + 0x2000040) == INVALID         # partial overlap with comb
+    assert _fused(lib, pre_out=A + 0x100000) == INVALID           # pre_out aliases pre_in
+    assert _fused(lib, n=3) == UNSUPPORTED
+    assert _fused(lib, T=0, x=None, y=None) == OK
+
+
+def test_fused_exact_aliases_pass_the_host_checks(lib):
+    # x_new == x, comb_out == comb, post_out == post are allowed: with no GPU
+    # in this process the call gets past every argument check and then fails
+    # to find a device (MHC_ERR_CUDA), instead of MHC_ERR_INVALID_ARGUMENT
+    assert _fused(lib, x_new=A) == CUDA_ERR
+    assert _fused(lib, comb_out=A + 0x2000000, post_out=A + 0x2100000) == CUDA_ERR

@@ -214,6 +214,87 @@ def test_post_in_place():
     assert torch.equal(ref, x2)
 
 
+def _fused_case(T, C, fold, seed):
+    """Previous seam's gates (from a pre call on other weights) plus this
+    seam's inputs; x is the residual entering the previous seam's post."""
+    d = seam_inputs(T, C=C, seed=seed, fold=fold, with_y=True)
+    gd = _to_dev(d)
+    prev = chain_seam_params(seed % 97, C=C, device="cuda")
+    g = mhc.pre_delayed(gd["x"], gd["pre_in"], prev["fn"], prev["bias"], prev["alpha"], prev["norm_w"])
+    torch.cuda.synchronize()
+    return d, gd, g["comb"].clone(), g["post"].clone()
+
+
+@pytest.mark.parametrize("T,C,fold", [(1, 5120, True), (5, 5120, False), (32, 5120, True), (100, 5120, True),
+                                      (33, 1000, False), (300, 1000, True), (300, 5120, True), (7, 8, True)])
+def test_fused_seam_is_bit_identical_to_post_then_pre(T, C, fold):
+    """mhc_post_pre_delayed gives exactly the bits of mhc_post followed by
+    mhc_pre_delayed: one kernel below 256 tokens (and at C = 1000), two at
+    T = 300, C = 5120; multi-round tiles at T = 300, C = 1000."""
+    d, gd, comb, post = _fused_case(T, C, fold, seed=1100 + T + C)
+    xn_ref = mhc.post(gd["x"], gd["y"], comb, post)
+    ref = mhc.pre_delayed(xn_ref, gd["pre_in"], gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"], return_logits=True)
+    got = mhc.post_pre_delayed(gd["x"], gd["y"], comb, post, gd["pre_in"], gd["fn"], gd["bias"], gd["alpha"],
+                               gd["norm_w"], return_logits=True)
+    torch.cuda.synchronize()
+    assert mhc.device_status() == 0
+    assert torch.equal(got["x_new"], xn_ref)
+    for k in ("pre", "post", "comb", "layer_input", "logits"):
+        assert torch.equal(got[k], ref[k]), k
+
+
+@pytest.mark.parametrize("T", [4, 300])
+def test_fused_seam_in_place_and_shared_gate_buffers(T):
+    """x_new == x and comb_out / post_out == the incoming comb / post."""
+    d, gd, comb, post = _fused_case(T, 5120, True, seed=1300 + T)
+    xn_ref = mhc.post(gd["x"], gd["y"], comb, post)
+    ref = mhc.pre_delayed(xn_ref, gd["pre_in"], gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"])
+    x = gd["x"].clone()
+    out = {"comb": comb, "post": post}
+    got = mhc.post_pre_delayed(x, gd["y"], comb, post, gd["pre_in"], gd["fn"], gd["bias"], gd["alpha"],
+                               gd["norm_w"], x_new=x, out=out)
+    torch.cuda.synchronize()
+    assert mhc.device_status() == 0
+    assert torch.equal(x, xn_ref)
+    for k in ("pre", "post", "comb", "layer_input"):
+        assert torch.equal(got[k], ref[k]), k
+
+
+def test_fused_seam_against_the_oracle():
+    """The fused call checked against the oracle directly: x_new against the
+    oracle's post, the pre outputs against the oracle's pre on that x_new."""
+    T, C = 24, 5120
+    d, gd, comb, post = _fused_case(T, C, True, seed=1500)
+    got = mhc.post_pre_delayed(gd["x"], gd["y"], comb, post, gd["pre_in"], gd["fn"], gd["bias"], gd["alpha"],
+                               gd["norm_w"], return_logits=True)
+    torch.cuda.synchronize()
+    xb, yb = bf16_bits(d["x"]), bf16_bits(d["y"])
+    cb, pb = comb.cpu().numpy(), post.cpu().numpy()
+    o_bits, _ = oracle.post(xb, yb, cb, pb)
+    g_bits = got["x_new"].cpu().view(torch.int16).numpy().view(np.uint16)
+    assert_bf16(g_bits, o_bits, "x_new", abs_scale=post_abs_scale(xb, yb, cb, pb))
+    d2 = dict(d, x=got["x_new"].cpu())
+    o, xb2 = _oracle_pre(d2)
+    _check_pre({k: v.cpu() for k, v in got.items() if k != "x_new"}, o, xb2, d2, fold=True)
+
+
+def test_fused_seam_is_one_launch_in_a_graph():
+    d, gd, comb, post = _fused_case(4, 5120, True, seed=1600)
+    out = {"pre": torch.empty(4, 4, device="cuda"), "post": torch.empty(4, 4, device="cuda"),
+           "comb": torch.empty(4, 4, 4, device="cuda"),
+           "layer_input": torch.empty(4, 5120, dtype=torch.bfloat16, device="cuda")}
+    xn = torch.empty_like(gd["x"])
+    s = torch.cuda.Stream()
+    g = SeamGraph(lambda st: mhc.post_pre_delayed(gd["x"], gd["y"], comb, post, gd["pre_in"], gd["fn"],
+                                                  gd["bias"], gd["alpha"], gd["norm_w"], x_new=xn, out=out,
+                                                  stream=st), s)
+    assert g.kernel_nodes == 1, g.kernel_nodes
+    g.replay(3)
+    s.synchronize()
+    assert mhc.device_status() == 0
+    g.close()
+
+
 def test_graph_seam_is_two_launches_and_replays_exactly():
     """One seam (pre + post) captured in a CUDA graph holds exactly 2 kernel
     nodes; 200 replays give the eager result bit for bit."""
@@ -296,6 +377,66 @@ def test_launch_overlap_is_bit_identical(T):
             assert torch.equal(got, want)
         g = SeamGraph(lambda st: _seam_chain(b, params, ys, st), s)
         assert g.kernel_nodes == 2 * seams, g.kernel_nodes
+        reset()
+        g.replay(1)
+        s.synchronize()
+        assert mhc.device_status() == 0
+        for got, want in zip(_chain_result(b), ref):
+            assert torch.equal(got, want)
+        g.close()
+    finally:
+        mhc.set_launch_overlap(prev)
+
+
+def _fused_chain(b, params, ys, stream):
+    """The same chain with each post(s - 1) fused into pre(s): pre(0), then
+    (post(s - 1) + pre(s)) for s >= 1, then post of the last seam."""
+    outs = b["outs"]
+    for si, o in enumerate(outs):
+        p = params[si]
+        out = dict(o, pre=b["pre"][(si + 1) & 1])
+        if si == 0:
+            mhc.pre_delayed(b["x"], b["pre"][0], p["fn"], p["bias"], p["alpha"], p["norm_w"], out=out,
+                            stream=stream)
+        else:
+            q = outs[si - 1]
+            mhc.post_pre_delayed(b["x"], ys[si - 1], q["comb"], q["post"], b["pre"][si & 1], p["fn"], p["bias"],
+                                 p["alpha"], p["norm_w"], x_new=b["x"], out=out, stream=stream)
+    mhc.post(b["x"], ys[len(outs) - 1], outs[-1]["comb"], outs[-1]["post"], out=b["x"], stream=stream)
+
+
+@pytest.mark.parametrize("T", [4, 100])
+def test_fused_chain_matches_and_overlaps_exactly(T):
+    """A chain of fused seams equals the chain of separate calls bit for bit,
+    with launch overlap off and on, eager and graph-captured."""
+    seams, C, dev = 6, 5120, "cuda"
+    params = [chain_seam_params(si, device=dev) for si in range(seams)]
+    ys = [chain_stub_delta(si, T=T, device=dev) for si in range(seams)]
+    d = seam_inputs(T, seed=950 + T, device=dev)
+    b = _chain_buffers(T, seams, C, dev)
+    s = torch.cuda.Stream()
+
+    def reset():
+        b["x"].copy_(d["x"])
+        b["pre"][0].copy_(d["pre_in"])
+        torch.cuda.synchronize()
+
+    prev = mhc.set_launch_overlap(False)
+    try:
+        reset()
+        _seam_chain(b, params, ys, s)
+        s.synchronize()
+        ref = _chain_result(b)
+        for ov in (False, True):
+            mhc.set_launch_overlap(ov)
+            reset()
+            _fused_chain(b, params, ys, s)
+            s.synchronize()
+            assert mhc.device_status() == 0
+            for got, want in zip(_chain_result(b), ref):
+                assert torch.equal(got, want)
+        g = SeamGraph(lambda st: _fused_chain(b, params, ys, st), s)
+        assert g.kernel_nodes == seams + 1, g.kernel_nodes
         reset()
         g.replay(1)
         s.synchronize()
