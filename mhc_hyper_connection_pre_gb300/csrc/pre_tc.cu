@@ -35,11 +35,13 @@
 //              scale is known and stored, folded, during the next tile's
 //              stages.  At the tile end group 0 adds group 1's sums, reads the
 //              72 accumulator columns, adds the planes and pushes 26 partials
-//              to the token's finalizer CTA over DSMEM;
+//              to the token's finalizer CTA (st.async into its shared
+//              memory, bytes counted on its mbarrier);
 //   warp 10    finalizer: for its 8 tokens of the tile sums the 16 CTAs'
 //              partials in rank order, pushes the fold scale to all 16 CTAs,
 //              then logits, gates and the Sinkhorn comb in registers.
-// No global scratch; every wait is bounded (see sm100.cuh).
+// The only global scratch is the fn planes in the caller's workspace; every
+// wait is bounded (see sm100.cuh).
 #include "common.cuh"
 #include "sm100.cuh"
 
