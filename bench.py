@@ -351,8 +351,12 @@ def run_ours(args, rank, world, local):
                 mhc.post_pre_delayed(dd["x"], dd["y"], o["comb"], o["post"], dd["pre_in"], dd["fn"], dd["bias"],
                                      dd["alpha"], dd["norm_w"], x_new=xn, out=o, stream=st)
 
+            def nondelayed_call(st):
+                # the non-delayed block: collapse with its own pre-mix
+                mhc.pre(dd["x"], dd["fn"], dd["bias"], dd["alpha"], dd["norm_w"], out=o, stream=st)
+
             for name, one, ov in (("pre", pre_call, False), ("seam", seam_call, False),
-                                  ("fused_seam", fused_call, False),
+                                  ("fused_seam", fused_call, False), ("pre_nondelayed", nondelayed_call, False),
                                   ("pre_overlap", pre_call, True), ("seam_overlap", seam_call, True),
                                   ("fused_seam_overlap", fused_call, True)):
                 mhc.set_launch_overlap(ov)

@@ -96,7 +96,9 @@ mhc_status mhc_pre_delayed(const uint16_t *x, const float *pre_in, const float *
  * (host only).  0 when the shape runs on the CUDA-core kernel (fewer than 256
  * tokens, or a hidden size the tensor-core kernel does not take); otherwise
  * the per-call copy of the fn slices split into three bf16 planes, one copy
- * per co-resident 16-CTA cluster (about 20 MB at C = 5120 on a GB300).
+ * per co-resident 16-CTA cluster (about 20 MB at C = 5120 on a GB300), plus
+ * T x 16 bytes (rounded to 256) that mhc_pre uses; the same size serves
+ * mhc_pre_delayed, mhc_pre and mhc_post_pre_delayed.
  * Returns 0 as well for shapes mhc_pre_delayed rejects.
  */
 size_t mhc_pre_workspace_bytes(int64_t T, int n, int C);
@@ -151,6 +153,26 @@ mhc_status mhc_pre_delayed_noalloc(const uint16_t *x, const float *pre_in, const
 mhc_status mhc_post(const uint16_t *x, const uint16_t *y, const float *comb,
                     const float *post, int64_t T, int n, int C, uint16_t *x_new,
                     void *stream);
+
+/*
+ * mhc_pre -- the non-delayed mHC pre block (the V4 form, MHCPreOp, that [A]
+ * "Why V4.1 cannot just reuse MHCPreOp" contrasts with the delayed one; its
+ * norm_weight= keyword per [B] "The bug"): the same gates, comb and fold as
+ * mhc_pre_delayed, but the collapse uses THIS token's own pre-mix,
+ *   h[t][c] = ((pre[t][0] x[t][0][c] + pre[t][1] x[t][1][c]) + ...) + ...,
+ * with pre[t] exactly the fp32 values written to pre_out.  Equivalently:
+ * mhc_pre_delayed with pre_in := its own pre_out.  No pre_in argument; all
+ * other arguments as mhc_pre_delayed.  Below 256 tokens (and for hidden sizes
+ * the tensor-core kernel does not take) one kernel, where the finalising CTA
+ * sends each token's pre to the cluster before the collapse; from 256 tokens
+ * two tensor-core passes (the first for the gates; its pre-mix goes to a
+ * scratch area of the workspace, so mhc_pre_workspace_bytes covers it).
+ */
+mhc_status mhc_pre(const uint16_t *x, const float *fn, const float *bias, const float *alpha,
+                   const uint16_t *norm_weight, int64_t T, int n, int C, int sinkhorn_iters,
+                   float rms_eps, float norm_eps, float sinkhorn_eps, float *pre_out,
+                   float *post_out, float *comb_out, uint16_t *layer_input, float *logits_out,
+                   void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * mhc_post_pre_delayed -- one seam boundary in a single call: the PREVIOUS

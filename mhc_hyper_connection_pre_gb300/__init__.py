@@ -66,6 +66,8 @@ def load_library():
         lib.mhc_post_pre_delayed.argtypes = [P, P, P, P, P, P, P, P, P, P, I64, I, I, I, F, F, F, P, P, P, P, P,
                                              P, ctypes.c_size_t, P]
         lib.mhc_post_pre_delayed.restype = I
+        lib.mhc_pre.argtypes = [P, P, P, P, P, I64, I, I, I, F, F, F, P, P, P, P, P, P, ctypes.c_size_t, P]
+        lib.mhc_pre.restype = I
         lib.mhc_status_string.argtypes = [I]
         lib.mhc_status_string.restype = ctypes.c_char_p
         lib.mhc_pre_delayed_plan.argtypes = [I64, I, I, P, P, P, P]
@@ -176,6 +178,52 @@ def pre_delayed(x: torch.Tensor, pre_in: torch.Tensor, fn: torch.Tensor, bias: t
     st = lib.mhc_pre_delayed(*args, T, n, C, int(sinkhorn_iters), float(rms_eps), float(norm_eps),
                              float(sinkhorn_eps), *outs, ws_ptr, ws_bytes, _stream_ptr(stream, dev))
     _check("mhc_pre_delayed", st)
+    return o
+
+
+def pre(x: torch.Tensor, fn: torch.Tensor, bias: torch.Tensor, alpha: torch.Tensor,
+        norm_weight: torch.Tensor | None = None, *, sinkhorn_iters: int = SINKHORN_ITERS, rms_eps: float = 1e-6,
+        norm_eps: float = 1e-6, sinkhorn_eps: float = 1e-6, out: dict | None = None, return_logits: bool = False,
+        workspace: torch.Tensor | None = None, stream=None) -> dict:
+    """Non-delayed mHC pre block (``mhc_pre``): as ``pre_delayed`` but the
+    collapse uses each token's own pre-mix (no pre_in)."""
+    lib = load_library()
+    if x.dim() != 3:
+        raise ValueError("x must be [T, n, C]")
+    T, n, C = x.shape
+    dev = x.device
+    M = 2 * n + n * n
+    o = dict(out) if out else {}
+    if "pre" not in o:
+        o["pre"] = torch.empty(T, n, dtype=torch.float32, device=dev)
+    if "post" not in o:
+        o["post"] = torch.empty(T, n, dtype=torch.float32, device=dev)
+    if "comb" not in o:
+        o["comb"] = torch.empty(T, n, n, dtype=torch.float32, device=dev)
+    if "layer_input" not in o:
+        o["layer_input"] = torch.empty(T, C, dtype=torch.bfloat16, device=dev)
+    if return_logits and "logits" not in o:
+        o["logits"] = torch.empty(T, M, dtype=torch.float32, device=dev)
+    if fn.numel() != M * n * C or bias.numel() != M or alpha.numel() != 3:
+        raise ValueError("fn / bias / alpha have the wrong number of elements")
+    if norm_weight is not None and norm_weight.numel() != C:
+        raise ValueError("norm_weight must have C elements")
+    args = [_dev_ptr(x, "x", torch.bfloat16, dev), _dev_ptr(fn, "fn", torch.float32, dev),
+            _dev_ptr(bias, "bias", torch.float32, dev), _dev_ptr(alpha, "alpha", torch.float32, dev),
+            _dev_ptr(norm_weight, "norm_weight", torch.bfloat16, dev)]
+    outs = [_dev_ptr(o["pre"], "pre", torch.float32, dev), _dev_ptr(o["post"], "post", torch.float32, dev),
+            _dev_ptr(o["comb"], "comb", torch.float32, dev),
+            _dev_ptr(o["layer_input"], "layer_input", torch.bfloat16, dev),
+            _dev_ptr(o.get("logits"), "logits", torch.float32, dev)]
+    if workspace is None:
+        workspace = workspace_for(T, n, C, dev)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr = _dev_ptr(workspace, "workspace", torch.uint8, dev)
+        ws_bytes = workspace.numel()
+    st = lib.mhc_pre(*args, T, n, C, int(sinkhorn_iters), float(rms_eps), float(norm_eps), float(sinkhorn_eps),
+                     *outs, ws_ptr, ws_bytes, _stream_ptr(stream, dev))
+    _check("mhc_pre", st)
     return o
 
 

@@ -17,7 +17,7 @@ cudaError_t launch_pre_cluster(const uint16_t* x, const float* pre_in, const flo
                                float sk_eps, float* pre_out, float* post_out, float* comb_out,
                                uint16_t* layer_input, float* logits_out, cudaStream_t stream,
                                int max_clusters, bool overlap, const uint16_t* y, const float* comb_prev,
-                               const float* post_prev, uint16_t* x_new);
+                               const float* post_prev, uint16_t* x_new, bool nondelayed);
 int pre_cluster_tile_tokens(int64_t T, int max_clusters);
 int pre_cluster_max_tile();
 int pre_cluster_ctas();
@@ -111,6 +111,9 @@ bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
     return a0 < b0 + bn && b0 < a0 + an;
 }
 
+// mhc_pre from 256 tokens: the first tensor-core pass's pre-mix [T][4]
+size_t nondelayed_scratch_bytes(int64_t T) { return ((size_t)T * 16 + 255) / 256 * 256; }
+
 mhc_status check_pre_shape(int64_t T, int n, int C, int iters) {
     if (T < 0 || n < 1 || C < 1 || iters < 1) return MHC_ERR_INVALID_ARGUMENT;
     if (n != 4 || C % 8 != 0 || C > kMaxC) return MHC_ERR_UNSUPPORTED;
@@ -173,7 +176,8 @@ size_t mhc_pre_workspace_bytes(int64_t T, int n, int C) {
     int dev = current_device();
     if (dev < 0) return 0;
     int tcc = tc_clusters(dev);
-    return tcc > 0 ? mhc::pre_tc_workspace_bytes(T, C, tcc) : 0;
+    // fn planes, then (mhc_pre only) the first pass's pre-mix
+    return tcc > 0 ? mhc::pre_tc_workspace_bytes(T, C, tcc) + nondelayed_scratch_bytes(T) : 0;
 }
 
 }  // extern "C"
@@ -190,12 +194,12 @@ mhc_status pre_entry(const uint16_t* x, const float* pre_in, const float* fn, co
                      int sinkhorn_iters, float rms_eps, float norm_eps, float sinkhorn_eps, float* pre_out,
                      float* post_out, float* comb_out, uint16_t* layer_input, float* logits_out, void* workspace,
                      size_t workspace_bytes, void* stream, bool fused, const uint16_t* y, const float* comb_prev,
-                     const float* post_prev, uint16_t* x_new) {
+                     const float* post_prev, uint16_t* x_new, bool nondelayed = false) {
     mhc_status st = check_pre_shape(T, n, C, sinkhorn_iters);
     if (st != MHC_OK) return st;
     if (!(rms_eps >= 0.f) || !(norm_eps >= 0.f) || !(sinkhorn_eps >= 0.f)) return MHC_ERR_INVALID_ARGUMENT;
     if (T == 0) return MHC_OK;
-    const void* req[] = {x, pre_in, fn, bias, alpha, pre_out, post_out, comb_out, layer_input};
+    const void* req[] = {x, nondelayed ? fn : pre_in, fn, bias, alpha, pre_out, post_out, comb_out, layer_input};
     for (const void* p : req)
         if (!p || !aligned16(p)) return MHC_ERR_INVALID_ARGUMENT;
     if (fused) {
@@ -211,7 +215,8 @@ mhc_status pre_entry(const uint16_t* x, const float* pre_in, const float* fn, co
     const size_t fnb = (size_t)M * n * C * 4, bb = (size_t)M * 4, ab = 12, nwb = (size_t)C * 2;
     // Exact aliases allowed when fused: x_new == x, comb_out == comb_prev,
     // post_out == post_prev (each is read, for a token, before it is written).
-    const Span ins[] = {{x, xb}, {pre_in, pb}, {fn, fnb}, {bias, bb}, {alpha, ab}, {norm_weight, nwb},
+    const Span ins[] = {{x, xb}, {nondelayed ? nullptr : pre_in, pb}, {fn, fnb}, {bias, bb}, {alpha, ab},
+                        {norm_weight, nwb},
                         {fused ? y : nullptr, lib}, {fused ? comb_prev : nullptr, cb},
                         {fused ? post_prev : nullptr, pb}};
     const Span outs[] = {{pre_out, pb}, {post_out, pb}, {comb_out, cb}, {layer_input, lib}, {logits_out, lob},
@@ -233,9 +238,24 @@ mhc_status pre_entry(const uint16_t* x, const float* pre_in, const float* fn, co
     if (use_tc(T, C)) {
         int tcc = tc_clusters(dev);
         if (tcc > 0) {
-            const size_t need = mhc::pre_tc_workspace_bytes(T, C, tcc);
+            const size_t planes = mhc::pre_tc_workspace_bytes(T, C, tcc);
+            const size_t need = planes + (nondelayed ? nondelayed_scratch_bytes(T) : 0);
             if (workspace_bytes < need || (need && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))))
                 return MHC_ERR_INVALID_ARGUMENT;
+            if (nondelayed) {
+                // pass 1: the gates (its collapse, with an arbitrary pre-mix,
+                // is overwritten); pass 2: the delayed block with pre_in = the
+                // pre-mix of pass 1, which reproduces the gates bit for bit
+                float* pre1 = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + planes);
+                cudaError_t e = mhc::launch_pre_tc(x, pre1, fn, bias, alpha, norm_weight, T, C, sinkhorn_iters,
+                                                   rms_eps, norm_eps, sinkhorn_eps, pre1, post_out, comb_out,
+                                                   layer_input, logits_out, workspace, s, tcc);
+                if (e == cudaSuccess)
+                    e = mhc::launch_pre_tc(x, pre1, fn, bias, alpha, norm_weight, T, C, sinkhorn_iters, rms_eps,
+                                           norm_eps, sinkhorn_eps, pre_out, post_out, comb_out, layer_input,
+                                           logits_out, workspace, s, tcc);
+                return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA;
+            }
             const uint16_t* xin = x;
             if (fused) {   // large T: the post kernel, then the tensor-core pre on x_new
                 int sms = num_sms(dev);
@@ -256,7 +276,7 @@ mhc_status pre_entry(const uint16_t* x, const float* pre_in, const float* fn, co
                                             norm_eps, sinkhorn_eps, pre_out, post_out, comb_out, layer_input,
                                             logits_out, s, mc, overlap, fused ? y : nullptr,
                                             fused ? comb_prev : nullptr, fused ? post_prev : nullptr,
-                                            fused ? x_new : nullptr);
+                                            fused ? x_new : nullptr, nondelayed);
     return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA;
 }
 
@@ -273,6 +293,15 @@ mhc_status mhc_pre_delayed(const uint16_t* x, const float* pre_in, const float* 
     return pre_entry(x, pre_in, fn, bias, alpha, norm_weight, T, n, C, sinkhorn_iters, rms_eps, norm_eps,
                      sinkhorn_eps, pre_out, post_out, comb_out, layer_input, logits_out, workspace, workspace_bytes,
                      stream, false, nullptr, nullptr, nullptr, nullptr);
+}
+
+mhc_status mhc_pre(const uint16_t* x, const float* fn, const float* bias, const float* alpha,
+                   const uint16_t* norm_weight, int64_t T, int n, int C, int sinkhorn_iters, float rms_eps,
+                   float norm_eps, float sinkhorn_eps, float* pre_out, float* post_out, float* comb_out,
+                   uint16_t* layer_input, float* logits_out, void* workspace, size_t workspace_bytes, void* stream) {
+    return pre_entry(x, nullptr, fn, bias, alpha, norm_weight, T, n, C, sinkhorn_iters, rms_eps, norm_eps,
+                     sinkhorn_eps, pre_out, post_out, comb_out, layer_input, logits_out, workspace, workspace_bytes,
+                     stream, false, nullptr, nullptr, nullptr, nullptr, true);
 }
 
 mhc_status mhc_post_pre_delayed(const uint16_t* x, const uint16_t* y, const float* comb, const float* post,

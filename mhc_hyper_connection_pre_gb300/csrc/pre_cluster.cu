@@ -36,7 +36,14 @@
 //   6. meanwhile warps 2..11 form each token's fold scale from the 16 sum h^2
 //      partials (the same sum, in rank order, in every CTA: the same bits),
 //      fold h and store layer_input.
-// Fused with the previous seam's post (y != nullptr): before step 2 every
+// Non-delayed (MODE kNonDelayed, the V4 form without an incoming pre-mix):
+// the collapse needs this tile's own pre, so step 2 only sums x^2; the
+// finalising CTA sends each token's pre to all 16 CTAs as soon as it has the
+// logits, then every CTA collapses with it and exchanges sum h^2 for the
+// fold, while the finaliser goes on with the comb.  The x tile is read by
+// that collapse, so the next tile's x is fetched only after it.
+//
+// Fused with the previous seam's post (MODE kFusedPost): before step 2 every
 // thread turns its share of the tile's x slice into x_new = post(x, y, comb,
 // post) with the post kernel's arithmetic (the same bits), writes it out and
 // leaves it in shared memory, where the pre block reads it in place of x.
@@ -60,7 +67,8 @@ constexpr int kSlots = kMaxTile / kCtas;   // tokens each CTA finalises per tile
 constexpr int kRowWarp0 = kSlots;          // warps kRowWarp0.. collapse and fold
 constexpr int kRowWarps = kWarps - kRowWarp0;
 constexpr int kSqBytes = kCtas * 2 * 4;            // per token: 16 x (sum x^2, sum h^2)
-constexpr int kNumBars = 2 + 2 * kSlots;           // sq_full[parity], dots_full[parity][slot]
+constexpr int kNumBars = 6 + 2 * kSlots;           // sq_full[p], dots_full[p][slot], pre_full[p], sh_full[p]
+enum Mode { kDelayed = 0, kFusedPost = 1, kNonDelayed = 2 };
 constexpr int kDotsBytes = kCtas * kLogits * 4;    // per token: 16 x 24 partial dots
 
 struct Args {
@@ -92,14 +100,14 @@ struct Args {
 
 // Shared-memory carve-up (bytes), in this order.
 struct Layout {
-    int xs, hs, red, pin, nw, sq, dots, ys, gates, bars, abort_flag, total;
+    int xs, hs, red, pin, nw, sq, dots, ys, gates, prex, shin, bars, abort_flag, total;
 };
 __host__ __device__ inline int dec_xstride(int lcmax) {
     // 64 bytes per group (4 streams x 8 bf16); rows an odd multiple of 64
     // bytes apart so that the MMA's row loads of 8 tokens hit distinct banks
     return ((64 * lcmax + 127) / 128) * 128 + 64;
 }
-__host__ __device__ inline Layout dec_layout(int lcmax, bool fused) {
+__host__ __device__ inline Layout dec_layout(int lcmax, int mode) {
     Layout L;
     int o = 0;
     L.xs = o;    o += kMaxTile * dec_xstride(lcmax);
@@ -113,7 +121,9 @@ __host__ __device__ inline Layout dec_layout(int lcmax, bool fused) {
     // post step: the y slice with h, the gates with the warps' partials
     L.ys = L.hs;     // kMaxTile x 8 lcmax bf16 <= the h buffer
     L.gates = L.red; // kMaxTile x 20 fp32 <= the partials buffer
-    (void)fused;
+    // non-delayed: this tile's pre per token, sum h^2 partials [parity]
+    L.prex = o;  o += mode == kNonDelayed ? 2 * kMaxTile * 16 : 0;
+    L.shin = o;  o += mode == kNonDelayed ? 2 * kMaxTile * kCtas * 4 : 0;
     L.bars = o;  o += kNumBars * 8;
     L.abort_flag = o; o += 16;
     L.total = o;
@@ -142,7 +152,7 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-template <int JMAX, bool FUSED>
+template <int JMAX, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
     const int rank = (int)cluster_ctarank();
     const int64_t cid = cluster_id_x();
@@ -155,11 +165,12 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
     const int ncols = 8 * lc;
     const int c0 = 8 * ch0;
     const bool fold = a.norm_w != nullptr;
-    constexpr bool fused = FUSED;   // the previous seam's post runs first
+    constexpr bool fused = MODE == kFusedPost;     // the previous seam's post runs first
+    constexpr bool nondel = MODE == kNonDelayed;   // collapse with this tile's own pre
     const int TT = a.tile;
 
     extern __shared__ __align__(128) unsigned char smem[];
-    const Layout L = dec_layout(a.lcmax, FUSED);
+    const Layout L = dec_layout(a.lcmax, MODE);
     unsigned char* xs = smem + L.xs;
     float* hs = reinterpret_cast<float*>(smem + L.hs);
     float* red = reinterpret_cast<float*>(smem + L.red);
@@ -172,6 +183,10 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
     uint64_t* sq_full = bars;              // [parity]
     uint64_t* dots_full = bars + 2;        // [parity][slot]
+    uint64_t* pre_full = bars + 2 + 2 * kSlots;   // [parity] (non-delayed)
+    uint64_t* sh_full = pre_full + 2;             // [parity] (non-delayed)
+    float* prex = reinterpret_cast<float*>(smem + L.prex);   // [parity][token][4]
+    float* shin = reinterpret_cast<float*>(smem + L.shin);   // [parity][token][src]
     volatile int* abort = reinterpret_cast<volatile int*>(smem + L.abort_flag);
     const int hstride = 8 * a.lcmax;       // floats per token row of h
 
@@ -195,6 +210,10 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
         mbar_arrive_expect_tx(&sq_full[parity], kSqBytes * n);
         for (int s = 0; s < kSlots; ++s)
             if (kCtas * s + rank < n) mbar_arrive_expect_tx(&dots_full[parity * kSlots + s], kDotsBytes);
+        if (nondel) {
+            mbar_arrive_expect_tx(&pre_full[parity], 16 * n);          // every token's pre, once
+            mbar_arrive_expect_tx(&sh_full[parity], kCtas * 4 * n);    // 16 x sum h^2 per token
+        }
     };
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i) mbar_init(&bars[i], 1);
@@ -243,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
             const uint16_t* src = a.x + ((t0 + tt) * 4 + i) * (int64_t)C + c0 + 8 * cc;
             cp_async16(smem_u32(xs + tt * a.xstride + (i * ncols + 8 * cc) * 2), src);
         }
-        if (tid < n) cp_async16(smem_u32(pin + 4 * tid), a.pre_in + (t0 + tid) * 4);
+        if (!nondel && tid < n) cp_async16(smem_u32(pin + 4 * tid), a.pre_in + (t0 + tid) * 4);
     };
     // y slice and gates of a tile (fused post).  Their buffers double as h and
     // the partials later in a tile, so a later tile's are loaded at its start.
@@ -337,7 +356,31 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
         }
 
         // ---- 2. collapse (warps 2..11), one token per warp at a time
-        if (warp >= kRowWarp0) {
+        //         (non-delayed: only sum x^2 here, the collapse follows the
+        //         pre from the finaliser)
+        if (nondel && warp >= kRowWarp0) {
+            for (int tt = warp - kRowWarp0; tt < nv; tt += kRowWarps) {
+                float sx = 0.f;
+                for (int cc = lane; cc < lc; cc += 32) {
+                    float xv[4][8];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        unpack8(*reinterpret_cast<const uint4*>(xs + tt * a.xstride + (i * ncols + 8 * cc) * 2), xv[i]);
+                    // the delayed block's order of accumulation, so that both
+                    // blocks give the same RMS scale and gates bit for bit
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) sx = fmaf(xv[i][e], xv[i][e], sx);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) sx += __shfl_xor_sync(0xffffffffu, sx, o);
+                if (lane < kCtas)
+                    st_async_v2(mapa(smem_u32(inbox_sq + ((par * kMaxTile + tt) * kCtas + rank) * 2), lane), sx, 0.f,
+                                mapa(smem_u32(&sq_full[par]), lane));
+            }
+        }
+        if (!nondel && warp >= kRowWarp0) {
             for (int tt = warp - kRowWarp0; tt < nv; tt += kRowWarps) {
                 const float p0 = pin[4 * tt], p1 = pin[4 * tt + 1], p2 = pin[4 * tt + 2], p3 = pin[4 * tt + 3];
                 float sx = 0.f, sh = 0.f;
@@ -418,9 +461,9 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
             }
         }
         if (fused && tid < 4 * nv) bulk_wait_read_all();   // x_new copies done reading the x tile
-        __syncthreads();  // partials complete; the x tile and pre_in are free
+        __syncthreads();  // partials complete; the x tile (delayed: also pre_in) is free
 
-        if (!last) {
+        if (!last && !nondel) {
             issue_tile(tile + ncl, nv_next);
             cp_async_commit();
         }
@@ -472,8 +515,16 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
                         if (a.logits_out) a.logits_out[t * kLogits + lane] = l;
                     }
                     // gates: lanes 0..3 pre, 4..7 post
-                    if (lane < 4) a.pre_out[t * 4 + lane] = __fdividef(1.0f, 1.0f + expf(-l));
-                    else if (lane < 8) a.post_out[t * 4 + lane - 4] = __fdividef(2.0f, 1.0f + expf(-l));
+                    const float gate = lane < 4 ? __fdividef(1.0f, 1.0f + expf(-l)) : __fdividef(2.0f, 1.0f + expf(-l));
+                    if (lane < 4) a.pre_out[t * 4 + lane] = gate;
+                    else if (lane < 8) a.post_out[t * 4 + lane - 4] = gate;
+                    if (nondel) {   // this token's pre to every CTA, for their collapse
+                        const float q0 = __shfl_sync(0xffffffffu, gate, 0), q1 = __shfl_sync(0xffffffffu, gate, 1);
+                        const float q2 = __shfl_sync(0xffffffffu, gate, 2), q3 = __shfl_sync(0xffffffffu, gate, 3);
+                        if (lane < kCtas)
+                            st_async_v4(mapa(smem_u32(prex + (par * kMaxTile + tok) * 4), lane), q0, q1, q2, q3,
+                                        mapa(smem_u32(&pre_full[par]), lane));
+                    }
                     // comb: lanes 8..23 hold the 4x4 logits row-major; row softmax
                     // across each group of 4 lanes, plus eps
                     float mx = fmaxf(l, __shfl_xor_sync(0xffffffffu, l, 1));
@@ -494,16 +545,66 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
                 }
             }
         }
+        // ---- 5b. non-delayed: collapse with the tile's own pre, then send
+        //          sum h^2 to every CTA (warps 2..11)
+        if (nondel && warp >= kRowWarp0) {
+            const bool ok = mbar_wait<true>(&pre_full[par], (round >> 1) & 1, abort);
+            for (int tt = warp - kRowWarp0; ok && tt < nv; tt += kRowWarps) {
+                const float* pp = prex + (par * kMaxTile + tt) * 4;
+                const float p0 = pp[0], p1 = pp[1], p2 = pp[2], p3 = pp[3];
+                float sh = 0.f;
+                for (int cc = lane; cc < lc; cc += 32) {
+                    float h[8];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        float xv[8];
+                        unpack8(*reinterpret_cast<const uint4*>(xs + tt * a.xstride + (i * ncols + 8 * cc) * 2), xv);
+                        const float pi = i == 0 ? p0 : (i == 1 ? p1 : (i == 2 ? p2 : p3));
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            h[e] = i == 0 ? __fmul_rn(pi, xv[e]) : __fadd_rn(h[e], __fmul_rn(pi, xv[e]));
+                    }
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) sh = fmaf(h[e], h[e], sh);
+                    if (fold) {
+                        float4* hp = reinterpret_cast<float4*>(hs + tt * hstride + 8 * cc);
+                        hp[0] = make_float4(h[0], h[1], h[2], h[3]);
+                        hp[1] = make_float4(h[4], h[5], h[6], h[7]);
+                    } else {
+                        st_stream(reinterpret_cast<uint4*>(a.layer_input + (t0 + tt) * C + c0 + 8 * cc), pack8(h));
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) sh += __shfl_xor_sync(0xffffffffu, sh, o);
+                if (lane < kCtas)
+                    st_async_f32(mapa(smem_u32(shin + (par * kMaxTile + tt) * kCtas + rank), lane), sh,
+                                 mapa(smem_u32(&sh_full[par]), lane));
+            }
+        }
+        if (nondel && !last) {   // the collapse above was the x tile's last reader
+            __syncthreads();
+            issue_tile(tile + ncl, nv_next);
+            cp_async_commit();
+        }
+
         // ---- 6. fold scales from the 16 sum h^2 partials; fold and store
         //         (warps 2..11)
         if (warp >= kRowWarp0) {
-            const bool ok = mbar_wait<true>(&sq_full[par], (round >> 1) & 1, abort);
+            const bool ok = nondel ? mbar_wait<true>(&sh_full[par], (round >> 1) & 1, abort)
+                                   : mbar_wait<true>(&sq_full[par], (round >> 1) & 1, abort);
+            if (nondel) mbar_wait<true>(&sq_full[par], (round >> 1) & 1, abort);   // every incoming byte seen
             if (fold && ok) {
                 for (int tt = warp - kRowWarp0; tt < nv; tt += kRowWarps) {
-                    const float* sq = inbox_sq + (par * kMaxTile + tt) * kCtas * 2;
                     float sh = 0.f;
+                    if (nondel) {
+                        const float* sp = shin + (par * kMaxTile + tt) * kCtas;
 #pragma unroll
-                    for (int s2 = 0; s2 < kCtas; ++s2) sh += sq[2 * s2 + 1];
+                        for (int s2 = 0; s2 < kCtas; ++s2) sh += sp[s2];
+                    } else {
+                        const float* sq = inbox_sq + (par * kMaxTile + tt) * kCtas * 2;
+#pragma unroll
+                        for (int s2 = 0; s2 < kCtas; ++s2) sh += sq[2 * s2 + 1];
+                    }
                     const float s = 1.0f / sqrtf(sh / (float)C + a.norm_eps);
                     for (int cc = lane; cc < lc; cc += 32) {
                         const float4* hp = reinterpret_cast<const float4*>(hs + tt * hstride + 8 * cc);
@@ -574,9 +675,9 @@ int pre_cluster_prepare(int C) {
     const int jmax = dec::jmax_of(C);
     int n_min = 0;
     cudaError_t e = cudaSuccess;
-    auto setup = [&](auto kern, bool fused) {
-        const size_t smem = (size_t)dec::dec_layout(dec::lcmax_of(C), fused).total;
-        const size_t smem_cap = (size_t)dec::dec_layout(dec::kWarps * jmax, fused).total;
+    auto setup = [&](auto kern, int mode) {
+        const size_t smem = (size_t)dec::dec_layout(dec::lcmax_of(C), mode).total;
+        const size_t smem_cap = (size_t)dec::dec_layout(dec::kWarps * jmax, mode).total;
         cudaLaunchAttribute attr[1];
         cudaLaunchConfig_t cfg = dec::cluster_config(attr, smem, nullptr);
         int n = 0;
@@ -587,9 +688,21 @@ int pre_cluster_prepare(int C) {
         n_min = (n_min == 0 || n < n_min) ? n : n_min;
     };
     switch (jmax) {
-        case 1: setup(dec::pre_decode_kernel<1, false>, false); setup(dec::pre_decode_kernel<1, true>, true); break;
-        case 2: setup(dec::pre_decode_kernel<2, false>, false); setup(dec::pre_decode_kernel<2, true>, true); break;
-        case 4: setup(dec::pre_decode_kernel<4, false>, false); setup(dec::pre_decode_kernel<4, true>, true); break;
+        case 1:
+            setup(dec::pre_decode_kernel<1, dec::kDelayed>, dec::kDelayed);
+            setup(dec::pre_decode_kernel<1, dec::kFusedPost>, dec::kFusedPost);
+            setup(dec::pre_decode_kernel<1, dec::kNonDelayed>, dec::kNonDelayed);
+            break;
+        case 2:
+            setup(dec::pre_decode_kernel<2, dec::kDelayed>, dec::kDelayed);
+            setup(dec::pre_decode_kernel<2, dec::kFusedPost>, dec::kFusedPost);
+            setup(dec::pre_decode_kernel<2, dec::kNonDelayed>, dec::kNonDelayed);
+            break;
+        case 4:
+            setup(dec::pre_decode_kernel<4, dec::kDelayed>, dec::kDelayed);
+            setup(dec::pre_decode_kernel<4, dec::kFusedPost>, dec::kFusedPost);
+            setup(dec::pre_decode_kernel<4, dec::kNonDelayed>, dec::kNonDelayed);
+            break;
         default: return 0;
     }
     return e == cudaSuccess ? n_min : 0;
@@ -601,7 +714,7 @@ cudaError_t launch_pre_cluster(const uint16_t* x, const float* pre_in, const flo
                                float sk_eps, float* pre_out, float* post_out, float* comb_out,
                                uint16_t* layer_input, float* logits_out, cudaStream_t stream,
                                int max_clusters, bool overlap, const uint16_t* y, const float* comb_prev,
-                               const float* post_prev, uint16_t* x_new) {
+                               const float* post_prev, uint16_t* x_new, bool nondelayed) {
     dec::Args a;
     a.y = y; a.comb_prev = comb_prev; a.post_prev = post_prev; a.x_new = x_new;
     a.x = x; a.pre_in = pre_in; a.fn = fn; a.bias = bias; a.alpha = alpha; a.norm_w = norm_w;
@@ -614,8 +727,8 @@ cudaError_t launch_pre_cluster(const uint16_t* x, const float* pre_in, const flo
     a.lcmax = dec::lcmax_of(C);
     a.xstride = dec::dec_xstride(a.lcmax);
     cudaLaunchAttribute attr[2];
-    const bool fused = y != nullptr;
-    cudaLaunchConfig_t cfg = dec::cluster_config(attr, (size_t)dec::dec_layout(a.lcmax, fused).total, stream);
+    const int mode = nondelayed ? dec::kNonDelayed : (y != nullptr ? dec::kFusedPost : dec::kDelayed);
+    cudaLaunchConfig_t cfg = dec::cluster_config(attr, (size_t)dec::dec_layout(a.lcmax, mode).total, stream);
     if (overlap) {
         attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[1].val.programmaticStreamSerializationAllowed = 1;
@@ -623,13 +736,16 @@ cudaError_t launch_pre_cluster(const uint16_t* x, const float* pre_in, const flo
     }
     const int64_t nclusters = a.ntiles < max_clusters ? a.ntiles : max_clusters;
     cfg.gridDim = dim3((unsigned)(nclusters * dec::kCtas), 1, 1);
-    switch (dec::jmax_of(C) * 2 + (fused ? 1 : 0)) {
-        case 2: return cudaLaunchKernelEx(&cfg, dec::pre_decode_kernel<1, false>, a);
-        case 3: return cudaLaunchKernelEx(&cfg, dec::pre_decode_kernel<1, true>, a);
-        case 4: return cudaLaunchKernelEx(&cfg, dec::pre_decode_kernel<2, false>, a);
-        case 5: return cudaLaunchKernelEx(&cfg, dec::pre_decode_kernel<2, true>, a);
-        case 8: return cudaLaunchKernelEx(&cfg, dec::pre_decode_kernel<4, false>, a);
-        case 9: return cudaLaunchKernelEx(&cfg, dec::pre_decode_kernel<4, true>, a);
+    switch (dec::jmax_of(C) * 3 + mode) {
+        case 3: return cudaLaunchKernelEx(&cfg, dec::pre_decode_kernel<1, dec::kDelayed>, a);
+        case 4: return cudaLaunchKernelEx(&cfg, dec::pre_decode_kernel<1, dec::kFusedPost>, a);
+        case 5: return cudaLaunchKernelEx(&cfg, dec::pre_decode_kernel<1, dec::kNonDelayed>, a);
+        case 6: return cudaLaunchKernelEx(&cfg, dec::pre_decode_kernel<2, dec::kDelayed>, a);
+        case 7: return cudaLaunchKernelEx(&cfg, dec::pre_decode_kernel<2, dec::kFusedPost>, a);
+        case 8: return cudaLaunchKernelEx(&cfg, dec::pre_decode_kernel<2, dec::kNonDelayed>, a);
+        case 12: return cudaLaunchKernelEx(&cfg, dec::pre_decode_kernel<4, dec::kDelayed>, a);
+        case 13: return cudaLaunchKernelEx(&cfg, dec::pre_decode_kernel<4, dec::kFusedPost>, a);
+        case 14: return cudaLaunchKernelEx(&cfg, dec::pre_decode_kernel<4, dec::kNonDelayed>, a);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -144,6 +144,31 @@ def pre_delayed(x_bits, pre_in, fn, bias, alpha, norm_w_bits=None, *,
     return out
 
 
+def pre_nondelayed(x_bits, fn, bias, alpha, norm_w_bits=None, *, pre_mix=None, iters=SINKHORN_ITERS,
+                   rms_eps=RMS_EPS, norm_eps=NORM_EPS, sinkhorn_eps=SINKHORN_EPS, nthreads=1) -> dict:
+    """Non-delayed mHC pre block (the #56503 page, "Why V4.1 cannot just reuse
+    MHCPreOp": the V4 block collapses a sublayer's input with the pre-mix it
+    computes itself, where V4.1 uses the previous seam's): the gates of
+    ``pre_delayed`` (which do not depend on the incoming pre-mix) and the
+    collapse with this block's own pre-mix rounded to fp32 -- the kernel's
+    stored values.  ``pre_mix`` (float32 [T, n]) replaces that rounding with
+    given values (a kernel's own pre, for a layered bit-exact check of the
+    collapse); otherwise the fp64 pre is rounded to nearest fp32 here.
+
+    A composition of ``pre_delayed`` calls, so it rests on that function's
+    pins; ``tests/test_oracle_pins.py`` adds the invariants specific to it."""
+    x_bits = _c(x_bits, np.uint16)
+    T, n, C = x_bits.shape
+    gates = pre_delayed(x_bits, np.zeros((T, n), np.float32), fn, bias, alpha, norm_w_bits, iters=iters,
+                        rms_eps=rms_eps, norm_eps=norm_eps, sinkhorn_eps=sinkhorn_eps, nthreads=nthreads)
+    mix = gates["pre"].astype(np.float32) if pre_mix is None else _c(pre_mix, np.float32).reshape(T, n)
+    coll = pre_delayed(x_bits, mix, fn, bias, alpha, norm_w_bits, iters=iters, rms_eps=rms_eps,
+                       norm_eps=norm_eps, sinkhorn_eps=sinkhorn_eps, nthreads=nthreads)
+    out = dict(gates)
+    out["h32"], out["layer_input"], out["pre_mix"] = coll["h32"], coll["layer_input"], mix
+    return out
+
+
 def gates_from_logits(logits, n=4, *, iters=SINKHORN_ITERS,
                       sinkhorn_eps=SINKHORN_EPS) -> dict:
     """pre = sigmoid(l[:n]), post = 2 sigmoid(l[n:2n]), comb = Sinkhorn of

@@ -461,3 +461,44 @@ def test_threads_do_not_change_results():
     o1, o4 = _run(a, nthreads=1), _run(a, nthreads=4)
     for k in o1:
         assert np.array_equal(o1[k], o4[k]), k
+
+
+# ------------------------------------------------------------ non-delayed ---
+
+@pytest.mark.parametrize("k", [0, 2])
+def test_nondelayed_dominant_pre_selects_its_stream(k):
+    """With pre logits driven to +40 for stream k and -40 for the others, the
+    block's own pre-mix is (1, 0, 0, 0) up to 4e-18, so the non-delayed
+    collapse (no fold) returns stream k's bits exactly -- the collapse must
+    use this block's pre, in stream order."""
+    T, C = 3, 16
+    rng = np.random.default_rng(5 + k)
+    x = rng.standard_normal((T, 4, C)).astype(np.float32)
+    xb = bf16_bits(torch.from_numpy(x).to(torch.bfloat16))
+    fn = (0.02 * rng.standard_normal((24, 4 * C))).astype(np.float32)
+    bias = np.zeros(24, np.float32)
+    bias[:4] = -40.0
+    bias[k] = 40.0
+    o = oracle.pre_nondelayed(xb, fn, bias, np.ones(3, np.float32))
+    assert np.all(o["pre_mix"][:, k] == 1.0)
+    assert np.array_equal(o["layer_input"], xb[:, k, :])
+    # the delayed block with another incoming pre-mix does not (control)
+    d = oracle.pre_delayed(xb, np.full((T, 4), 0.25, np.float32), fn, bias, np.ones(3, np.float32))
+    assert not np.array_equal(d["layer_input"], xb[:, k, :])
+
+
+def test_nondelayed_identical_streams_closed_form():
+    """All four streams equal to x0: h = (sum_i pre_i) x0 up to the rounding
+    of four products and three adds, with pre this block's own pre-mix."""
+    T, C = 4, 32
+    rng = np.random.default_rng(11)
+    x0 = rng.standard_normal((T, 1, C)).astype(np.float32)
+    xb = bf16_bits(torch.from_numpy(np.repeat(x0, 4, axis=1)).to(torch.bfloat16))
+    fn = (0.05 * rng.standard_normal((24, 4 * C))).astype(np.float32)
+    bias = (0.3 * rng.standard_normal(24)).astype(np.float32)
+    o = oracle.pre_nondelayed(xb, fn, bias, np.ones(3, np.float32))
+    xv = oracle.bf16_to_f64(xb[:, 0, :])
+    s = o["pre_mix"].astype(np.float64).sum(1, keepdims=True)
+    want = s * xv
+    bound = 4 * 2.0 ** -24 * (np.abs(o["pre_mix"]).astype(np.float64).sum(1, keepdims=True) * np.abs(xv)) + 1e-30
+    assert np.all(np.abs(o["h32"].astype(np.float64) - want) <= bound)

@@ -295,6 +295,69 @@ def test_fused_seam_is_one_launch_in_a_graph():
     g.close()
 
 
+@pytest.mark.parametrize("T,C,fold", [(1, 5120, True), (7, 5120, False), (33, 5120, True), (128, 5120, False),
+                                      (100, 1000, True), (300, 1000, False), (300, 5120, True), (1000, 5120, False),
+                                      (5, 8, True)])
+def test_nondelayed_pre_equals_delayed_with_its_own_pre(T, C, fold):
+    """mhc_pre's gates are those of mhc_pre_delayed (they do not depend on the
+    incoming pre-mix), and its layer input is bit for bit the delayed call's
+    with pre_in set to the pre it returned: the cluster kernel below 256
+    tokens, the two-pass tensor-core path above, multi-round tiles at C=1000."""
+    d = seam_inputs(T, C=C, seed=1700 + T + C, fold=fold)
+    gd = _to_dev(d)
+    got = mhc.pre(gd["x"], gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"], return_logits=True)
+    torch.cuda.synchronize()
+    assert mhc.device_status() == 0
+    ref = mhc.pre_delayed(gd["x"], got["pre"].clone(), gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"],
+                          return_logits=True)
+    torch.cuda.synchronize()
+    assert mhc.device_status() == 0
+    for k in ("pre", "post", "comb", "layer_input", "logits"):
+        assert torch.equal(got[k], ref[k]), k
+
+
+@pytest.mark.parametrize("T,C,fold", [(1, 5120, True), (33, 5120, False), (300, 5120, True), (17, 2056, False)])
+def test_nondelayed_pre_against_the_oracle(T, C, fold):
+    """Gates within the gate tolerance of the oracle's; the collapse (no
+    fold: bit-exact) and the fold (1 ulp) against the oracle's non-delayed
+    block fed the kernel's own fp32 pre, so that a rounding of pre near a
+    tie cannot move the comparison."""
+    d = seam_inputs(T, C=C, seed=1800 + T + C, fold=fold)
+    gd = _to_dev(d)
+    got = mhc.pre(gd["x"], gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"], return_logits=True)
+    torch.cuda.synchronize()
+    assert mhc.device_status() == 0
+    g = {k: v.cpu() for k, v in got.items()}
+    xb = bf16_bits(d["x"])
+    nw = None if d["norm_w"] is None else bf16_bits(d["norm_w"])
+    o = oracle.pre_nondelayed(xb, d["fn"].numpy(), d["bias"].numpy(), d["alpha"].numpy(), nw,
+                              pre_mix=g["pre"].numpy(), nthreads=NTHREADS)
+    _check_pre(g, o, xb, d, fold)
+    # the pre-mix the kernel used is its own, not a stale or zero one
+    o_own = oracle.pre_nondelayed(xb, d["fn"].numpy(), d["bias"].numpy(), d["alpha"].numpy(), nw,
+                                  nthreads=NTHREADS)
+    assert_gates(g["pre"].numpy(), o_own["pre"], "pre")
+
+
+def test_nondelayed_pre_is_one_launch_in_a_graph_below_256_tokens():
+    d = seam_inputs(16, C=5120, seed=1900, fold=True)
+    gd = _to_dev(d)
+    out = {"pre": torch.empty(16, 4, device="cuda"), "post": torch.empty(16, 4, device="cuda"),
+           "comb": torch.empty(16, 4, 4, device="cuda"),
+           "layer_input": torch.empty(16, 5120, dtype=torch.bfloat16, device="cuda")}
+    ref = mhc.pre(gd["x"], gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"])
+    s = torch.cuda.Stream()
+    g = SeamGraph(lambda st: mhc.pre(gd["x"], gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"], out=out,
+                                     stream=st), s)
+    assert g.kernel_nodes == 1, g.kernel_nodes
+    g.replay(5)
+    s.synchronize()
+    assert mhc.device_status() == 0
+    for k in ("pre", "post", "comb", "layer_input"):
+        assert torch.equal(out[k], ref[k]), k
+    g.close()
+
+
 def test_graph_seam_is_two_launches_and_replays_exactly():
     """One seam (pre + post) captured in a CUDA graph holds exactly 2 kernel
     nodes; 200 replays give the eager result bit for bit."""
