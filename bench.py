@@ -43,6 +43,9 @@ PRE_BYTES_PER_TOKEN = 40960 + 10240 + 16 + 16 + 16 + 64   # x, layer_input, pre_
 PRE_BYTES_FIXED = 24 * 20480 * 4 + 24 * 4 + 12 + 5120 * 2  # fn, bias, alpha, norm_weight
 POST_BYTES_PER_TOKEN = 40960 + 10240 + 64 + 16 + 40960     # x, y, comb, post, x_new
 PRE_FLOP_PER_TOKEN = 2 * 24 * 20480
+# model-entry broadcast seam: x is [T, C], read once for all four streams
+PRE_BCAST_BYTES_PER_TOKEN = 10240 + 10240 + 16 + 16 + 16 + 64   # x, layer_input, pre_in, pre, post, comb
+POST_BCAST_BYTES_PER_TOKEN = 10240 + 10240 + 64 + 16 + 40960    # x, y, comb, post, x_new
 
 
 def pre_bytes(T):
@@ -327,6 +330,43 @@ def run_ours(args, rank, world, local):
                "ms_per_step": round(e_ms / ek, 4)}
         del hx, hy, hp, ho, hpo, dx, dy, dp
 
+    # ---- the other prefill entry points at the same T (rank 0 only): the
+    # model-entry broadcast seam and the non-delayed pre
+    other_prefill = None
+    if rank == 0 and not args.skip_decode:
+        xe = x[:, 0, :].contiguous()
+        oe = {k: torch.empty_like(v) for k, v in outs[0].items()}
+        xne = torch.empty_like(x)
+
+        def timed(call, reps=20):
+            for _ in range(3):
+                call()
+            a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            a_ev.record(stream)
+            for _ in range(reps):
+                call()
+            b_ev.record(stream)
+            torch.cuda.synchronize(dev)
+            return a_ev.elapsed_time(b_ev) * 1e3 / reps
+
+        fixed = PRE_BYTES_FIXED
+        cases = {
+            "mhc_pre_delayed_broadcast": (lambda: mhc.pre_delayed_broadcast(
+                xe, pre_in[0], d["fn"], d["bias"], d["alpha"], d["norm_w"], out=oe),
+                T * PRE_BCAST_BYTES_PER_TOKEN + fixed),
+            "mhc_post_broadcast": (lambda: mhc.post_broadcast(xe, y, oe["comb"], oe["post"], out=xne),
+                                   T * POST_BCAST_BYTES_PER_TOKEN),
+            "mhc_pre": (lambda: mhc.pre(x, d["fn"], d["bias"], d["alpha"], d["norm_w"], out=oe), pre_bytes(T)),
+        }
+        other_prefill = {}
+        for name, (call, nbytes) in cases.items():
+            us = timed(call)
+            other_prefill[name] = {"us": round(us, 2), "bytes": nbytes, "gbs": round(nbytes / us / 1e3, 1),
+                                   "frac_of_hbm_peak": round(nbytes / us / 1e3 / hbm_peak, 4)}
+        assert mhc.device_status() == 0, "a bounded in-kernel wait timed out"
+        del xe, oe, xne
+
     # ---- decode sweep and the 80-seam chain (rank 0 only)
     decode = chain = None
     if rank == 0 and not args.skip_decode:
@@ -351,12 +391,21 @@ def run_ours(args, rank, world, local):
                 mhc.post_pre_delayed(dd["x"], dd["y"], o["comb"], o["post"], dd["pre_in"], dd["fn"], dd["bias"],
                                      dd["alpha"], dd["norm_w"], x_new=xn, out=o, stream=st)
 
+            xe = dd["x"][:, 0, :].contiguous()
+
+            def entry_call(st):
+                # the model-entry broadcast seam: pre and post on x [T, C]
+                mhc.pre_delayed_broadcast(xe, dd["pre_in"], dd["fn"], dd["bias"], dd["alpha"], dd["norm_w"],
+                                          out=o, stream=st)
+                mhc.post_broadcast(xe, dd["y"], o["comb"], o["post"], out=xn, stream=st)
+
             def nondelayed_call(st):
                 # the non-delayed block: collapse with its own pre-mix
                 mhc.pre(dd["x"], dd["fn"], dd["bias"], dd["alpha"], dd["norm_w"], out=o, stream=st)
 
             for name, one, ov in (("pre", pre_call, False), ("seam", seam_call, False),
                                   ("fused_seam", fused_call, False), ("pre_nondelayed", nondelayed_call, False),
+                                  ("entry_seam", entry_call, False),
                                   ("pre_overlap", pre_call, True), ("seam_overlap", seam_call, True),
                                   ("fused_seam_overlap", fused_call, True)):
                 mhc.set_launch_overlap(ov)
@@ -472,6 +521,7 @@ def run_ours(args, rank, world, local):
         "e2e": e2e,
         "gpu_launches": 2 * args.steps,
         "clocks": clk.summary(),
+        "other_prefill": other_prefill,
         "decode_graph": decode,
         "decode_chain_80": chain,
     }

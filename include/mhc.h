@@ -208,6 +208,52 @@ mhc_status mhc_post_pre_delayed(const uint16_t *x, const uint16_t *y, const floa
                                 float *comb_out, uint16_t *layer_input, float *logits_out,
                                 void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * Model-entry broadcast seam ([A] "Approach": the model-entry seam projects a
+ * narrower operand, x, and AITER declines it; [A] "Test Plan": the delayed
+ * block is tested with the carried pre-mix and with the model-entry one).
+ * At the model's entry the n residual streams are n copies of one hidden
+ * state x[t][c] (the embedding output), so these calls take x as [T, C] and
+ * read it as every stream:  x_b[t][i][c] = x[t][c], i < n.
+ *
+ * mhc_pre_delayed_broadcast -- mhc_pre_delayed on x_b, with pre_in the
+ *   model-entry pre-mix the caller supplies.  In closed form the projection
+ *   operand narrows to C columns (x_flat . fn[m] = x . sum_i fn[m][i*C ..],
+ *   r = 1/sqrt(sum_c x^2 / C + rms_eps)) and h = the fp32 sum of
+ *   pre_in[i] * x in stream order; the kernels compute it as the n-stream
+ *   block on x_b, so every output is bit-identical to mhc_pre_delayed on an
+ *   explicit copy x_b.  x is read once per token (C * 2 bytes instead of
+ *   n * C * 2).
+ * mhc_pre_broadcast -- mhc_pre (non-delayed) on x_b, the same way.
+ *  x  [T, C] bf16; all other arguments, the workspace, the plan and the
+ *     errors as mhc_pre_delayed / mhc_pre (x's byte range is T * C * 2).
+ */
+mhc_status mhc_pre_delayed_broadcast(const uint16_t *x, const float *pre_in, const float *fn,
+                                     const float *bias, const float *alpha,
+                                     const uint16_t *norm_weight, int64_t T, int n, int C,
+                                     int sinkhorn_iters, float rms_eps, float norm_eps,
+                                     float sinkhorn_eps, float *pre_out, float *post_out,
+                                     float *comb_out, uint16_t *layer_input, float *logits_out,
+                                     void *workspace, size_t workspace_bytes, void *stream);
+mhc_status mhc_pre_broadcast(const uint16_t *x, const float *fn, const float *bias,
+                             const float *alpha, const uint16_t *norm_weight, int64_t T, int n,
+                             int C, int sinkhorn_iters, float rms_eps, float norm_eps,
+                             float sinkhorn_eps, float *pre_out, float *post_out,
+                             float *comb_out, uint16_t *layer_input, float *logits_out,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * mhc_post_broadcast -- mhc_post on x_b: the entry seam's post, which turns
+ * the single hidden state into the n residual streams,
+ *   x_new[t][j][c] = bf16( sum_i comb[t][i][j] * x[t][c] + post[t][j] * y[t][c] ),
+ * with mhc_post's arithmetic (bit-identical to mhc_post on x_b).
+ *  x [T, C] bf16 (read once per column); y, comb, post, x_new, errors as
+ *  mhc_post; x_new [T, n, C] must not overlap x or any other input.
+ */
+mhc_status mhc_post_broadcast(const uint16_t *x, const uint16_t *y, const float *comb,
+                              const float *post, int64_t T, int n, int C, uint16_t *x_new,
+                              void *stream);
+
 /* Static description of the status code (never NULL). */
 const char *mhc_status_string(mhc_status status);
 

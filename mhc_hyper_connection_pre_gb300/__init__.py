@@ -68,6 +68,12 @@ def load_library():
         lib.mhc_post_pre_delayed.restype = I
         lib.mhc_pre.argtypes = [P, P, P, P, P, I64, I, I, I, F, F, F, P, P, P, P, P, P, ctypes.c_size_t, P]
         lib.mhc_pre.restype = I
+        lib.mhc_pre_delayed_broadcast.argtypes = lib.mhc_pre_delayed.argtypes
+        lib.mhc_pre_delayed_broadcast.restype = I
+        lib.mhc_pre_broadcast.argtypes = lib.mhc_pre.argtypes
+        lib.mhc_pre_broadcast.restype = I
+        lib.mhc_post_broadcast.argtypes = lib.mhc_post.argtypes
+        lib.mhc_post_broadcast.restype = I
         lib.mhc_status_string.argtypes = [I]
         lib.mhc_status_string.restype = ctypes.c_char_p
         lib.mhc_pre_delayed_plan.argtypes = [I64, I, I, P, P, P, P]
@@ -123,6 +129,70 @@ def _stream_ptr(stream, device) -> int:
     return s.cuda_stream
 
 
+def _pre_outputs(o: dict, T: int, n: int, C: int, dev, return_logits: bool) -> dict:
+    M = 2 * n + n * n
+    if "pre" not in o:
+        o["pre"] = torch.empty(T, n, dtype=torch.float32, device=dev)
+    if "post" not in o:
+        o["post"] = torch.empty(T, n, dtype=torch.float32, device=dev)
+    if "comb" not in o:
+        o["comb"] = torch.empty(T, n, n, dtype=torch.float32, device=dev)
+    if "layer_input" not in o:
+        o["layer_input"] = torch.empty(T, C, dtype=torch.bfloat16, device=dev)
+    if return_logits and "logits" not in o:
+        o["logits"] = torch.empty(T, M, dtype=torch.float32, device=dev)
+    return o
+
+
+def _pre_call(fname: str, x: torch.Tensor, pre_in: torch.Tensor | None, fn: torch.Tensor, bias: torch.Tensor,
+              alpha: torch.Tensor, norm_weight: torch.Tensor | None, T: int, n: int, C: int, sinkhorn_iters: int,
+              rms_eps: float, norm_eps: float, sinkhorn_eps: float, out: dict | None, return_logits: bool,
+              workspace: torch.Tensor | None, stream) -> dict:
+    """Marshal one pre-block call (delayed or not, four-stream or broadcast
+    x) into the C entry point ``fname``."""
+    lib = load_library()
+    dev = x.device
+    M = 2 * n + n * n
+    o = _pre_outputs(dict(out) if out else {}, T, n, C, dev, return_logits)
+    if fn.numel() != M * n * C or bias.numel() != M or alpha.numel() != 3:
+        raise ValueError("fn / bias / alpha have the wrong number of elements")
+    if pre_in is not None and pre_in.numel() != T * n:
+        raise ValueError("pre_in must have T * n elements")
+    if norm_weight is not None and norm_weight.numel() != C:
+        raise ValueError("norm_weight must have C elements")
+    args = [_dev_ptr(x, "x", torch.bfloat16, dev)]
+    if pre_in is not None:
+        args.append(_dev_ptr(pre_in, "pre_in", torch.float32, dev))
+    args += [_dev_ptr(fn, "fn", torch.float32, dev), _dev_ptr(bias, "bias", torch.float32, dev),
+             _dev_ptr(alpha, "alpha", torch.float32, dev), _dev_ptr(norm_weight, "norm_weight", torch.bfloat16, dev)]
+    outs = [_dev_ptr(o["pre"], "pre", torch.float32, dev), _dev_ptr(o["post"], "post", torch.float32, dev),
+            _dev_ptr(o["comb"], "comb", torch.float32, dev),
+            _dev_ptr(o["layer_input"], "layer_input", torch.bfloat16, dev),
+            _dev_ptr(o.get("logits"), "logits", torch.float32, dev)]
+    if workspace is None:
+        workspace = workspace_for(T, n, C, dev)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr = _dev_ptr(workspace, "workspace", torch.uint8, dev)
+        ws_bytes = workspace.numel()
+    st = getattr(lib, fname)(*args, T, n, C, int(sinkhorn_iters), float(rms_eps), float(norm_eps),
+                             float(sinkhorn_eps), *outs, ws_ptr, ws_bytes, _stream_ptr(stream, dev))
+    _check(fname, st)
+    return o
+
+
+def _shape3(x: torch.Tensor):
+    if x.dim() != 3:
+        raise ValueError("x must be [T, n, C]")
+    return x.shape
+
+
+def _shape2(x: torch.Tensor):
+    if x.dim() != 2:
+        raise ValueError("x must be [T, C] (the model-entry broadcast seam)")
+    return x.shape
+
+
 def pre_delayed(x: torch.Tensor, pre_in: torch.Tensor, fn: torch.Tensor, bias: torch.Tensor,
                 alpha: torch.Tensor, norm_weight: torch.Tensor | None = None, *,
                 sinkhorn_iters: int = SINKHORN_ITERS, rms_eps: float = 1e-6,
@@ -138,47 +208,9 @@ def pre_delayed(x: torch.Tensor, pre_in: torch.Tensor, fn: torch.Tensor, bias: t
     ``workspace``: uint8 device buffer of at least ``mhc_pre_workspace_bytes``;
     by default a cached per-device buffer is used.
     """
-    lib = load_library()
-    if x.dim() != 3:
-        raise ValueError("x must be [T, n, C]")
-    T, n, C = x.shape
-    dev = x.device
-    M = 2 * n + n * n
-    o = dict(out) if out else {}
-    if "pre" not in o:
-        o["pre"] = torch.empty(T, n, dtype=torch.float32, device=dev)
-    if "post" not in o:
-        o["post"] = torch.empty(T, n, dtype=torch.float32, device=dev)
-    if "comb" not in o:
-        o["comb"] = torch.empty(T, n, n, dtype=torch.float32, device=dev)
-    if "layer_input" not in o:
-        o["layer_input"] = torch.empty(T, C, dtype=torch.bfloat16, device=dev)
-    if return_logits and "logits" not in o:
-        o["logits"] = torch.empty(T, M, dtype=torch.float32, device=dev)
-    args = [
-        _dev_ptr(x, "x", torch.bfloat16, dev), _dev_ptr(pre_in, "pre_in", torch.float32, dev),
-        _dev_ptr(fn, "fn", torch.float32, dev), _dev_ptr(bias, "bias", torch.float32, dev),
-        _dev_ptr(alpha, "alpha", torch.float32, dev),
-        _dev_ptr(norm_weight, "norm_weight", torch.bfloat16, dev),
-    ]
-    if pre_in.numel() != T * n or fn.numel() != M * n * C or bias.numel() != M or alpha.numel() != 3:
-        raise ValueError("pre_in / fn / bias / alpha have the wrong number of elements")
-    if norm_weight is not None and norm_weight.numel() != C:
-        raise ValueError("norm_weight must have C elements")
-    outs = [_dev_ptr(o["pre"], "pre", torch.float32, dev), _dev_ptr(o["post"], "post", torch.float32, dev),
-            _dev_ptr(o["comb"], "comb", torch.float32, dev),
-            _dev_ptr(o["layer_input"], "layer_input", torch.bfloat16, dev),
-            _dev_ptr(o.get("logits"), "logits", torch.float32, dev)]
-    if workspace is None:
-        workspace = workspace_for(T, n, C, dev)
-    ws_ptr, ws_bytes = None, 0
-    if workspace is not None:
-        ws_ptr = _dev_ptr(workspace, "workspace", torch.uint8, dev)
-        ws_bytes = workspace.numel()
-    st = lib.mhc_pre_delayed(*args, T, n, C, int(sinkhorn_iters), float(rms_eps), float(norm_eps),
-                             float(sinkhorn_eps), *outs, ws_ptr, ws_bytes, _stream_ptr(stream, dev))
-    _check("mhc_pre_delayed", st)
-    return o
+    T, n, C = _shape3(x)
+    return _pre_call("mhc_pre_delayed", x, pre_in, fn, bias, alpha, norm_weight, T, n, C, sinkhorn_iters,
+                     rms_eps, norm_eps, sinkhorn_eps, out, return_logits, workspace, stream)
 
 
 def pre(x: torch.Tensor, fn: torch.Tensor, bias: torch.Tensor, alpha: torch.Tensor,
@@ -187,44 +219,33 @@ def pre(x: torch.Tensor, fn: torch.Tensor, bias: torch.Tensor, alpha: torch.Tens
         workspace: torch.Tensor | None = None, stream=None) -> dict:
     """Non-delayed mHC pre block (``mhc_pre``): as ``pre_delayed`` but the
     collapse uses each token's own pre-mix (no pre_in)."""
-    lib = load_library()
-    if x.dim() != 3:
-        raise ValueError("x must be [T, n, C]")
-    T, n, C = x.shape
-    dev = x.device
-    M = 2 * n + n * n
-    o = dict(out) if out else {}
-    if "pre" not in o:
-        o["pre"] = torch.empty(T, n, dtype=torch.float32, device=dev)
-    if "post" not in o:
-        o["post"] = torch.empty(T, n, dtype=torch.float32, device=dev)
-    if "comb" not in o:
-        o["comb"] = torch.empty(T, n, n, dtype=torch.float32, device=dev)
-    if "layer_input" not in o:
-        o["layer_input"] = torch.empty(T, C, dtype=torch.bfloat16, device=dev)
-    if return_logits and "logits" not in o:
-        o["logits"] = torch.empty(T, M, dtype=torch.float32, device=dev)
-    if fn.numel() != M * n * C or bias.numel() != M or alpha.numel() != 3:
-        raise ValueError("fn / bias / alpha have the wrong number of elements")
-    if norm_weight is not None and norm_weight.numel() != C:
-        raise ValueError("norm_weight must have C elements")
-    args = [_dev_ptr(x, "x", torch.bfloat16, dev), _dev_ptr(fn, "fn", torch.float32, dev),
-            _dev_ptr(bias, "bias", torch.float32, dev), _dev_ptr(alpha, "alpha", torch.float32, dev),
-            _dev_ptr(norm_weight, "norm_weight", torch.bfloat16, dev)]
-    outs = [_dev_ptr(o["pre"], "pre", torch.float32, dev), _dev_ptr(o["post"], "post", torch.float32, dev),
-            _dev_ptr(o["comb"], "comb", torch.float32, dev),
-            _dev_ptr(o["layer_input"], "layer_input", torch.bfloat16, dev),
-            _dev_ptr(o.get("logits"), "logits", torch.float32, dev)]
-    if workspace is None:
-        workspace = workspace_for(T, n, C, dev)
-    ws_ptr, ws_bytes = None, 0
-    if workspace is not None:
-        ws_ptr = _dev_ptr(workspace, "workspace", torch.uint8, dev)
-        ws_bytes = workspace.numel()
-    st = lib.mhc_pre(*args, T, n, C, int(sinkhorn_iters), float(rms_eps), float(norm_eps), float(sinkhorn_eps),
-                     *outs, ws_ptr, ws_bytes, _stream_ptr(stream, dev))
-    _check("mhc_pre", st)
-    return o
+    T, n, C = _shape3(x)
+    return _pre_call("mhc_pre", x, None, fn, bias, alpha, norm_weight, T, n, C, sinkhorn_iters, rms_eps,
+                     norm_eps, sinkhorn_eps, out, return_logits, workspace, stream)
+
+
+def pre_delayed_broadcast(x: torch.Tensor, pre_in: torch.Tensor, fn: torch.Tensor, bias: torch.Tensor,
+                          alpha: torch.Tensor, norm_weight: torch.Tensor | None = None, *, n: int = 4,
+                          sinkhorn_iters: int = SINKHORN_ITERS, rms_eps: float = 1e-6, norm_eps: float = 1e-6,
+                          sinkhorn_eps: float = 1e-6, out: dict | None = None, return_logits: bool = False,
+                          workspace: torch.Tensor | None = None, stream=None) -> dict:
+    """Model-entry broadcast seam, delayed (``mhc_pre_delayed_broadcast``):
+    ``pre_delayed`` on x bf16 [T, C] read as all n streams; pre_in is the
+    model-entry pre-mix [T, n]."""
+    T, C = _shape2(x)
+    return _pre_call("mhc_pre_delayed_broadcast", x, pre_in, fn, bias, alpha, norm_weight, T, n, C,
+                     sinkhorn_iters, rms_eps, norm_eps, sinkhorn_eps, out, return_logits, workspace, stream)
+
+
+def pre_broadcast(x: torch.Tensor, fn: torch.Tensor, bias: torch.Tensor, alpha: torch.Tensor,
+                  norm_weight: torch.Tensor | None = None, *, n: int = 4, sinkhorn_iters: int = SINKHORN_ITERS,
+                  rms_eps: float = 1e-6, norm_eps: float = 1e-6, sinkhorn_eps: float = 1e-6,
+                  out: dict | None = None, return_logits: bool = False, workspace: torch.Tensor | None = None,
+                  stream=None) -> dict:
+    """Model-entry broadcast seam, non-delayed (``mhc_pre_broadcast``)."""
+    T, C = _shape2(x)
+    return _pre_call("mhc_pre_broadcast", x, None, fn, bias, alpha, norm_weight, T, n, C, sinkhorn_iters,
+                     rms_eps, norm_eps, sinkhorn_eps, out, return_logits, workspace, stream)
 
 
 def post_pre_delayed(x: torch.Tensor, y: torch.Tensor, comb: torch.Tensor, post: torch.Tensor,
@@ -316,26 +337,39 @@ def pre_delayed_noalloc(x: torch.Tensor, pre_in: torch.Tensor, fn: torch.Tensor,
     return out
 
 
+def _post_call(fname: str, x: torch.Tensor, y: torch.Tensor, comb: torch.Tensor, post_gate: torch.Tensor,
+               T: int, n: int, C: int, out: torch.Tensor, stream) -> torch.Tensor:
+    dev = x.device
+    if y.numel() != T * C or comb.numel() != T * n * n or post_gate.numel() != T * n or \
+            tuple(out.shape) != (T, n, C):
+        raise ValueError("y / comb / post / out have the wrong shape")
+    st = getattr(load_library(), fname)(
+        _dev_ptr(x, "x", torch.bfloat16, dev), _dev_ptr(y, "y", torch.bfloat16, dev),
+        _dev_ptr(comb, "comb", torch.float32, dev), _dev_ptr(post_gate, "post", torch.float32, dev), T, n, C,
+        _dev_ptr(out, "out", torch.bfloat16, dev), _stream_ptr(stream, dev))
+    _check(fname, st)
+    return out
+
+
 def post(x: torch.Tensor, y: torch.Tensor, comb: torch.Tensor, post_gate: torch.Tensor, *,
          out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """mHC post block (``mhc_post``): x_new[j] = sum_i comb[i, j] x[i] + post[j] y.
     x bf16 [T, 4, C]; y bf16 [T, C]; comb fp32 [T, 4, 4]; post_gate fp32 [T, 4].
     ``out`` may be ``x`` itself (in place)."""
-    lib = load_library()
-    if x.dim() != 3:
-        raise ValueError("x must be [T, n, C]")
-    T, n, C = x.shape
-    dev = x.device
+    T, n, C = _shape3(x)
     if out is None:
         out = torch.empty_like(x)
-    if y.numel() != T * C or comb.numel() != T * n * n or post_gate.numel() != T * n or out.shape != x.shape:
-        raise ValueError("y / comb / post / out have the wrong shape")
-    st = lib.mhc_post(_dev_ptr(x, "x", torch.bfloat16, dev), _dev_ptr(y, "y", torch.bfloat16, dev),
-                      _dev_ptr(comb, "comb", torch.float32, dev),
-                      _dev_ptr(post_gate, "post", torch.float32, dev), T, n, C,
-                      _dev_ptr(out, "out", torch.bfloat16, dev), _stream_ptr(stream, dev))
-    _check("mhc_post", st)
-    return out
+    return _post_call("mhc_post", x, y, comb, post_gate, T, n, C, out, stream)
+
+
+def post_broadcast(x: torch.Tensor, y: torch.Tensor, comb: torch.Tensor, post_gate: torch.Tensor, *,
+                   n: int = 4, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Model-entry broadcast seam's post (``mhc_post_broadcast``): ``post`` on
+    x bf16 [T, C] read as all n streams; returns x_new bf16 [T, n, C]."""
+    T, C = _shape2(x)
+    if out is None:
+        out = torch.empty(T, n, C, dtype=torch.bfloat16, device=x.device)
+    return _post_call("mhc_post_broadcast", x, y, comb, post_gate, T, n, C, out, stream)
 
 
 def device_status() -> int:

@@ -10,14 +10,14 @@
 namespace mhc {
 cudaError_t launch_post(const uint16_t* x, const uint16_t* y, const float* comb,
                         const float* post, int64_t T, int C, uint16_t* x_new,
-                        cudaStream_t stream, int num_sms, bool overlap);
+                        cudaStream_t stream, int num_sms, bool overlap, bool broadcast);
 cudaError_t launch_pre_cluster(const uint16_t* x, const float* pre_in, const float* fn,
                                const float* bias, const float* alpha, const uint16_t* norm_w,
                                int64_t T, int C, int iters, float rms_eps, float norm_eps,
                                float sk_eps, float* pre_out, float* post_out, float* comb_out,
                                uint16_t* layer_input, float* logits_out, cudaStream_t stream,
                                int max_clusters, bool overlap, const uint16_t* y, const float* comb_prev,
-                               const float* post_prev, uint16_t* x_new, bool nondelayed);
+                               const float* post_prev, uint16_t* x_new, bool nondelayed, bool broadcast);
 int pre_cluster_tile_tokens(int64_t T, int max_clusters);
 int pre_cluster_max_tile();
 int pre_cluster_ctas();
@@ -30,7 +30,7 @@ cudaError_t launch_pre_tc(const uint16_t* x, const float* pre_in, const float* f
                           const float* alpha, const uint16_t* norm_w, int64_t T, int C, int iters,
                           float rms_eps, float norm_eps, float sk_eps, float* pre_out, float* post_out,
                           float* comb_out, uint16_t* layer_input, float* logits_out, void* workspace,
-                          cudaStream_t stream, int max_clusters);
+                          cudaStream_t stream, int max_clusters, bool broadcast);
 cudaError_t read_device_status(unsigned int* status);
 cudaError_t read_decode_status(unsigned int* status);
 }  // namespace mhc
@@ -186,15 +186,16 @@ namespace {
 
 struct Span { const void* p; size_t n; };
 
-// Host-side checks shared by mhc_pre_delayed and mhc_post_pre_delayed, then
-// the launch(es).  fused: the previous seam's post runs first on x (into
-// x_new) and the pre block reads x_new.
+// Host-side checks shared by the pre entry points, then the launch(es).
+// fused: the previous seam's post runs first on x (into x_new) and the pre
+// block reads x_new.  nondelayed: the collapse takes the token's own pre-mix
+// (no pre_in).  bcast: x is [T, C], read as every one of the n streams.
 mhc_status pre_entry(const uint16_t* x, const float* pre_in, const float* fn, const float* bias,
                      const float* alpha, const uint16_t* norm_weight, int64_t T, int n, int C,
                      int sinkhorn_iters, float rms_eps, float norm_eps, float sinkhorn_eps, float* pre_out,
                      float* post_out, float* comb_out, uint16_t* layer_input, float* logits_out, void* workspace,
                      size_t workspace_bytes, void* stream, bool fused, const uint16_t* y, const float* comb_prev,
-                     const float* post_prev, uint16_t* x_new, bool nondelayed = false) {
+                     const float* post_prev, uint16_t* x_new, bool nondelayed = false, bool bcast = false) {
     mhc_status st = check_pre_shape(T, n, C, sinkhorn_iters);
     if (st != MHC_OK) return st;
     if (!(rms_eps >= 0.f) || !(norm_eps >= 0.f) || !(sinkhorn_eps >= 0.f)) return MHC_ERR_INVALID_ARGUMENT;
@@ -210,7 +211,8 @@ mhc_status pre_entry(const uint16_t* x, const float* pre_in, const float* fn, co
     if ((norm_weight && !aligned16(norm_weight)) || (logits_out && !aligned16(logits_out)))
         return MHC_ERR_INVALID_ARGUMENT;
     const int M = 2 * n + n * n;
-    const size_t xb = (size_t)T * n * C * 2, pb = (size_t)T * n * 4, cb = (size_t)T * n * n * 4;
+    if (fused && bcast) return MHC_ERR_INVALID_ARGUMENT;
+    const size_t xb = (size_t)T * (bcast ? 1 : n) * C * 2, pb = (size_t)T * n * 4, cb = (size_t)T * n * n * 4;
     const size_t lib = (size_t)T * C * 2, lob = (size_t)T * M * 4;
     const size_t fnb = (size_t)M * n * C * 4, bb = (size_t)M * 4, ab = 12, nwb = (size_t)C * 2;
     // Exact aliases allowed when fused: x_new == x, comb_out == comb_prev,
@@ -249,24 +251,24 @@ mhc_status pre_entry(const uint16_t* x, const float* pre_in, const float* fn, co
                 float* pre1 = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + planes);
                 cudaError_t e = mhc::launch_pre_tc(x, pre1, fn, bias, alpha, norm_weight, T, C, sinkhorn_iters,
                                                    rms_eps, norm_eps, sinkhorn_eps, pre1, post_out, comb_out,
-                                                   layer_input, logits_out, workspace, s, tcc);
+                                                   layer_input, logits_out, workspace, s, tcc, bcast);
                 if (e == cudaSuccess)
                     e = mhc::launch_pre_tc(x, pre1, fn, bias, alpha, norm_weight, T, C, sinkhorn_iters, rms_eps,
                                            norm_eps, sinkhorn_eps, pre_out, post_out, comb_out, layer_input,
-                                           logits_out, workspace, s, tcc);
+                                           logits_out, workspace, s, tcc, bcast);
                 return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA;
             }
             const uint16_t* xin = x;
             if (fused) {   // large T: the post kernel, then the tensor-core pre on x_new
                 int sms = num_sms(dev);
                 if (sms <= 0) return MHC_ERR_CUDA;
-                if (mhc::launch_post(x, y, comb_prev, post_prev, T, C, x_new, s, sms, overlap) != cudaSuccess)
+                if (mhc::launch_post(x, y, comb_prev, post_prev, T, C, x_new, s, sms, overlap, false) != cudaSuccess)
                     return MHC_ERR_CUDA;
                 xin = x_new;
             }
             cudaError_t e = mhc::launch_pre_tc(xin, pre_in, fn, bias, alpha, norm_weight, T, C, sinkhorn_iters,
                                                rms_eps, norm_eps, sinkhorn_eps, pre_out, post_out, comb_out,
-                                               layer_input, logits_out, workspace, s, tcc);
+                                               layer_input, logits_out, workspace, s, tcc, bcast);
             return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA;
         }
     }
@@ -276,7 +278,7 @@ mhc_status pre_entry(const uint16_t* x, const float* pre_in, const float* fn, co
                                             norm_eps, sinkhorn_eps, pre_out, post_out, comb_out, layer_input,
                                             logits_out, s, mc, overlap, fused ? y : nullptr,
                                             fused ? comb_prev : nullptr, fused ? post_prev : nullptr,
-                                            fused ? x_new : nullptr, nondelayed);
+                                            fused ? x_new : nullptr, nondelayed, bcast);
     return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA;
 }
 
@@ -315,16 +317,43 @@ mhc_status mhc_post_pre_delayed(const uint16_t* x, const uint16_t* y, const floa
                      stream, true, y, comb, post, x_new);
 }
 
-mhc_status mhc_post(const uint16_t* x, const uint16_t* y, const float* comb, const float* post,
-                    int64_t T, int n, int C, uint16_t* x_new, void* stream) {
+mhc_status mhc_pre_delayed_broadcast(const uint16_t* x, const float* pre_in, const float* fn, const float* bias,
+                                     const float* alpha, const uint16_t* norm_weight, int64_t T, int n, int C,
+                                     int sinkhorn_iters, float rms_eps, float norm_eps, float sinkhorn_eps,
+                                     float* pre_out, float* post_out, float* comb_out, uint16_t* layer_input,
+                                     float* logits_out, void* workspace, size_t workspace_bytes, void* stream) {
+    return pre_entry(x, pre_in, fn, bias, alpha, norm_weight, T, n, C, sinkhorn_iters, rms_eps, norm_eps,
+                     sinkhorn_eps, pre_out, post_out, comb_out, layer_input, logits_out, workspace, workspace_bytes,
+                     stream, false, nullptr, nullptr, nullptr, nullptr, false, true);
+}
+
+mhc_status mhc_pre_broadcast(const uint16_t* x, const float* fn, const float* bias, const float* alpha,
+                             const uint16_t* norm_weight, int64_t T, int n, int C, int sinkhorn_iters,
+                             float rms_eps, float norm_eps, float sinkhorn_eps, float* pre_out, float* post_out,
+                             float* comb_out, uint16_t* layer_input, float* logits_out, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+    return pre_entry(x, nullptr, fn, bias, alpha, norm_weight, T, n, C, sinkhorn_iters, rms_eps, norm_eps,
+                     sinkhorn_eps, pre_out, post_out, comb_out, layer_input, logits_out, workspace, workspace_bytes,
+                     stream, false, nullptr, nullptr, nullptr, nullptr, true, true);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Host-side checks and the launch for mhc_post and mhc_post_broadcast
+// (bcast: x is [T, C], every stream equal to it; x_new may not alias it).
+mhc_status post_entry(const uint16_t* x, const uint16_t* y, const float* comb, const float* post,
+                      int64_t T, int n, int C, uint16_t* x_new, void* stream, bool bcast) {
     if (T < 0 || n < 1 || C < 1) return MHC_ERR_INVALID_ARGUMENT;
     if (n != 4 || C % 8 != 0) return MHC_ERR_UNSUPPORTED;
     if (T == 0) return MHC_OK;
     const void* req[] = {x, y, comb, post, x_new};
     for (const void* p : req)
         if (!p || !aligned16(p)) return MHC_ERR_INVALID_ARGUMENT;
-    const size_t xb = (size_t)T * n * C * 2;
-    if ((const void*)x_new != (const void*)x && overlaps(x_new, xb, x, xb)) return MHC_ERR_INVALID_ARGUMENT;
+    const size_t xb = (size_t)T * n * C * 2, xinb = bcast ? (size_t)T * C * 2 : xb;
+    if ((bcast || (const void*)x_new != (const void*)x) && overlaps(x_new, xb, x, xinb))
+        return MHC_ERR_INVALID_ARGUMENT;
     if (overlaps(x_new, xb, y, (size_t)T * C * 2) || overlaps(x_new, xb, comb, (size_t)T * n * n * 4) ||
         overlaps(x_new, xb, post, (size_t)T * n * 4))
         return MHC_ERR_INVALID_ARGUMENT;
@@ -333,8 +362,22 @@ mhc_status mhc_post(const uint16_t* x, const uint16_t* y, const float* comb, con
     int sms = num_sms(dev);
     if (sms <= 0) return MHC_ERR_CUDA;
     cudaError_t e = mhc::launch_post(x, y, comb, post, T, C, x_new, static_cast<cudaStream_t>(stream), sms,
-                                     g_launch_overlap.load() != 0);
+                                     g_launch_overlap.load() != 0, bcast);
     return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+mhc_status mhc_post(const uint16_t* x, const uint16_t* y, const float* comb, const float* post,
+                    int64_t T, int n, int C, uint16_t* x_new, void* stream) {
+    return post_entry(x, y, comb, post, T, n, C, x_new, stream, false);
+}
+
+mhc_status mhc_post_broadcast(const uint16_t* x, const uint16_t* y, const float* comb, const float* post,
+                              int64_t T, int n, int C, uint16_t* x_new, void* stream) {
+    return post_entry(x, y, comb, post, T, n, C, x_new, stream, true);
 }
 
 }  // extern "C"

@@ -13,10 +13,15 @@
 // once-touched data does not evict reused lines from L2.  x_new may be x
 // (in place): a thread reads all four streams of its item before writing them
 // and items are disjoint, so x and x_new carry no __restrict__.
+//
+// The model-entry broadcast seam (BCAST): x is [T][C], every stream of the
+// residual equal to it; one 16-byte load serves all four streams and the
+// arithmetic is unchanged (the same bits as on a copied x).
 #include "common.cuh"
 
 namespace mhc {
 
+template <bool BCAST>
 __global__ void __launch_bounds__(256)
 post_kernel(const uint4* x, const uint4* __restrict__ y,
             const float4* __restrict__ comb, const float4* __restrict__ post,
@@ -36,9 +41,14 @@ post_kernel(const uint4* x, const uint4* __restrict__ y,
             if (!ok[u]) it = base;
             tok[u] = it / c8;
             col[u] = it - tok[u] * c8;
-            const uint4* xp = x + tok[u] * (4 * (int64_t)c8) + col[u];
+            if (BCAST) {
+                xv[u][0] = ld_stream(x + tok[u] * (int64_t)c8 + col[u]);
+                xv[u][1] = xv[u][2] = xv[u][3] = xv[u][0];
+            } else {
+                const uint4* xp = x + tok[u] * (4 * (int64_t)c8) + col[u];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) xv[u][i] = ld_stream(xp + (int64_t)i * c8);
+                for (int i = 0; i < 4; ++i) xv[u][i] = ld_stream(xp + (int64_t)i * c8);
+            }
             yv[u] = ld_stream(y + tok[u] * c8 + col[u]);
         }
 #pragma unroll
@@ -73,7 +83,7 @@ post_kernel(const uint4* x, const uint4* __restrict__ y,
 
 cudaError_t launch_post(const uint16_t* x, const uint16_t* y, const float* comb,
                         const float* post, int64_t T, int C, uint16_t* x_new,
-                        cudaStream_t stream, int num_sms, bool overlap) {
+                        cudaStream_t stream, int num_sms, bool overlap, bool broadcast) {
     const int c8 = C / 8;
     const int64_t items = T * (int64_t)c8;
     const int threads = 256;
@@ -90,7 +100,8 @@ cudaError_t launch_post(const uint16_t* x, const uint16_t* y, const float* comb,
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = overlap ? 1 : 0;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, post_kernel, reinterpret_cast<const uint4*>(x),
+    cudaError_t e = cudaLaunchKernelEx(&cfg, broadcast ? post_kernel<true> : post_kernel<false>,
+                                       reinterpret_cast<const uint4*>(x),
                                        reinterpret_cast<const uint4*>(y), reinterpret_cast<const float4*>(comb),
                                        reinterpret_cast<const float4*>(post), items, c8,
                                        reinterpret_cast<uint4*>(x_new));

@@ -91,6 +91,8 @@ struct Args {
     int tile;      // tokens per tile (1..kMaxTile)
     int lcmax;     // max 8-column groups per CTA slice
     int xstride;   // bytes per token row of the x tile in shared memory
+    int64_t xtok;  // elements between tokens of x: 4C, or C for the broadcast seam
+    int64_t xsc;   // elements between streams of x: C, or 0 (all four read x[t])
     // previous seam's post, fused in front (y == nullptr: none)
     const uint16_t* y;
     const float* comb_prev;
@@ -259,7 +261,9 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
         for (int idx = tid; idx < items; idx += kThreads) {
             const int tt = idx / (4 * lc), r2 = idx - tt * 4 * lc;
             const int i = r2 / lc, cc = r2 - i * lc;
-            const uint16_t* src = a.x + ((t0 + tt) * 4 + i) * (int64_t)C + c0 + 8 * cc;
+            // (the fused instance never takes a broadcast x)
+            const int64_t xtok = fused ? 4 * (int64_t)C : a.xtok, xsc = fused ? (int64_t)C : a.xsc;
+            const uint16_t* src = a.x + (t0 + tt) * xtok + i * xsc + c0 + 8 * cc;
             cp_async16(smem_u32(xs + tt * a.xstride + (i * ncols + 8 * cc) * 2), src);
         }
         if (!nondel && tid < n) cp_async16(smem_u32(pin + 4 * tid), a.pre_in + (t0 + tid) * 4);
@@ -714,7 +718,8 @@ cudaError_t launch_pre_cluster(const uint16_t* x, const float* pre_in, const flo
                                float sk_eps, float* pre_out, float* post_out, float* comb_out,
                                uint16_t* layer_input, float* logits_out, cudaStream_t stream,
                                int max_clusters, bool overlap, const uint16_t* y, const float* comb_prev,
-                               const float* post_prev, uint16_t* x_new, bool nondelayed) {
+                               const float* post_prev, uint16_t* x_new, bool nondelayed, bool broadcast) {
+    if (broadcast && y != nullptr) return cudaErrorInvalidValue;   // no fused post on a broadcast x
     dec::Args a;
     a.y = y; a.comb_prev = comb_prev; a.post_prev = post_prev; a.x_new = x_new;
     a.x = x; a.pre_in = pre_in; a.fn = fn; a.bias = bias; a.alpha = alpha; a.norm_w = norm_w;
@@ -726,6 +731,8 @@ cudaError_t launch_pre_cluster(const uint16_t* x, const float* pre_in, const flo
     a.ntiles = (T + a.tile - 1) / a.tile;
     a.lcmax = dec::lcmax_of(C);
     a.xstride = dec::dec_xstride(a.lcmax);
+    a.xtok = broadcast ? C : 4 * (int64_t)C;
+    a.xsc = broadcast ? 0 : C;
     cudaLaunchAttribute attr[2];
     const int mode = nondelayed ? dec::kNonDelayed : (y != nullptr ? dec::kFusedPost : dec::kDelayed);
     cudaLaunchConfig_t cfg = dec::cluster_config(attr, (size_t)dec::dec_layout(a.lcmax, mode).total, stream);

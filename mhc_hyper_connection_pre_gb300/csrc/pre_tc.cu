@@ -40,6 +40,10 @@
 //   warp 10    finalizer: for its 8 tokens of the tile sums the 16 CTAs'
 //              partials in rank order, pushes the fold scale to all 16 CTAs,
 //              then logits, gates and the Sinkhorn comb in registers.
+// The model-entry broadcast seam (x is [T][C], the same for all four
+// streams) brings one x box per stage, which the MMA and the collapse read
+// as every stream: the same operands, so the same bits as the four-stream
+// call on a copied x, with a quarter of the x traffic.
 // The only global scratch is the fn planes in the caller's workspace; every
 // wait is bounded (see sm100.cuh).
 #include "common.cuh"
@@ -144,6 +148,7 @@ __device__ __forceinline__ void split3(const float (&w)[8], uint32_t (&pk)[3][4]
     }
 }
 
+template <bool BCAST>
 __global__ void __launch_bounds__(kThreads, 1)
 pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap omap, const Args a) {
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -170,6 +175,9 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
     const int cid = (int)cluster_id_x(), ncl = (int)ncluster_x();
     const int C = a.C, K = 4 * C, slice = C / kCtas, ngroups = slice / kCols, c0 = (int)rank * slice;
     const bool fold = a.norm_w != nullptr;
+    // broadcast seam: one x box per stage, read as all four streams
+    constexpr int nbox = BCAST ? 1 : 4, xbox = BCAST ? 0 : kBoxBytes;
+    constexpr uint32_t slot_bytes = (uint32_t)(kSlotBytes - (4 - nbox) * kBoxBytes);
     unsigned char* wreg = a.ws + (size_t)(cid * kCtas + (int)rank) * ngroups * kWStage;
     // stages of this CTA in the whole launch, and those issued before the fn planes are ready
     const int my_tiles = cid < a.ntiles ? (a.ntiles - 1 - cid) / ncl + 1 : 0;
@@ -199,9 +207,9 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
         const uint64_t pol_x = policy_evict_first();
         for (uint32_t q = 0; q < early; ++q) {
             const int tile = cid + (int)(q / ngroups) * ncl, grp = (int)(q % ngroups);
-            mbar_arrive_expect_tx(&full[q], kSlotBytes);
+            mbar_arrive_expect_tx(&full[q], slot_bytes);
 #pragma unroll
-            for (int st = 0; st < 4; ++st)
+            for (int st = 0; st < nbox; ++st)
                 tma_load_3d_hint(stages + q * kSlotBytes + st * kBoxBytes, &xmap, c0 + kCols * grp, st,
                                  tile * kTile, &full[q], pol_x);
         }
@@ -271,9 +279,9 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
                 const int s = g % kStages;
                 mbar_wait(&empty[s], ((g / kStages) & 1) ^ 1, abort);
                 unsigned char* slot = stages + s * kSlotBytes;
-                mbar_arrive_expect_tx(&full[s], kSlotBytes);
+                mbar_arrive_expect_tx(&full[s], slot_bytes);
 #pragma unroll
-                for (int st = 0; st < 4; ++st)
+                for (int st = 0; st < nbox; ++st)
                     tma_load_3d_hint(slot + st * kBoxBytes, &xmap, c0 + kCols * grp, st, tile * kTile, &full[s],
                                      pol_x);
                 bulk_load_hint(slot + kXBytes, wreg + grp * kWStage, kWStage, &full[s], pol_w);
@@ -302,7 +310,7 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
 #pragma unroll
                     for (int st = 0; st < 4; ++st) {
                         const uint32_t slot = sbase + s * kSlotBytes;
-                        const uint64_t ad = smem_desc(slot + st * kBoxBytes, 16, 256, kLayoutSwizzle32B);
+                        const uint64_t ad = smem_desc(slot + st * xbox, 16, 256, kLayoutSwizzle32B);
                         const uint64_t bd = smem_desc(slot + kXBytes + st * kWBlock, 16, 256, kLayoutSwizzle32B);
                         mma_bf16(dt, ad, bd, idesc, (grp | st) != 0);
                     }
@@ -397,8 +405,8 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
                 f32x2 xv[4][8];
 #pragma unroll
                 for (int st = 0; st < 4; ++st) {
-                    const uint4 lo = *reinterpret_cast<const uint4*>(sb + st * kBoxBytes + xo0);
-                    const uint4 hi = *reinterpret_cast<const uint4*>(sb + st * kBoxBytes + xo1);
+                    const uint4 lo = *reinterpret_cast<const uint4*>(sb + st * xbox + xo0);
+                    const uint4 hi = *reinterpret_cast<const uint4*>(sb + st * xbox + xo1);
                     xv[st][0] = bf16x2_to_f32x2(lo.x); xv[st][1] = bf16x2_to_f32x2(lo.y);
                     xv[st][2] = bf16x2_to_f32x2(lo.z); xv[st][3] = bf16x2_to_f32x2(lo.w);
                     xv[st][4] = bf16x2_to_f32x2(hi.x); xv[st][5] = bf16x2_to_f32x2(hi.y);
@@ -629,9 +637,11 @@ int pre_tc_tile_tokens() { return tc::kTile; }
 // One-time set-up for the current device: cluster-size and shared-memory
 // attributes, then the number of co-resident 16-CTA clusters (0 on error).
 int pre_tc_prepare() {
-    cudaError_t e = cudaFuncSetAttribute(tc::pre_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(tc::pre_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemBytes);
+    cudaError_t e = cudaSuccess;
+    for (auto k : {tc::pre_tc_kernel<false>, tc::pre_tc_kernel<true>}) {
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemBytes);
+    }
     if (e != cudaSuccess || encode_fn() == nullptr) return 0;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -645,7 +655,7 @@ int pre_tc_prepare() {
     cfg.gridDim = dim3(tc::kCtas, 1, 1);
     cfg.dynamicSmemBytes = tc::kSmemBytes;
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, tc::pre_tc_kernel, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&n, tc::pre_tc_kernel<false>, &cfg);
     return e == cudaSuccess ? n : 0;
 }
 
@@ -653,14 +663,16 @@ cudaError_t launch_pre_tc(const uint16_t* x, const float* pre_in, const float* f
                           const float* alpha, const uint16_t* norm_w, int64_t T, int C, int iters,
                           float rms_eps, float norm_eps, float sk_eps, float* pre_out, float* post_out,
                           float* comb_out, uint16_t* layer_input, float* logits_out, void* workspace,
-                          cudaStream_t stream, int max_clusters) {
+                          cudaStream_t stream, int max_clusters, bool broadcast) {
     PFN_encodeTiled enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
-    // x viewed as [T][4][C] bf16; box = 16 columns (32 B) x 1 stream x 128
-    // tokens, written to shared memory with the 32-byte swizzle the MMA reads.
+    // x viewed as [T][4][C] bf16 (broadcast: [T][1][C], every stream's box
+    // taken at stream 0); box = 16 columns (32 B) x 1 stream x 128 tokens,
+    // written to shared memory with the 32-byte swizzle the MMA reads.
     alignas(64) CUtensorMap map;
-    const cuuint64_t dims[3] = {(cuuint64_t)C, 4, (cuuint64_t)T};
-    const cuuint64_t strides[2] = {(cuuint64_t)C * 2, (cuuint64_t)C * 8};
+    const cuuint64_t ns = broadcast ? 1 : 4;
+    const cuuint64_t dims[3] = {(cuuint64_t)C, ns, (cuuint64_t)T};
+    const cuuint64_t strides[2] = {(cuuint64_t)C * 2, (cuuint64_t)C * 2 * ns};
     const cuuint32_t box[3] = {(cuuint32_t)tc::kCols, 1, (cuuint32_t)tc::kTile};
     const cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(x), dims, strides, box, estr,
@@ -698,7 +710,8 @@ cudaError_t launch_pre_tc(const uint16_t* x, const float* pre_in, const float* f
     cfg.gridDim = dim3((unsigned)(nclusters * tc::kCtas), 1, 1);
     cfg.dynamicSmemBytes = tc::kSmemBytes;
     cfg.stream = stream;
-    return cudaLaunchKernelEx(&cfg, tc::pre_tc_kernel, map, omap, a);
+    return broadcast ? cudaLaunchKernelEx(&cfg, tc::pre_tc_kernel<true>, map, omap, a)
+                     : cudaLaunchKernelEx(&cfg, tc::pre_tc_kernel<false>, map, omap, a);
 }
 
 // Host read-and-clear of the device status word (synchronous).

@@ -169,6 +169,27 @@ def pre_nondelayed(x_bits, fn, bias, alpha, norm_w_bits=None, *, pre_mix=None, i
     return out
 
 
+def broadcast_streams(x_bits, n: int = 4) -> np.ndarray:
+    """The model-entry residual: n copies of the hidden state x [T, C] as the
+    streams of a [T, n, C] residual (the #56503 page, "Approach": the
+    model-entry seam projects the narrower operand x)."""
+    x_bits = _c(x_bits, np.uint16)
+    T, C = x_bits.shape
+    return np.ascontiguousarray(np.broadcast_to(x_bits[:, None, :], (T, n, C)))
+
+
+def pre_delayed_broadcast(x_bits, pre_in, fn, bias, alpha, norm_w_bits=None, n: int = 4, **kw) -> dict:
+    """Delayed pre block of the model-entry broadcast seam: by definition the
+    delayed block on the broadcast residual (pre_in: the model-entry
+    pre-mix, the #56503 page, "Test Plan")."""
+    return pre_delayed(broadcast_streams(x_bits, n), pre_in, fn, bias, alpha, norm_w_bits, **kw)
+
+
+def pre_nondelayed_broadcast(x_bits, fn, bias, alpha, norm_w_bits=None, n: int = 4, **kw) -> dict:
+    """Non-delayed pre block of the model-entry broadcast seam (definition)."""
+    return pre_nondelayed(broadcast_streams(x_bits, n), fn, bias, alpha, norm_w_bits, **kw)
+
+
 def gates_from_logits(logits, n=4, *, iters=SINKHORN_ITERS,
                       sinkhorn_eps=SINKHORN_EPS) -> dict:
     """pre = sigmoid(l[:n]), post = 2 sigmoid(l[n:2n]), comb = Sinkhorn of
@@ -204,3 +225,9 @@ def post(x_bits, y_bits, comb, post_gate, *, nthreads=1) -> tuple[np.ndarray, np
     if rc != 0:
         raise ValueError("oracle: bad arguments to post")
     return xn, x64
+
+
+def post_broadcast(x_bits, y_bits, comb, post_gate, n: int = 4, *, nthreads=1):
+    """Post of the model-entry broadcast seam: by definition ``post`` on the
+    broadcast residual; returns x_new [T, n, C] as ``post`` does."""
+    return post(broadcast_streams(x_bits, n), y_bits, comb, post_gate, nthreads=nthreads)

@@ -166,3 +166,30 @@ def test_fused_exact_aliases_pass_the_host_checks(lib):
     # to find a device (MHC_ERR_CUDA), instead of MHC_ERR_INVALID_ARGUMENT
     assert _fused(lib, x_new=A) == CUDA_ERR
     assert _fused(lib, comb_out=A + 0x2000000, post_out=A + 0x2100000) == CUDA_ERR
+
+
+def test_broadcast_entry_points_size_x_as_t_by_c(lib):
+    """The broadcast calls take x as [T, C]: an output just past T*C*2 bytes
+    of x passes the host checks (and then finds no device), where the
+    four-stream call sees it inside x; x_new may never alias a broadcast x."""
+    just_past = A + 16 * 5120 * 2            # T * C * 2 bytes after x
+    assert _pre(lib, layer_input=just_past) == INVALID
+    args = dict(x=A, pre_in=A + 0x100000, fn=A + 0x200000, bias=A + 0x3000000, alpha=A + 0x3001000,
+                norm_weight=None, T=16, n=4, C=5120, iters=20, rms_eps=1e-6, norm_eps=1e-6,
+                sk_eps=1e-6, pre_out=A + 0x4000000, post_out=A + 0x4100000, comb_out=A + 0x4200000,
+                layer_input=just_past, logits_out=None, workspace=None, workspace_bytes=0, stream=None)
+    assert lib.mhc_pre_delayed_broadcast(*args.values()) == CUDA_ERR
+    args["layer_input"] = A + 0x100
+    assert lib.mhc_pre_delayed_broadcast(*args.values()) == INVALID
+    args["layer_input"] = just_past
+    del args["pre_in"]
+    assert lib.mhc_pre_broadcast(*args.values()) == CUDA_ERR
+    args["n"] = 3
+    assert lib.mhc_pre_broadcast(*args.values()) == UNSUPPORTED
+    post = dict(x=A, y=A + 0x1000000, comb=A + 0x2000000, post=A + 0x2100000, T=16, n=4, C=5120,
+                x_new=A, stream=None)
+    assert _post(lib, x_new=A) == CUDA_ERR                          # in place is allowed for mhc_post
+    assert lib.mhc_post_broadcast(*post.values()) == INVALID        # never for the broadcast x
+    post["x_new"] = just_past
+    assert _post(lib, x_new=just_past) == INVALID
+    assert lib.mhc_post_broadcast(*post.values()) == CUDA_ERR

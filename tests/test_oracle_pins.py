@@ -502,3 +502,64 @@ def test_nondelayed_identical_streams_closed_form():
     want = s * xv
     bound = 4 * 2.0 ** -24 * (np.abs(o["pre_mix"]).astype(np.float64).sum(1, keepdims=True) * np.abs(xv)) + 1e-30
     assert np.all(np.abs(o["h32"].astype(np.float64) - want) <= bound)
+
+
+# ------------------------------------------------- model-entry broadcast ---
+
+def _bcast_case(T=5, C=96, seed=21):
+    rng = np.random.default_rng(seed)
+    x = bf16_bits(torch.from_numpy(rng.standard_normal((T, C)).astype(np.float32)).to(torch.bfloat16))
+    fn = (0.05 * rng.standard_normal((24, N * C))).astype(np.float32)
+    bias = (0.2 * rng.standard_normal(24)).astype(np.float32)
+    pre_in = (1.0 / (1.0 + np.exp(-rng.standard_normal((T, N))))).astype(np.float32)
+    return x, fn, bias, pre_in
+
+
+def test_broadcast_projection_narrows_to_c_columns():
+    """The model-entry seam projects the narrower operand: with every stream
+    equal to x, x_flat . fn[m] = x . (sum_i fn[m][iC:(i+1)C]) and the RMS
+    over K = 4C equals the RMS over C, so the logits follow from a [24, C]
+    matmul against the stream-summed fn (numpy, fp64).  A broadcast along the
+    wrong axis or a K/C mix-up in the RMS fails it."""
+    T, C = 5, 96
+    x, fn, bias, pre_in = _bcast_case(T, C)
+    al = np.asarray((0.5, 1.5, 2.0), np.float32)
+    out = oracle.pre_delayed_broadcast(x, pre_in, fn, bias, al)
+    xv = oracle.bf16_to_f64(x)
+    fsum = fn.astype(np.float64).reshape(24, N, C).sum(1)
+    r = 1.0 / np.sqrt((xv * xv).sum(1) / C + oracle.RMS_EPS)
+    a = np.array([0.5] * N + [1.5] * N + [2.0] * (N * N))
+    want = r[:, None] * (xv @ fsum.T) * a[None, :] + bias.astype(np.float64)[None, :]
+    np.testing.assert_allclose(out["logits"], want, rtol=1e-12, atol=1e-12)
+
+
+def test_broadcast_collapse_one_hot_and_non_delayed_equals_delayed():
+    """A one-hot model-entry pre-mix returns x itself (no fold), and the
+    non-delayed broadcast block equals the delayed one fed its own pre."""
+    T, C = 4, 64
+    x, fn, bias, pre_in = _bcast_case(T, C, seed=22)
+    al = np.ones(3, np.float32)
+    oh = np.zeros((T, N), np.float32)
+    oh[:, 2] = 1.0
+    d = oracle.pre_delayed_broadcast(x, oh, fn, bias, al)
+    assert np.array_equal(d["layer_input"], x)
+    nd = oracle.pre_nondelayed_broadcast(x, fn, bias, al)
+    d2 = oracle.pre_delayed_broadcast(x, nd["pre"].astype(np.float32), fn, bias, al)
+    assert np.array_equal(nd["layer_input"], d2["layer_input"])
+
+
+def test_broadcast_post_is_column_sum_times_x():
+    """Post on the broadcast residual: sum_i comb[i, j] x = (sum_i comb[i, j])
+    x, so x_new[j] = bf16(colsum_j x + post_j y) (numpy, fp64)."""
+    T, C = 6, 40
+    rng = np.random.default_rng(23)
+    x, _, _, _ = _bcast_case(T, C, seed=24)
+    y = bf16_bits(torch.from_numpy(rng.standard_normal((T, C)).astype(np.float32)).to(torch.bfloat16))
+    comb = rng.random((T, N, N)).astype(np.float32)
+    pg = (2.0 * rng.random((T, N))).astype(np.float32)
+    bits, v64 = oracle.post_broadcast(x, y, comb, pg)
+    xv, yv = oracle.bf16_to_f64(x), oracle.bf16_to_f64(y)
+    cs = comb.astype(np.float64).sum(1)                      # [T, j]
+    want = cs[:, :, None] * xv[:, None, :] + pg.astype(np.float64)[:, :, None] * yv[:, None, :]
+    np.testing.assert_allclose(v64, want, rtol=1e-14, atol=1e-300)
+    assert np.array_equal(bits, oracle.bf16_round(want))

@@ -358,6 +358,68 @@ def test_nondelayed_pre_is_one_launch_in_a_graph_below_256_tokens():
     g.close()
 
 
+def _bcast_case(T, C, fold, seed):
+    d = seam_inputs(T, C=C, seed=seed, fold=fold, with_y=True)
+    d["x"] = d["x"][:, 0, :].contiguous()          # the model-entry hidden state [T, C]
+    return d, _to_dev(d)
+
+
+@pytest.mark.parametrize("T,C,fold", [(1, 5120, True), (7, 5120, False), (33, 5120, True), (128, 5120, False),
+                                      (300, 1000, True), (300, 5120, True), (1000, 5120, False), (5, 8, True)])
+def test_broadcast_pre_is_bit_identical_to_the_copied_residual(T, C, fold):
+    """mhc_pre_delayed_broadcast / mhc_pre_broadcast on x [T, C] give every
+    output bit for bit as the four-stream calls on x copied into four
+    streams (decode kernel, multi-round tiles at C = 1000, tensor-core
+    kernel from 256 tokens at C = 5120)."""
+    d, gd = _bcast_case(T, C, fold, seed=2000 + T + C)
+    xb = gd["x"][:, None, :].expand(T, 4, C).contiguous()
+    got = mhc.pre_delayed_broadcast(gd["x"], gd["pre_in"], gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"],
+                                    return_logits=True)
+    ref = mhc.pre_delayed(xb, gd["pre_in"], gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"], return_logits=True)
+    got_nd = mhc.pre_broadcast(gd["x"], gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"], return_logits=True)
+    ref_nd = mhc.pre(xb, gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"], return_logits=True)
+    torch.cuda.synchronize()
+    assert mhc.device_status() == 0
+    for k in ("pre", "post", "comb", "layer_input", "logits"):
+        assert torch.equal(got[k], ref[k]), k
+        assert torch.equal(got_nd[k], ref_nd[k]), "non-delayed " + k
+
+
+@pytest.mark.parametrize("T,C", [(1, 5120), (64, 5120), (1000, 5120), (17, 2056)])
+def test_broadcast_post_is_bit_identical_to_the_copied_residual(T, C):
+    d, gd = _bcast_case(T, C, False, seed=2100 + T)
+    comb = torch.rand(T, 4, 4, device="cuda")
+    post = 2 * torch.rand(T, 4, device="cuda")
+    xb = gd["x"][:, None, :].expand(T, 4, C).contiguous()
+    got = mhc.post_broadcast(gd["x"], gd["y"], comb, post)
+    ref = mhc.post(xb, gd["y"], comb, post)
+    torch.cuda.synchronize()
+    assert torch.equal(got, ref)
+
+
+@pytest.mark.parametrize("T,C,fold", [(24, 5120, True), (300, 5120, False)])
+def test_broadcast_seam_against_the_oracle(T, C, fold):
+    """The entry seam against the oracle's broadcast definitions: gates
+    within 2e-5, collapse bit-exact or fold within 1 ulp, logits within the
+    dot-product bound; the entry post's x_new within 1 ulp."""
+    d, gd = _bcast_case(T, C, fold, seed=2200 + T)
+    got = mhc.pre_delayed_broadcast(gd["x"], gd["pre_in"], gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"],
+                                    return_logits=True)
+    xn = mhc.post_broadcast(gd["x"], gd["y"], got["comb"], got["post"])
+    torch.cuda.synchronize()
+    assert mhc.device_status() == 0
+    g = {k: v.cpu() for k, v in got.items()}
+    x1 = bf16_bits(d["x"])
+    nw = None if d["norm_w"] is None else bf16_bits(d["norm_w"])
+    o = oracle.pre_delayed_broadcast(x1, d["pre_in"].numpy(), d["fn"].numpy(), d["bias"].numpy(),
+                                     d["alpha"].numpy(), nw, nthreads=NTHREADS)
+    _check_pre(g, o, oracle.broadcast_streams(x1), d, fold)
+    yb, cb, pb = bf16_bits(d["y"]), g["comb"].numpy(), g["post"].numpy()
+    o_bits, _ = oracle.post_broadcast(x1, yb, cb, pb, nthreads=NTHREADS)
+    g_bits = xn.cpu().view(torch.int16).numpy().view(np.uint16)
+    assert_bf16(g_bits, o_bits, "x_new", abs_scale=post_abs_scale(oracle.broadcast_streams(x1), yb, cb, pb))
+
+
 def test_graph_seam_is_two_launches_and_replays_exactly():
     """One seam (pre + post) captured in a CUDA graph holds exactly 2 kernel
     nodes; 200 replays give the eager result bit for bit."""
