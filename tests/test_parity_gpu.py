@@ -660,3 +660,39 @@ def test_config4_stress_full_size_sampled():
     assert_bf16(g["layer_input"].view(torch.int16).numpy().view(np.uint16)[rows], o["layer_input"],
                 "layer_input")
     assert torch.all(g["layer_input"].view(torch.int16)[zero.cpu()] == 0)
+
+
+def test_entry_points_full_size_properties():
+    """T = 16384 with the fold, the benchmark's launch configuration, for the
+    other entry points: the broadcast pre and post equal the four-stream calls
+    on the copied residual bit for bit; the non-delayed pre equals the
+    delayed call fed its own pre bit for bit (two tensor-core passes against
+    one); sampled rows of the broadcast seam against the oracle."""
+    T = 16384
+    gd = seam_inputs(T, seed=3, fold=True, with_y=True, device="cuda")
+    xe = gd["x"][:, 0, :].contiguous()
+    xb4 = xe[:, None, :].expand(T, 4, xe.shape[1]).contiguous()
+    args = (gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"])
+    got_b = mhc.pre_delayed_broadcast(xe, gd["pre_in"], *args, return_logits=True)
+    ref_b = mhc.pre_delayed(xb4, gd["pre_in"], *args, return_logits=True)
+    xn_b = mhc.post_broadcast(xe, gd["y"], got_b["comb"], got_b["post"])
+    xn_4 = mhc.post(xb4, gd["y"], got_b["comb"], got_b["post"])
+    torch.cuda.synchronize()
+    assert mhc.device_status() == 0
+    for k in ("pre", "post", "comb", "layer_input", "logits"):
+        assert torch.equal(got_b[k], ref_b[k]), "broadcast " + k
+    assert torch.equal(xn_b, xn_4)
+    del xb4, ref_b, xn_4
+    got_n = mhc.pre(gd["x"], *args, return_logits=True)
+    ref_n = mhc.pre_delayed(gd["x"], got_n["pre"].clone(), *args, return_logits=True)
+    torch.cuda.synchronize()
+    assert mhc.device_status() == 0
+    for k in ("pre", "post", "comb", "layer_input", "logits"):
+        assert torch.equal(got_n[k], ref_n[k]), "non-delayed " + k
+    rows = _sample_rows(T)
+    g = {k: v.cpu() for k, v in got_b.items()}
+    x1 = bf16_bits(xe)[rows]
+    nw = bf16_bits(gd["norm_w"])
+    o = oracle.pre_delayed_broadcast(x1, gd["pre_in"].cpu().numpy()[rows], gd["fn"].cpu().numpy(),
+                                     gd["bias"].cpu().numpy(), gd["alpha"].cpu().numpy(), nw, nthreads=NTHREADS)
+    _check_pre(g, o, oracle.broadcast_streams(x1), gd, fold=True, rows=rows)
