@@ -502,6 +502,17 @@ def run_ours(args, rank, world, local):
         cpu = {"value": round(tokens / dt, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"first {tokens} of the {T} tokens, pre + post, fp64 oracle, {cores} threads"
                          + (f" ({model})" if model else "")}
+        # the oracle per call at the decode sizes and on a prefill sample, one
+        # thread and every core (context for the GPU numbers, not a target)
+        by_t = {}
+        for Tc in (16, 128):
+            dc = seam_inputs(Tc, seed=Tc, fold=True, with_y=True)
+            r = {}
+            for th in (1, cores):
+                r[f"us_per_call_{th}_threads"] = round(time_oracle_sample(dc, Tc, th) * 1e6, 1)
+            by_t[str(Tc)] = r
+        by_t[str(T) + "_sample_64"] = {"tokens_per_s_1_thread": round(64 / time_oracle_sample(d, 64, 1), 1)}
+        cpu["by_T"] = by_t
 
     line = {
         "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world,
