@@ -254,6 +254,42 @@ mhc_status mhc_post_broadcast(const uint16_t *x, const uint16_t *y, const float 
                               const float *post, int64_t T, int n, int C, uint16_t *x_new,
                               void *stream);
 
+/*
+ * mhc_seam_host -- one seam, the delayed pre block then the post block on
+ * the same residual (mhc_pre_delayed, then mhc_post with that call's comb
+ * and post), for activations in page-locked HOST memory: the end-to-end call
+ * for a caller whose tokens live on the host.
+ *  x_h [T, n, C] bf16, y_h [T, C] bf16, pre_in_h [T, n] fp32: HOST inputs.
+ *  fn, bias, alpha, norm_weight: DEVICE weights, as mhc_pre_delayed.
+ *  x_new_h [T, n, C] bf16, pre_out_h [T, n] fp32: HOST outputs (required);
+ *  post_out_h [T, n], comb_out_h [T, n, n] fp32 and layer_input_h [T, C]
+ *  bf16: HOST outputs, each optional (NULL: not copied back).
+ *  Every host pointer must be page-locked (cudaHostAlloc / cudaHostRegister):
+ *  MHC_ERR_INVALID_ARGUMENT otherwise.  x_new_h may be exactly x_h; no other
+ *  host ranges may overlap.
+ *  workspace: DEVICE, 256-byte aligned, at least
+ *  mhc_seam_host_workspace_bytes(T, n, C) bytes (two chunks of device copies
+ *  of the activations plus the pre block's workspace); owned by the caller,
+ *  and calls that share one must be ordered on the same stream.
+ * The tokens go in chunks (1024 tokens from 2048 on; one chunk below 512;
+ * no chunk under 256 tokens, so every chunk takes the kernel the whole call
+ * would): chunk k's kernels run on `stream` while chunk k+1 is copied in and
+ * chunk k-1 copied out on two library-owned streams (created once per
+ * device).  The outputs are bit-identical to mhc_pre_delayed + mhc_post on
+ * device copies.  Asynchronous: the host outputs are complete when `stream`
+ * reaches the point after this call; capturable in a CUDA graph (the
+ * library streams fork from and join back to `stream`).  Host enqueue is
+ * serialised by a process-wide lock.  Errors as mhc_pre_delayed.
+ */
+size_t mhc_seam_host_workspace_bytes(int64_t T, int n, int C);
+mhc_status mhc_seam_host(const uint16_t *x_h, const uint16_t *y_h, const float *pre_in_h,
+                         const float *fn, const float *bias, const float *alpha,
+                         const uint16_t *norm_weight, int64_t T, int n, int C,
+                         int sinkhorn_iters, float rms_eps, float norm_eps, float sinkhorn_eps,
+                         uint16_t *x_new_h, float *pre_out_h, float *post_out_h,
+                         float *comb_out_h, uint16_t *layer_input_h, void *workspace,
+                         size_t workspace_bytes, void *stream);
+
 /* Static description of the status code (never NULL). */
 const char *mhc_status_string(mhc_status status);
 

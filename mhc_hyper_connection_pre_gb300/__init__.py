@@ -74,6 +74,11 @@ def load_library():
         lib.mhc_pre_broadcast.restype = I
         lib.mhc_post_broadcast.argtypes = lib.mhc_post.argtypes
         lib.mhc_post_broadcast.restype = I
+        lib.mhc_seam_host_workspace_bytes.argtypes = [I64, I, I]
+        lib.mhc_seam_host_workspace_bytes.restype = ctypes.c_size_t
+        lib.mhc_seam_host.argtypes = [P, P, P, P, P, P, P, I64, I, I, I, F, F, F, P, P, P, P, P, P,
+                                      ctypes.c_size_t, P]
+        lib.mhc_seam_host.restype = I
         lib.mhc_status_string.argtypes = [I]
         lib.mhc_status_string.restype = ctypes.c_char_p
         lib.mhc_pre_delayed_plan.argtypes = [I64, I, I, P, P, P, P]
@@ -370,6 +375,62 @@ def post_broadcast(x: torch.Tensor, y: torch.Tensor, comb: torch.Tensor, post_ga
     if out is None:
         out = torch.empty(T, n, C, dtype=torch.bfloat16, device=x.device)
     return _post_call("mhc_post_broadcast", x, y, comb, post_gate, T, n, C, out, stream)
+
+
+def _host_ptr(t: torch.Tensor | None, name: str, dtype: torch.dtype) -> int | None:
+    if t is None:
+        return None
+    if t.device.type != "cpu" or not t.is_pinned():
+        raise ValueError(f"{name} must be a page-locked (pinned) host tensor")
+    if t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor")
+    return t.data_ptr()
+
+
+def seam_host(x: torch.Tensor, y: torch.Tensor, pre_in: torch.Tensor, fn: torch.Tensor, bias: torch.Tensor,
+              alpha: torch.Tensor, norm_weight: torch.Tensor | None = None, *, sinkhorn_iters: int = SINKHORN_ITERS,
+              rms_eps: float = 1e-6, norm_eps: float = 1e-6, sinkhorn_eps: float = 1e-6, out: dict | None = None,
+              outputs: tuple = ("x_new", "pre"), workspace: torch.Tensor | None = None, device=None,
+              stream=None) -> dict:
+    """One seam on pinned HOST activations (``mhc_seam_host``): the delayed
+    pre block, then the post block, with the chunked copies and kernels
+    overlapped inside the library.  x bf16 [T, 4, C], y bf16 [T, C], pre_in
+    fp32 [T, 4] (pinned host); fn, bias, alpha, norm_weight on the device.
+    Returns pinned host tensors {"x_new", "pre"[, "post", "comb",
+    "layer_input"]} (``outputs`` names the optional ones to copy back;
+    ``out`` may supply them)."""
+    lib = load_library()
+    if x.dim() != 3:
+        raise ValueError("x must be [T, n, C]")
+    T, n, C = x.shape
+    dev = fn.device if device is None else torch.device(device)
+    o = dict(out) if out else {}
+    shapes = {"x_new": ((T, n, C), torch.bfloat16), "pre": ((T, n), torch.float32),
+              "post": ((T, n), torch.float32), "comb": ((T, n, n), torch.float32),
+              "layer_input": ((T, C), torch.bfloat16)}
+    for k in ("x_new", "pre") + tuple(k for k in outputs if k not in ("x_new", "pre")):
+        if k not in o:
+            shp, dt = shapes[k]
+            o[k] = torch.empty(shp, dtype=dt, pin_memory=True)
+    if workspace is None:
+        need = int(lib.mhc_seam_host_workspace_bytes(T, n, C))
+        key = ("seam_host", dev.index if dev.index is not None else torch.cuda.current_device())
+        workspace = _workspaces.get(key)
+        if workspace is None or workspace.numel() < need:
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+            _workspaces[key] = workspace
+    st = lib.mhc_seam_host(
+        _host_ptr(x, "x", torch.bfloat16), _host_ptr(y, "y", torch.bfloat16),
+        _host_ptr(pre_in, "pre_in", torch.float32), _dev_ptr(fn, "fn", torch.float32, dev),
+        _dev_ptr(bias, "bias", torch.float32, dev), _dev_ptr(alpha, "alpha", torch.float32, dev),
+        _dev_ptr(norm_weight, "norm_weight", torch.bfloat16, dev), T, n, C, int(sinkhorn_iters), float(rms_eps),
+        float(norm_eps), float(sinkhorn_eps), _host_ptr(o["x_new"], "x_new", torch.bfloat16),
+        _host_ptr(o["pre"], "pre", torch.float32), _host_ptr(o.get("post"), "post", torch.float32),
+        _host_ptr(o.get("comb"), "comb", torch.float32),
+        _host_ptr(o.get("layer_input"), "layer_input", torch.bfloat16),
+        _dev_ptr(workspace, "workspace", torch.uint8, dev), workspace.numel(), _stream_ptr(stream, dev))
+    _check("mhc_seam_host", st)
+    return o
 
 
 def device_status() -> int:

@@ -193,3 +193,34 @@ def test_broadcast_entry_points_size_x_as_t_by_c(lib):
     post["x_new"] = just_past
     assert _post(lib, x_new=just_past) == INVALID
     assert lib.mhc_post_broadcast(*post.values()) == CUDA_ERR
+
+
+def _seam_host(lib, **kw):
+    args = dict(x=A, y=A + 0x1000000, pre_in=A + 0x2000000, fn=A + 0x3000000, bias=A + 0x4000000,
+                alpha=A + 0x4001000, norm_weight=None, T=16, n=4, C=5120, iters=20, rms_eps=1e-6, norm_eps=1e-6,
+                sk_eps=1e-6, x_new=A + 0x5000000, pre_out=A + 0x6000000, post_out=None, comb_out=None,
+                layer_input=None, workspace=A + 0x7000000, workspace_bytes=1 << 30,
+                stream=None)
+    args.update(kw)
+    return lib.mhc_seam_host(*args.values())
+
+
+def test_seam_host_rejects_on_the_host(lib):
+    """mhc_seam_host checks shapes, pointers, host overlaps, the workspace
+    and page-locked host memory before touching a device (here there is
+    none: memory that is not page-locked is what every fake address is)."""
+    assert _seam_host(lib, T=0, x=None) == OK
+    assert _seam_host(lib, n=3) == UNSUPPORTED
+    assert _seam_host(lib, C=100) == UNSUPPORTED
+    assert _seam_host(lib, T=-1) == INVALID
+    assert _seam_host(lib, x=None) == INVALID
+    assert _seam_host(lib, pre_out=None) == INVALID
+    assert _seam_host(lib, workspace=None) == INVALID
+    assert _seam_host(lib, x_new=A + 0x100) == INVALID            # partial overlap with x
+    assert _seam_host(lib, pre_out=A + 0x1000000) == INVALID      # inside y
+    assert _seam_host(lib, workspace=A + 0x7000010) == INVALID    # not 256-byte aligned
+    assert _seam_host(lib, workspace_bytes=16) == INVALID         # too small
+    assert _seam_host(lib) == INVALID                             # not page-locked
+    assert lib.mhc_seam_host_workspace_bytes(0, 4, 5120) == 0
+    assert lib.mhc_seam_host_workspace_bytes(16, 3, 5120) == 0
+    assert lib.mhc_seam_host_workspace_bytes(16, 4, 5120) > 16 * 4 * 5120 * 2

@@ -696,3 +696,55 @@ def test_entry_points_full_size_properties():
     o = oracle.pre_delayed_broadcast(x1, gd["pre_in"].cpu().numpy()[rows], gd["fn"].cpu().numpy(),
                                      gd["bias"].cpu().numpy(), gd["alpha"].cpu().numpy(), nw, nthreads=NTHREADS)
     _check_pre(g, o, oracle.broadcast_streams(x1), gd, fold=True, rows=rows)
+
+
+def _pinned(t):
+    return t.cpu().pin_memory()
+
+
+@pytest.mark.parametrize("T", [1, 100, 300, 1000, 4097, 16384])
+def test_seam_host_is_bit_identical_to_the_device_calls(T):
+    """mhc_seam_host on pinned host activations (chunked, copies and kernels
+    on three streams) gives the bits of mhc_pre_delayed + mhc_post on device
+    copies: one chunk below 512 tokens, two chunks (384 + 616) at 1000,
+    1024-token chunks with the remainder joined to the last at 4097 and
+    16384."""
+    gd = seam_inputs(T, seed=2300 + T, fold=True, with_y=True, device="cuda")
+    ref = mhc.pre_delayed(gd["x"], gd["pre_in"], gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"])
+    xn_ref = mhc.post(gd["x"], gd["y"], ref["comb"], ref["post"])
+    hx, hy, hp = _pinned(gd["x"]), _pinned(gd["y"]), _pinned(gd["pre_in"])
+    got = mhc.seam_host(hx, hy, hp, gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"],
+                        outputs=("x_new", "pre", "post", "comb", "layer_input"))
+    torch.cuda.synchronize()
+    assert mhc.device_status() == 0
+    assert torch.equal(got["x_new"], xn_ref.cpu())
+    for k in ("pre", "post", "comb", "layer_input"):
+        assert torch.equal(got[k], ref[k].cpu()), k
+
+
+def test_seam_host_in_place_and_in_a_graph():
+    """x_new may be the input buffer itself; the call captures into a CUDA
+    graph (the library's copy streams fork from and join the capturing
+    stream) and replays to the same bits."""
+    T = 1000
+    gd = seam_inputs(T, seed=2400, fold=True, with_y=True, device="cuda")
+    ref = mhc.pre_delayed(gd["x"], gd["pre_in"], gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"])
+    xn_ref = mhc.post(gd["x"], gd["y"], ref["comb"], ref["post"]).cpu()
+    hy, hp = _pinned(gd["y"]), _pinned(gd["pre_in"])
+    hx = _pinned(gd["x"])
+    got = mhc.seam_host(hx, hy, hp, gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"], out={"x_new": hx})
+    torch.cuda.synchronize()
+    assert torch.equal(hx, xn_ref)
+    assert torch.equal(got["pre"], ref["pre"].cpu())
+    hx2 = _pinned(gd["x"])
+    out = {"x_new": torch.empty_like(hx2).pin_memory(), "pre": torch.empty(T, 4).pin_memory()}
+    s = torch.cuda.Stream()
+    g = SeamGraph(lambda st: mhc.seam_host(hx2, hy, hp, gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"],
+                                           out=out, stream=st), s)
+    out["x_new"].zero_()
+    g.replay(2)
+    s.synchronize()
+    assert mhc.device_status() == 0
+    assert torch.equal(out["x_new"], xn_ref)
+    assert torch.equal(out["pre"], ref["pre"].cpu())
+    g.close()
