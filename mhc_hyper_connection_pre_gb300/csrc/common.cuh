@@ -135,22 +135,37 @@ __device__ __forceinline__ float rcp_approx(float x) {
 // iterations 2..iters normalise rows then columns.  One thread; the chain of
 // 2*iters dependent normalisations is the latency, so each one multiplies by
 // one reciprocal of the sum.
+__device__ __forceinline__ void sinkhorn_rows(float (&P)[16]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float inv = rcp_approx(((P[4 * i] + P[4 * i + 1]) + P[4 * i + 2]) + P[4 * i + 3]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) P[4 * i + j] *= inv;
+    }
+}
+__device__ __forceinline__ void sinkhorn_cols(float (&P)[16]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float inv = rcp_approx(((P[j] + P[4 + j]) + P[8 + j]) + P[12 + j]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) P[4 * i + j] *= inv;
+    }
+}
 __device__ __forceinline__ void sinkhorn_iterations(float (&P)[16], int iters) {
-    for (int it = 0; it < iters; ++it) {
-        if (it > 0) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float inv = rcp_approx(((P[4 * i] + P[4 * i + 1]) + P[4 * i + 2]) + P[4 * i + 3]);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) P[4 * i + j] *= inv;
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float inv = rcp_approx(((P[j] + P[4 + j]) + P[8 + j]) + P[12 + j]);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) P[4 * i + j] *= inv;
-        }
+    sinkhorn_cols(P);
+    // two iterations per loop body: less loop overhead, and a body small
+    // enough to stay in the instruction cache (the kernels run this chain
+    // once per token, so a fully unrolled one is fetched cold every call)
+    int it = 1;
+    for (; it + 1 < iters; it += 2) {
+        sinkhorn_rows(P);
+        sinkhorn_cols(P);
+        sinkhorn_rows(P);
+        sinkhorn_cols(P);
+    }
+    if (it < iters) {
+        sinkhorn_rows(P);
+        sinkhorn_cols(P);
     }
 }
 
