@@ -130,43 +130,40 @@ __device__ __forceinline__ float rcp_approx(float x) {
     return r;
 }
 
-// Sinkhorn on a 4x4 row-major matrix that already holds iteration 1's row
+// Sinkhorn on a 4x4 row-major matrix A that already holds iteration 1's row
 // softmax plus eps: iteration 1 finishes with a column normalisation,
-// iterations 2..iters normalise rows then columns.  One thread; the chain of
-// 2*iters dependent normalisations is the latency, so each one multiplies by
-// one reciprocal of the sum.
-__device__ __forceinline__ void sinkhorn_rows(float (&P)[16]) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float inv = rcp_approx(((P[4 * i] + P[4 * i + 1]) + P[4 * i + 2]) + P[4 * i + 3]);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) P[4 * i + j] *= inv;
-    }
-}
-__device__ __forceinline__ void sinkhorn_cols(float (&P)[16]) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const float inv = rcp_approx(((P[j] + P[4 + j]) + P[8 + j]) + P[12 + j]);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) P[4 * i + j] *= inv;
-    }
-}
+// iterations 2..iters normalise rows then columns.  One thread.  The matrix
+// is carried as P_ij = A_ij R_i C_j: a row normalisation sets
+// R_i = 1 / sum_j A_ij C_j, a column one C_j = 1 / sum_i A_ij R_i, and P is
+// formed once at the end -- the same normalisations in exact arithmetic,
+// with a shorter dependent chain per step than rescaling all 16 entries.
+// The 2*iters steps are one dependent chain; two iterations per loop body
+// keep the loop overhead low and the body small enough for the instruction
+// cache (the kernels run the chain once per token: a fully unrolled chain
+// is fetched cold every call and was slower in them).
 __device__ __forceinline__ void sinkhorn_iterations(float (&P)[16], int iters) {
-    sinkhorn_cols(P);
-    // two iterations per loop body: less loop overhead, and a body small
-    // enough to stay in the instruction cache (the kernels run this chain
-    // once per token, so a fully unrolled one is fetched cold every call)
+    float R[4] = {1.f, 1.f, 1.f, 1.f}, Cs[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) Cs[j] = rcp_approx(((P[j] + P[4 + j]) + P[8 + j]) + P[12 + j]);
+    auto iteration = [&]() {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            R[i] = rcp_approx(
+                fmaf(P[4 * i + 3], Cs[3], fmaf(P[4 * i + 2], Cs[2], fmaf(P[4 * i + 1], Cs[1], P[4 * i] * Cs[0]))));
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            Cs[j] = rcp_approx(fmaf(P[12 + j], R[3], fmaf(P[8 + j], R[2], fmaf(P[4 + j], R[1], P[j] * R[0]))));
+    };
     int it = 1;
     for (; it + 1 < iters; it += 2) {
-        sinkhorn_rows(P);
-        sinkhorn_cols(P);
-        sinkhorn_rows(P);
-        sinkhorn_cols(P);
+        iteration();
+        iteration();
     }
-    if (it < iters) {
-        sinkhorn_rows(P);
-        sinkhorn_cols(P);
-    }
+    if (it < iters) iteration();
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) P[4 * i + j] = (P[4 * i + j] * R[i]) * Cs[j];
 }
 
 // Per-token gates and comb from the 2n+n^2 logits, in fp32, by one thread.
