@@ -30,7 +30,7 @@ cudaError_t launch_pre_tc(const uint16_t* x, const float* pre_in, const float* f
                           const float* alpha, const uint16_t* norm_w, int64_t T, int C, int iters,
                           float rms_eps, float norm_eps, float sk_eps, float* pre_out, float* post_out,
                           float* comb_out, uint16_t* layer_input, float* logits_out, void* workspace,
-                          cudaStream_t stream, int max_clusters, bool broadcast);
+                          cudaStream_t stream, int max_clusters, bool broadcast, bool gates_only);
 cudaError_t read_device_status(unsigned int* status);
 cudaError_t read_decode_status(unsigned int* status);
 }  // namespace mhc
@@ -245,17 +245,17 @@ mhc_status pre_entry(const uint16_t* x, const float* pre_in, const float* fn, co
             if (workspace_bytes < need || (need && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))))
                 return MHC_ERR_INVALID_ARGUMENT;
             if (nondelayed) {
-                // pass 1: the gates (its collapse, with an arbitrary pre-mix,
-                // is overwritten); pass 2: the delayed block with pre_in = the
-                // pre-mix of pass 1, which reproduces the gates bit for bit
+                // pass 1: the gates only (no collapse, fold or layer_input);
+                // pass 2: the delayed block with pre_in = the pre-mix of pass
+                // 1, which reproduces the gates bit for bit
                 float* pre1 = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + planes);
                 cudaError_t e = mhc::launch_pre_tc(x, pre1, fn, bias, alpha, norm_weight, T, C, sinkhorn_iters,
                                                    rms_eps, norm_eps, sinkhorn_eps, pre1, post_out, comb_out,
-                                                   layer_input, logits_out, workspace, s, tcc, bcast);
+                                                   layer_input, logits_out, workspace, s, tcc, bcast, true);
                 if (e == cudaSuccess)
                     e = mhc::launch_pre_tc(x, pre1, fn, bias, alpha, norm_weight, T, C, sinkhorn_iters, rms_eps,
                                            norm_eps, sinkhorn_eps, pre_out, post_out, comb_out, layer_input,
-                                           logits_out, workspace, s, tcc, bcast);
+                                           logits_out, workspace, s, tcc, bcast, false);
                 return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA;
             }
             const uint16_t* xin = x;
@@ -268,7 +268,7 @@ mhc_status pre_entry(const uint16_t* x, const float* pre_in, const float* fn, co
             }
             cudaError_t e = mhc::launch_pre_tc(xin, pre_in, fn, bias, alpha, norm_weight, T, C, sinkhorn_iters,
                                                rms_eps, norm_eps, sinkhorn_eps, pre_out, post_out, comb_out,
-                                               layer_input, logits_out, workspace, s, tcc, bcast);
+                                               layer_input, logits_out, workspace, s, tcc, bcast, false);
             return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA;
         }
     }

@@ -40,6 +40,9 @@
 //   warp 10    finalizer: for its 8 tokens of the tile sums the 16 CTAs'
 //              partials in rank order, pushes the fold scale to all 16 CTAs,
 //              then logits, gates and the Sinkhorn comb in registers.
+// A gates-only instance (GATES) serves the first of the non-delayed block's
+// two passes: the token rows only sum x^2 (in the same order, so the gates
+// are the same bits), with no collapse, fold or layer_input.
 // The model-entry broadcast seam (x is [T][C], the same for all four
 // streams) brings one x box per stage, which the MMA and the collapse read
 // as every stream: the same operands, so the same bits as the four-stream
@@ -148,7 +151,7 @@ __device__ __forceinline__ void split3(const float (&w)[8], uint32_t (&pk)[3][4]
     }
 }
 
-template <bool BCAST>
+template <bool BCAST, bool GATES>
 __global__ void __launch_bounds__(kThreads, 1)
 pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap omap, const Args a) {
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -414,6 +417,15 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
+                if (GATES) {
+                    // gates only: the sum of squares in the same order as
+                    // below (the same RMS scale, so the same gates)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+#pragma unroll
+                        for (int st = 0; st < 4; ++st) sx2 = fma_rn2(xv[st][e], xv[st][e], sx2);
+                    continue;
+                }
                 // collapse in scalar fp32, every product and sum rounded on its
                 // own, stream order (the bit-exact reference order); the sums
                 // of squares use the packed pipe in a fixed order
@@ -464,7 +476,7 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
             // this group's sums go out first: the finalizer needs only Σh² for
             // the fold scale, which gates every CTA's next tile
             st_async_v2(sq_dst, sx, sh, sq_bar);
-            if (fold) tmem_wait_st();
+            if (fold && !GATES) tmem_wait_st();
 
             if (grpsel == 0) {
                 // accumulated projection of this CTA's K-slice for the token
@@ -506,7 +518,7 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
             named_bar_sync(1, 32 * kRowWarps);
             tc_fence_after();
         }
-        if (fold && have_prev) {
+        if (fold && !GATES && have_prev) {
             // flush the last tile: this warp's share of the column groups
             for (int grp = grpsel; grp < ngroups; grp += 2) store_folded(grp);
         }
@@ -638,7 +650,8 @@ int pre_tc_tile_tokens() { return tc::kTile; }
 // attributes, then the number of co-resident 16-CTA clusters (0 on error).
 int pre_tc_prepare() {
     cudaError_t e = cudaSuccess;
-    for (auto k : {tc::pre_tc_kernel<false>, tc::pre_tc_kernel<true>}) {
+    for (auto k : {tc::pre_tc_kernel<false, false>, tc::pre_tc_kernel<true, false>, tc::pre_tc_kernel<false, true>,
+                   tc::pre_tc_kernel<true, true>}) {
         if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemBytes);
     }
@@ -655,7 +668,7 @@ int pre_tc_prepare() {
     cfg.gridDim = dim3(tc::kCtas, 1, 1);
     cfg.dynamicSmemBytes = tc::kSmemBytes;
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, tc::pre_tc_kernel<false>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&n, tc::pre_tc_kernel<false, false>, &cfg);
     return e == cudaSuccess ? n : 0;
 }
 
@@ -663,7 +676,7 @@ cudaError_t launch_pre_tc(const uint16_t* x, const float* pre_in, const float* f
                           const float* alpha, const uint16_t* norm_w, int64_t T, int C, int iters,
                           float rms_eps, float norm_eps, float sk_eps, float* pre_out, float* post_out,
                           float* comb_out, uint16_t* layer_input, float* logits_out, void* workspace,
-                          cudaStream_t stream, int max_clusters, bool broadcast) {
+                          cudaStream_t stream, int max_clusters, bool broadcast, bool gates_only) {
     PFN_encodeTiled enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     // x viewed as [T][4][C] bf16 (broadcast: [T][1][C], every stream's box
@@ -710,8 +723,11 @@ cudaError_t launch_pre_tc(const uint16_t* x, const float* pre_in, const float* f
     cfg.gridDim = dim3((unsigned)(nclusters * tc::kCtas), 1, 1);
     cfg.dynamicSmemBytes = tc::kSmemBytes;
     cfg.stream = stream;
-    return broadcast ? cudaLaunchKernelEx(&cfg, tc::pre_tc_kernel<true>, map, omap, a)
-                     : cudaLaunchKernelEx(&cfg, tc::pre_tc_kernel<false>, map, omap, a);
+    if (gates_only)
+        return broadcast ? cudaLaunchKernelEx(&cfg, tc::pre_tc_kernel<true, true>, map, omap, a)
+                         : cudaLaunchKernelEx(&cfg, tc::pre_tc_kernel<false, true>, map, omap, a);
+    return broadcast ? cudaLaunchKernelEx(&cfg, tc::pre_tc_kernel<true, false>, map, omap, a)
+                     : cudaLaunchKernelEx(&cfg, tc::pre_tc_kernel<false, false>, map, omap, a);
 }
 
 // Host read-and-clear of the device status word (synchronous).
