@@ -220,42 +220,43 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
     if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
 
     // ---- fn K-slice -> three bf16 planes in the operand layout, written to
-    //      this CTA's workspace region; every thread first loads all of its
-    //      items (one latency), then splits and stores them.
+    //      this CTA's workspace region.  Items of 8 columns; a warp takes
+    //      units of 8 rows x 4 neighbouring column chunks (lane = row * 4 +
+    //      chunk), so that a load covers 8 runs of 128 contiguous bytes of fn
+    //      and a plane store two whole 256-byte row atoms; every thread first
+    //      loads all of its items (one latency), then splits and stores them.
     {
-        constexpr int kItemsMax = 6;   // ceil(24 * 4 * 20 / 352)
-        float w[kItemsMax][2][8];
-        int nitems = 0;
+        constexpr int kUnitsMax = 11;   // ceil(4 streams x 10 chunk quads x 3 row octets / 11 warps)
+        const int nunits = 4 * ((ngroups + 1) / 2) * 3;   // an odd last chunk quad is half empty
+        const int mrow = lane >> 2, gc = lane & 3;
+        float w[kUnitsMax][8];
 #pragma unroll
-        for (int j = 0; j < kItemsMax; ++j) {
-            const int idx = tid + j * kThreads;
-            if (idx < 24 * 4 * ngroups) {
-                const int m = idx % 24, rest = idx / 24, s = rest & 3, g = rest >> 2;
-                const float4* src = reinterpret_cast<const float4*>(a.fn + (int64_t)m * K + (int64_t)s * C +
-                                                                    c0 + kCols * g);
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const float4 u = __ldg(src + 2 * c), v = __ldg(src + 2 * c + 1);
-                    w[j][c][0] = u.x; w[j][c][1] = u.y; w[j][c][2] = u.z; w[j][c][3] = u.w;
-                    w[j][c][4] = v.x; w[j][c][5] = v.y; w[j][c][6] = v.z; w[j][c][7] = v.w;
-                }
-                nitems = j + 1;
+        for (int j = 0; j < kUnitsMax; ++j) {
+            const int u = warp + j * (kThreads / 32);
+            if (u < nunits) {
+                const int mo = u % 3, rest = u / 3, st = rest & 3, gp = rest >> 2;
+                const int m = 8 * mo + mrow, g = 2 * gp + (gc >> 1), c = gc & 1;
+                if (g >= ngroups) continue;
+                const float4* src = reinterpret_cast<const float4*>(a.fn + (int64_t)m * K + (int64_t)st * C + c0 +
+                                                                    kCols * g + 8 * c);
+                const float4 u0 = __ldg(src), u1 = __ldg(src + 1);
+                w[j][0] = u0.x; w[j][1] = u0.y; w[j][2] = u0.z; w[j][3] = u0.w;
+                w[j][4] = u1.x; w[j][5] = u1.y; w[j][6] = u1.z; w[j][7] = u1.w;
             }
         }
 #pragma unroll
-        for (int j = 0; j < kItemsMax; ++j) {
-            if (j < nitems) {
-                const int idx = tid + j * kThreads;
-                const int m = idx % 24, rest = idx / 24, s = rest & 3, g = rest >> 2;
+        for (int j = 0; j < kUnitsMax; ++j) {
+            const int u = warp + j * (kThreads / 32);
+            if (u < nunits) {
+                const int mo = u % 3, rest = u / 3, st = rest & 3, gp = rest >> 2;
+                const int m = 8 * mo + mrow, g = 2 * gp + (gc >> 1), c = gc & 1;
+                if (g >= ngroups) continue;
+                uint32_t pk[3][4];
+                split3(w[j], pk);
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t pk[3][4];
-                    split3(w[j][c], pk);
-#pragma unroll
-                    for (int p = 0; p < 3; ++p)
-                        *reinterpret_cast<uint4*>(wreg + w_off(g, s, p * 24 + m, c)) =
-                            make_uint4(pk[p][0], pk[p][1], pk[p][2], pk[p][3]);
-                }
+                for (int p = 0; p < 3; ++p)
+                    *reinterpret_cast<uint4*>(wreg + w_off(g, st, p * 24 + m, c)) =
+                        make_uint4(pk[p][0], pk[p][1], pk[p][2], pk[p][3]);
             }
         }
     }
