@@ -348,17 +348,22 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
         unsigned char* ostage = smem + kOffOut + (warp - 2) * (32 * kCols * 2);
         const int oo0 = (lane >> 3) * 256 + sw32_off(lane & 7, 0);
         const int oo1 = (lane >> 3) * 256 + sw32_off(lane & 7, 1);
-        auto store_out = [&](const f32x2 (&o)[8], int col, int64_t row0) {
-            if (lane == 0) bulk_wait_read_all();   // the previous store has read the tile
-            __syncwarp();
-            *reinterpret_cast<uint4*>(ostage + oo0) = make_uint4(f32x2_to_bf16x2(o[0]), f32x2_to_bf16x2(o[1]),
-                                                                 f32x2_to_bf16x2(o[2]), f32x2_to_bf16x2(o[3]));
-            *reinterpret_cast<uint4*>(ostage + oo1) = make_uint4(f32x2_to_bf16x2(o[4]), f32x2_to_bf16x2(o[5]),
-                                                                 f32x2_to_bf16x2(o[6]), f32x2_to_bf16x2(o[7]));
+        // stg: the warp's own staging tile (reused: wait for the previous
+        // store to have read it), or a fresh one (no wait)
+        auto store_out = [&](const f32x2 (&o)[8], int col, int64_t row0, unsigned char* stg = nullptr) {
+            if (!stg) {
+                if (lane == 0) bulk_wait_read_all();   // the previous store has read the tile
+                __syncwarp();
+                stg = ostage;
+            }
+            *reinterpret_cast<uint4*>(stg + oo0) = make_uint4(f32x2_to_bf16x2(o[0]), f32x2_to_bf16x2(o[1]),
+                                                              f32x2_to_bf16x2(o[2]), f32x2_to_bf16x2(o[3]));
+            *reinterpret_cast<uint4*>(stg + oo1) = make_uint4(f32x2_to_bf16x2(o[4]), f32x2_to_bf16x2(o[5]),
+                                                              f32x2_to_bf16x2(o[6]), f32x2_to_bf16x2(o[7]));
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0 && row0 < a.T) {
-                tma_store_2d(&omap, ostage, col, (int)row0);
+                tma_store_2d(&omap, stg, col, (int)row0);
                 bulk_commit_group();
             }
         };
@@ -368,7 +373,7 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
         bool have_prev = false;
         int64_t t_prev = 0;
         float sc_prev = 1.f;
-        auto store_folded = [&](int grp) {
+        auto store_folded = [&](int grp, unsigned char* stg = nullptr) {
             uint32_t r[16];
             tmem_ld16(tl + kHCol + kCols * grp, r);
             tmem_wait_ld();
@@ -386,7 +391,7 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
                     o[4 * c + e] = mul_rn2(mul_rn2(hv, sc2), bf16x2_to_f32x2(ww[e]));   // (h * s) * w
                 }
             }
-            store_out(o, c0 + kCols * grp, t_prev - lane);
+            store_out(o, c0 + kCols * grp, t_prev - lane, stg);
         };
         uint32_t g = 0;
         int it = 0;
@@ -520,8 +525,13 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
             tc_fence_after();
         }
         if (fold && !GATES && have_prev) {
-            // flush the last tile: this warp's share of the column groups
-            for (int grp = grpsel; grp < ngroups; grp += 2) store_folded(grp);
+            // flush the last tile: this warp's share of the column groups,
+            // each through its own staging tile in the now idle ring (every
+            // load has landed and, past the tile-end barrier, every MMA that
+            // read the ring has completed), so no store waits for another
+            unsigned char* fstage = stages + (warp - 2) * ((kMaxGroups + 1) / 2) * (32 * kCols * 2);
+            for (int grp = grpsel, k = 0; grp < ngroups; grp += 2, ++k)
+                store_folded(grp, fstage + k * (32 * kCols * 2));
         }
         if (lane == 0) bulk_wait_all();   // stores complete before the CTA exits
     } else {
