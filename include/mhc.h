@@ -290,6 +290,40 @@ mhc_status mhc_seam_host(const uint16_t *x_h, const uint16_t *y_h, const float *
                          float *comb_out_h, uint16_t *layer_input_h, void *workspace,
                          size_t workspace_bytes, void *stream);
 
+/*
+ * Pre-packed weights for the tensor-core path (from 256 tokens).  fn is a
+ * weight: the tensor-core kernel otherwise converts it, at the start of every
+ * call, into three exact bf16 planes (fn = hi + mid + lo) in its MMA operand
+ * layout, one copy per 16-CTA cluster in the workspace.  Packed once, the
+ * planes are read by every cluster from one shared copy and the per-call
+ * conversion disappears.
+ *
+ * mhc_pre_packed_bytes -- size of the packed planes for (n, C): 16 regions
+ *   of C/256 x 9 KB (2.95 MB at C = 5120); 0 when the tensor-core kernel does
+ *   not take C (C a multiple of 256 up to 5120, n == 4).  Host only.
+ * mhc_pre_pack -- write the planes of fn [2n+n^2, n*C] fp32 (device) to
+ *   packed (device, 256-byte aligned, at least mhc_pre_packed_bytes; must not
+ *   overlap fn).  One kernel on `stream`.  The planes stay valid while fn
+ *   is unchanged: re-pack after writing fn.  MHC_ERR_UNSUPPORTED for a C the
+ *   tensor-core kernel does not take.
+ * mhc_pre_delayed_packed -- mhc_pre_delayed with the planes packed ahead:
+ *   bit-identical outputs.  fn (device) is still required, for calls under
+ *   256 tokens (the cluster kernel reads fn directly); packed, packed_bytes
+ *   as written by mhc_pre_pack for the same fn and C.  No workspace.
+ *   Errors as mhc_pre_delayed; MHC_ERR_INVALID_ARGUMENT for a NULL,
+ *   misaligned or short packed buffer, or a C without packed planes.
+ */
+size_t mhc_pre_packed_bytes(int n, int C);
+mhc_status mhc_pre_pack(const float *fn, int n, int C, void *packed, size_t packed_bytes,
+                        void *stream);
+mhc_status mhc_pre_delayed_packed(const uint16_t *x, const float *pre_in, const float *fn,
+                                  const void *packed, size_t packed_bytes, const float *bias,
+                                  const float *alpha, const uint16_t *norm_weight, int64_t T,
+                                  int n, int C, int sinkhorn_iters, float rms_eps,
+                                  float norm_eps, float sinkhorn_eps, float *pre_out,
+                                  float *post_out, float *comb_out, uint16_t *layer_input,
+                                  float *logits_out, void *stream);
+
 /* Static description of the status code (never NULL). */
 const char *mhc_status_string(mhc_status status);
 

@@ -74,6 +74,13 @@ def load_library():
         lib.mhc_pre_broadcast.restype = I
         lib.mhc_post_broadcast.argtypes = lib.mhc_post.argtypes
         lib.mhc_post_broadcast.restype = I
+        lib.mhc_pre_packed_bytes.argtypes = [I, I]
+        lib.mhc_pre_packed_bytes.restype = ctypes.c_size_t
+        lib.mhc_pre_pack.argtypes = [P, I, I, P, ctypes.c_size_t, P]
+        lib.mhc_pre_pack.restype = I
+        lib.mhc_pre_delayed_packed.argtypes = [P, P, P, P, ctypes.c_size_t, P, P, P, I64, I, I, I, F, F, F,
+                                               P, P, P, P, P, P]
+        lib.mhc_pre_delayed_packed.restype = I
         lib.mhc_seam_host_workspace_bytes.argtypes = [I64, I, I]
         lib.mhc_seam_host_workspace_bytes.restype = ctypes.c_size_t
         lib.mhc_seam_host.argtypes = [P, P, P, P, P, P, P, I64, I, I, I, F, F, F, P, P, P, P, P, P,
@@ -227,6 +234,56 @@ def pre(x: torch.Tensor, fn: torch.Tensor, bias: torch.Tensor, alpha: torch.Tens
     T, n, C = _shape3(x)
     return _pre_call("mhc_pre", x, None, fn, bias, alpha, norm_weight, T, n, C, sinkhorn_iters, rms_eps,
                      norm_eps, sinkhorn_eps, out, return_logits, workspace, stream)
+
+
+def pre_pack(fn: torch.Tensor, n: int = 4, C: int | None = None, *, out: torch.Tensor | None = None,
+             stream=None) -> torch.Tensor:
+    """Pack fn into the tensor-core kernel's bf16 planes (``mhc_pre_pack``);
+    returns the uint8 device buffer for ``pre_delayed_packed``.  Re-pack
+    after writing fn."""
+    lib = load_library()
+    if C is None:
+        C = fn.numel() // ((2 * n + n * n) * n)
+    need = int(lib.mhc_pre_packed_bytes(n, C))
+    if need == 0:
+        raise ValueError(f"no packed planes for n={n}, C={C} (the tensor-core kernel does not take it)")
+    dev = fn.device
+    if out is None:
+        out = torch.empty(need, dtype=torch.uint8, device=dev)
+    st = lib.mhc_pre_pack(_dev_ptr(fn, "fn", torch.float32, dev), n, C, _dev_ptr(out, "packed", torch.uint8, dev),
+                          out.numel(), _stream_ptr(stream, dev))
+    _check("mhc_pre_pack", st)
+    return out
+
+
+def pre_delayed_packed(x: torch.Tensor, pre_in: torch.Tensor, fn: torch.Tensor, packed: torch.Tensor,
+                       bias: torch.Tensor, alpha: torch.Tensor, norm_weight: torch.Tensor | None = None, *,
+                       sinkhorn_iters: int = SINKHORN_ITERS, rms_eps: float = 1e-6, norm_eps: float = 1e-6,
+                       sinkhorn_eps: float = 1e-6, out: dict | None = None, return_logits: bool = False,
+                       stream=None) -> dict:
+    """``pre_delayed`` with fn's planes packed ahead by ``pre_pack``
+    (``mhc_pre_delayed_packed``): the same bits, no per-call conversion, no
+    workspace."""
+    lib = load_library()
+    T, n, C = _shape3(x)
+    dev = x.device
+    M = 2 * n + n * n
+    o = _pre_outputs(dict(out) if out else {}, T, n, C, dev, return_logits)
+    if fn.numel() != M * n * C or bias.numel() != M or alpha.numel() != 3 or pre_in.numel() != T * n:
+        raise ValueError("pre_in / fn / bias / alpha have the wrong number of elements")
+    if norm_weight is not None and norm_weight.numel() != C:
+        raise ValueError("norm_weight must have C elements")
+    st = lib.mhc_pre_delayed_packed(
+        _dev_ptr(x, "x", torch.bfloat16, dev), _dev_ptr(pre_in, "pre_in", torch.float32, dev),
+        _dev_ptr(fn, "fn", torch.float32, dev), _dev_ptr(packed, "packed", torch.uint8, dev), packed.numel(),
+        _dev_ptr(bias, "bias", torch.float32, dev), _dev_ptr(alpha, "alpha", torch.float32, dev),
+        _dev_ptr(norm_weight, "norm_weight", torch.bfloat16, dev), T, n, C, int(sinkhorn_iters), float(rms_eps),
+        float(norm_eps), float(sinkhorn_eps), _dev_ptr(o["pre"], "pre", torch.float32, dev),
+        _dev_ptr(o["post"], "post", torch.float32, dev), _dev_ptr(o["comb"], "comb", torch.float32, dev),
+        _dev_ptr(o["layer_input"], "layer_input", torch.bfloat16, dev),
+        _dev_ptr(o.get("logits"), "logits", torch.float32, dev), _stream_ptr(stream, dev))
+    _check("mhc_pre_delayed_packed", st)
+    return o
 
 
 def pre_delayed_broadcast(x: torch.Tensor, pre_in: torch.Tensor, fn: torch.Tensor, bias: torch.Tensor,

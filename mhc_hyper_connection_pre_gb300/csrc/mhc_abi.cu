@@ -30,7 +30,10 @@ cudaError_t launch_pre_tc(const uint16_t* x, const float* pre_in, const float* f
                           const float* alpha, const uint16_t* norm_w, int64_t T, int C, int iters,
                           float rms_eps, float norm_eps, float sk_eps, float* pre_out, float* post_out,
                           float* comb_out, uint16_t* layer_input, float* logits_out, void* workspace,
-                          cudaStream_t stream, int max_clusters, bool broadcast, bool gates_only);
+                          cudaStream_t stream, int max_clusters, bool broadcast, bool gates_only,
+                          const void* packed);
+size_t pre_tc_packed_bytes(int C);
+cudaError_t launch_pre_tc_pack(const float* fn, int C, void* out, cudaStream_t stream);
 cudaError_t read_device_status(unsigned int* status);
 cudaError_t read_decode_status(unsigned int* status);
 }  // namespace mhc
@@ -195,7 +198,8 @@ mhc_status pre_entry(const uint16_t* x, const float* pre_in, const float* fn, co
                      int sinkhorn_iters, float rms_eps, float norm_eps, float sinkhorn_eps, float* pre_out,
                      float* post_out, float* comb_out, uint16_t* layer_input, float* logits_out, void* workspace,
                      size_t workspace_bytes, void* stream, bool fused, const uint16_t* y, const float* comb_prev,
-                     const float* post_prev, uint16_t* x_new, bool nondelayed = false, bool bcast = false) {
+                     const float* post_prev, uint16_t* x_new, bool nondelayed = false, bool bcast = false,
+                     const void* packed = nullptr, size_t packed_bytes = 0) {
     mhc_status st = check_pre_shape(T, n, C, sinkhorn_iters);
     if (st != MHC_OK) return st;
     if (!(rms_eps >= 0.f) || !(norm_eps >= 0.f) || !(sinkhorn_eps >= 0.f)) return MHC_ERR_INVALID_ARGUMENT;
@@ -212,13 +216,17 @@ mhc_status pre_entry(const uint16_t* x, const float* pre_in, const float* fn, co
         return MHC_ERR_INVALID_ARGUMENT;
     const int M = 2 * n + n * n;
     if (fused && bcast) return MHC_ERR_INVALID_ARGUMENT;
+    if (packed && (fused || bcast || nondelayed)) return MHC_ERR_INVALID_ARGUMENT;
+    if (packed && (!mhc::pre_tc_supports(C) || packed_bytes < mhc::pre_tc_packed_bytes(C) ||
+                   (reinterpret_cast<uintptr_t>(packed) & 255u)))
+        return MHC_ERR_INVALID_ARGUMENT;
     const size_t xb = (size_t)T * (bcast ? 1 : n) * C * 2, pb = (size_t)T * n * 4, cb = (size_t)T * n * n * 4;
     const size_t lib = (size_t)T * C * 2, lob = (size_t)T * M * 4;
     const size_t fnb = (size_t)M * n * C * 4, bb = (size_t)M * 4, ab = 12, nwb = (size_t)C * 2;
     // Exact aliases allowed when fused: x_new == x, comb_out == comb_prev,
     // post_out == post_prev (each is read, for a token, before it is written).
     const Span ins[] = {{x, xb}, {nondelayed ? nullptr : pre_in, pb}, {fn, fnb}, {bias, bb}, {alpha, ab},
-                        {norm_weight, nwb},
+                        {norm_weight, nwb}, {packed, packed_bytes},
                         {fused ? y : nullptr, lib}, {fused ? comb_prev : nullptr, cb},
                         {fused ? post_prev : nullptr, pb}};
     const Span outs[] = {{pre_out, pb}, {post_out, pb}, {comb_out, cb}, {layer_input, lib}, {logits_out, lob},
@@ -240,7 +248,7 @@ mhc_status pre_entry(const uint16_t* x, const float* pre_in, const float* fn, co
     if (use_tc(T, C)) {
         int tcc = tc_clusters(dev);
         if (tcc > 0) {
-            const size_t planes = mhc::pre_tc_workspace_bytes(T, C, tcc);
+            const size_t planes = packed ? 0 : mhc::pre_tc_workspace_bytes(T, C, tcc);
             const size_t need = planes + (nondelayed ? nondelayed_scratch_bytes(T) : 0);
             if (workspace_bytes < need || (need && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))))
                 return MHC_ERR_INVALID_ARGUMENT;
@@ -251,11 +259,12 @@ mhc_status pre_entry(const uint16_t* x, const float* pre_in, const float* fn, co
                 float* pre1 = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + planes);
                 cudaError_t e = mhc::launch_pre_tc(x, pre1, fn, bias, alpha, norm_weight, T, C, sinkhorn_iters,
                                                    rms_eps, norm_eps, sinkhorn_eps, pre1, post_out, comb_out,
-                                                   layer_input, logits_out, workspace, s, tcc, bcast, true);
+                                                   layer_input, logits_out, workspace, s, tcc, bcast, true,
+                                                   nullptr);
                 if (e == cudaSuccess)
                     e = mhc::launch_pre_tc(x, pre1, fn, bias, alpha, norm_weight, T, C, sinkhorn_iters, rms_eps,
                                            norm_eps, sinkhorn_eps, pre_out, post_out, comb_out, layer_input,
-                                           logits_out, workspace, s, tcc, bcast, false);
+                                           logits_out, workspace, s, tcc, bcast, false, nullptr);
                 return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA;
             }
             const uint16_t* xin = x;
@@ -268,7 +277,8 @@ mhc_status pre_entry(const uint16_t* x, const float* pre_in, const float* fn, co
             }
             cudaError_t e = mhc::launch_pre_tc(xin, pre_in, fn, bias, alpha, norm_weight, T, C, sinkhorn_iters,
                                                rms_eps, norm_eps, sinkhorn_eps, pre_out, post_out, comb_out,
-                                               layer_input, logits_out, workspace, s, tcc, bcast, false);
+                                               layer_input, logits_out, workspace, s, tcc, bcast, false,
+                                               packed);
             return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA;
         }
     }
@@ -295,6 +305,33 @@ mhc_status mhc_pre_delayed(const uint16_t* x, const float* pre_in, const float* 
     return pre_entry(x, pre_in, fn, bias, alpha, norm_weight, T, n, C, sinkhorn_iters, rms_eps, norm_eps,
                      sinkhorn_eps, pre_out, post_out, comb_out, layer_input, logits_out, workspace, workspace_bytes,
                      stream, false, nullptr, nullptr, nullptr, nullptr);
+}
+
+size_t mhc_pre_packed_bytes(int n, int C) {
+    if (n != 4 || C < 1 || C % 8 != 0 || C > kMaxC || !mhc::pre_tc_supports(C)) return 0;
+    return mhc::pre_tc_packed_bytes(C);
+}
+
+mhc_status mhc_pre_pack(const float* fn, int n, int C, void* packed, size_t packed_bytes, void* stream) {
+    if (n < 1 || C < 1) return MHC_ERR_INVALID_ARGUMENT;
+    if (n != 4 || C % 8 != 0 || C > kMaxC || !mhc::pre_tc_supports(C)) return MHC_ERR_UNSUPPORTED;
+    if (!fn || !packed || !aligned16(fn) || (reinterpret_cast<uintptr_t>(packed) & 255u)) return MHC_ERR_INVALID_ARGUMENT;
+    const size_t need = mhc::pre_tc_packed_bytes(C);
+    if (packed_bytes < need || overlaps(packed, need, fn, (size_t)24 * n * C * 4)) return MHC_ERR_INVALID_ARGUMENT;
+    if (current_device() < 0) return MHC_ERR_CUDA;
+    return mhc::launch_pre_tc_pack(fn, C, packed, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MHC_OK
+                                                                                                    : MHC_ERR_CUDA;
+}
+
+mhc_status mhc_pre_delayed_packed(const uint16_t* x, const float* pre_in, const float* fn, const void* packed,
+                                  size_t packed_bytes, const float* bias, const float* alpha,
+                                  const uint16_t* norm_weight, int64_t T, int n, int C, int sinkhorn_iters,
+                                  float rms_eps, float norm_eps, float sinkhorn_eps, float* pre_out, float* post_out,
+                                  float* comb_out, uint16_t* layer_input, float* logits_out, void* stream) {
+    if (!packed) return MHC_ERR_INVALID_ARGUMENT;
+    return pre_entry(x, pre_in, fn, bias, alpha, norm_weight, T, n, C, sinkhorn_iters, rms_eps, norm_eps,
+                     sinkhorn_eps, pre_out, post_out, comb_out, layer_input, logits_out, nullptr, 0, stream, false,
+                     nullptr, nullptr, nullptr, nullptr, false, false, packed, packed_bytes);
 }
 
 mhc_status mhc_pre(const uint16_t* x, const float* fn, const float* bias, const float* alpha,

@@ -31,7 +31,8 @@ cudaError_t launch_pre_tc(const uint16_t* x, const float* pre_in, const float* f
                           const float* alpha, const uint16_t* norm_w, int64_t T, int C, int iters,
                           float rms_eps, float norm_eps, float sk_eps, float* pre_out, float* post_out,
                           float* comb_out, uint16_t* layer_input, float* logits_out, void* workspace,
-                          cudaStream_t stream, int max_clusters, bool broadcast, bool gates_only);
+                          cudaStream_t stream, int max_clusters, bool broadcast, bool gates_only,
+                          const void* packed);
 }  // namespace mhc
 
 namespace {
@@ -115,6 +116,6 @@ extern "C" mhc_status mhc_pre_delayed_noalloc(const uint16_t* x, const float* pr
     cudaError_t e = mhc::launch_pre_tc(x, pre_in, fn, bias, alpha, norm_weight, T, C, sinkhorn_iters, rms_eps,
                                        norm_eps, sinkhorn_eps, pre_out, post_out, comb_out, layer_input,
                                        logits_out, scratch, static_cast<cudaStream_t>(stream), clusters, false,
-                                       false);
+                                       false, nullptr);
     return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA;
 }

@@ -114,6 +114,7 @@ struct Args {
     uint16_t* layer_input;
     float* logits_out;
     unsigned char* ws;  // fn planes, one region of ngroups x 9 KB per (cluster, rank)
+    const unsigned char* packed;  // or planes packed ahead (one region per rank, shared by the clusters)
     int ntiles;
 };
 
@@ -151,6 +152,51 @@ __device__ __forceinline__ void split3(const float (&w)[8], uint32_t (&pk)[3][4]
     }
 }
 
+// fn K-slice [c0, c0 + 16 ngroups) of all 24 rows and 4 streams -> the three
+// bf16 planes in the MMA operand layout at wreg (ngroups x 9 KB), by the 352
+// threads of a CTA.  Items of 8 columns; a warp takes units of 8 rows x 4
+// neighbouring column chunks (lane = row * 4 + chunk), so that a load covers
+// 8 runs of 128 contiguous bytes of fn and a plane store two whole 256-byte
+// row atoms; every thread first loads all of its items (one latency), then
+// splits and stores them.
+__device__ __forceinline__ void write_planes(const float* __restrict__ fn, int C, int c0, int ngroups,
+                                             unsigned char* wreg, int warp, int lane) {
+    const int64_t K = 4 * (int64_t)C;
+    constexpr int kUnitsMax = 11;   // ceil(4 streams x 10 chunk quads x 3 row octets / 11 warps)
+    const int nunits = 4 * ((ngroups + 1) / 2) * 3;   // an odd last chunk quad is half empty
+    const int mrow = lane >> 2, gc = lane & 3;
+    float w[kUnitsMax][8];
+#pragma unroll
+    for (int j = 0; j < kUnitsMax; ++j) {
+        const int u = warp + j * (kThreads / 32);
+        if (u < nunits) {
+            const int mo = u % 3, rest = u / 3, st = rest & 3, gp = rest >> 2;
+            const int m = 8 * mo + mrow, g = 2 * gp + (gc >> 1), c = gc & 1;
+            if (g >= ngroups) continue;
+            const float4* src = reinterpret_cast<const float4*>(fn + (int64_t)m * K + (int64_t)st * C + c0 +
+                                                                kCols * g + 8 * c);
+            const float4 u0 = __ldg(src), u1 = __ldg(src + 1);
+            w[j][0] = u0.x; w[j][1] = u0.y; w[j][2] = u0.z; w[j][3] = u0.w;
+            w[j][4] = u1.x; w[j][5] = u1.y; w[j][6] = u1.z; w[j][7] = u1.w;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < kUnitsMax; ++j) {
+        const int u = warp + j * (kThreads / 32);
+        if (u < nunits) {
+            const int mo = u % 3, rest = u / 3, st = rest & 3, gp = rest >> 2;
+            const int m = 8 * mo + mrow, g = 2 * gp + (gc >> 1), c = gc & 1;
+            if (g >= ngroups) continue;
+            uint32_t pk[3][4];
+            split3(w[j], pk);
+#pragma unroll
+            for (int p = 0; p < 3; ++p)
+                *reinterpret_cast<uint4*>(wreg + w_off(g, st, p * 24 + m, c)) =
+                    make_uint4(pk[p][0], pk[p][1], pk[p][2], pk[p][3]);
+        }
+    }
+}
+
 template <bool BCAST, bool GATES>
 __global__ void __launch_bounds__(kThreads, 1)
 pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap omap, const Args a) {
@@ -181,7 +227,8 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
     // broadcast seam: one x box per stage, read as all four streams
     constexpr int nbox = BCAST ? 1 : 4, xbox = BCAST ? 0 : kBoxBytes;
     constexpr uint32_t slot_bytes = (uint32_t)(kSlotBytes - (4 - nbox) * kBoxBytes);
-    unsigned char* wreg = a.ws + (size_t)(cid * kCtas + (int)rank) * ngroups * kWStage;
+    unsigned char* wreg = a.packed ? const_cast<unsigned char*>(a.packed) + (size_t)rank * ngroups * kWStage
+                                   : a.ws + (size_t)(cid * kCtas + (int)rank) * ngroups * kWStage;
     // stages of this CTA in the whole launch, and those issued before the fn planes are ready
     const int my_tiles = cid < a.ntiles ? (a.ntiles - 1 - cid) / ncl + 1 : 0;
     const uint32_t total_stages = (uint32_t)my_tiles * ngroups;
@@ -220,46 +267,8 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
     if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
 
     // ---- fn K-slice -> three bf16 planes in the operand layout, written to
-    //      this CTA's workspace region.  Items of 8 columns; a warp takes
-    //      units of 8 rows x 4 neighbouring column chunks (lane = row * 4 +
-    //      chunk), so that a load covers 8 runs of 128 contiguous bytes of fn
-    //      and a plane store two whole 256-byte row atoms; every thread first
-    //      loads all of its items (one latency), then splits and stores them.
-    {
-        constexpr int kUnitsMax = 11;   // ceil(4 streams x 10 chunk quads x 3 row octets / 11 warps)
-        const int nunits = 4 * ((ngroups + 1) / 2) * 3;   // an odd last chunk quad is half empty
-        const int mrow = lane >> 2, gc = lane & 3;
-        float w[kUnitsMax][8];
-#pragma unroll
-        for (int j = 0; j < kUnitsMax; ++j) {
-            const int u = warp + j * (kThreads / 32);
-            if (u < nunits) {
-                const int mo = u % 3, rest = u / 3, st = rest & 3, gp = rest >> 2;
-                const int m = 8 * mo + mrow, g = 2 * gp + (gc >> 1), c = gc & 1;
-                if (g >= ngroups) continue;
-                const float4* src = reinterpret_cast<const float4*>(a.fn + (int64_t)m * K + (int64_t)st * C + c0 +
-                                                                    kCols * g + 8 * c);
-                const float4 u0 = __ldg(src), u1 = __ldg(src + 1);
-                w[j][0] = u0.x; w[j][1] = u0.y; w[j][2] = u0.z; w[j][3] = u0.w;
-                w[j][4] = u1.x; w[j][5] = u1.y; w[j][6] = u1.z; w[j][7] = u1.w;
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < kUnitsMax; ++j) {
-            const int u = warp + j * (kThreads / 32);
-            if (u < nunits) {
-                const int mo = u % 3, rest = u / 3, st = rest & 3, gp = rest >> 2;
-                const int m = 8 * mo + mrow, g = 2 * gp + (gc >> 1), c = gc & 1;
-                if (g >= ngroups) continue;
-                uint32_t pk[3][4];
-                split3(w[j], pk);
-#pragma unroll
-                for (int p = 0; p < 3; ++p)
-                    *reinterpret_cast<uint4*>(wreg + w_off(g, st, p * 24 + m, c)) =
-                        make_uint4(pk[p][0], pk[p][1], pk[p][2], pk[p][3]);
-            }
-        }
-    }
+    //      this CTA's workspace region (unless packed ahead of the call)
+    if (!a.packed) write_planes(a.fn, C, c0, ngroups, wreg, warp, lane);
     if (fold)
         for (int i = tid; i < slice / 8; i += kThreads)
             reinterpret_cast<uint4*>(nw_s)[i] = __ldg(reinterpret_cast<const uint4*>(a.norm_w + c0) + i);
@@ -625,6 +634,13 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
     cluster_sync_all();  // no CTA leaves while a peer may still write into its shared memory
 }
 
+// Planes packed ahead of the calls: CTA r writes rank r's region (the same
+// bytes the kernel's prologue writes into each cluster's region).
+__global__ void __launch_bounds__(kThreads, 1) pre_tc_pack_kernel(const float* fn, int C, unsigned char* out) {
+    const int slice = C / kCtas, ngroups = slice / kCols, r = blockIdx.x;
+    write_planes(fn, C, r * slice, ngroups, out + (size_t)r * ngroups * kWStage, threadIdx.x >> 5, threadIdx.x & 31);
+}
+
 }  // namespace tc
 
 using PFN_encodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -644,6 +660,13 @@ static PFN_encodeTiled encode_fn() {
             fn = reinterpret_cast<PFN_encodeTiled>(p);
     }
     return fn;
+}
+
+size_t pre_tc_packed_bytes(int C) { return (size_t)tc::kCtas * (size_t)(C / (tc::kCols * tc::kCtas)) * tc::kWStage; }
+
+cudaError_t launch_pre_tc_pack(const float* fn, int C, void* out, cudaStream_t stream) {
+    tc::pre_tc_pack_kernel<<<tc::kCtas, tc::kThreads, 0, stream>>>(fn, C, static_cast<unsigned char*>(out));
+    return cudaGetLastError();
 }
 
 size_t pre_tc_workspace_bytes(int64_t T, int C, int max_clusters) {
@@ -687,7 +710,8 @@ cudaError_t launch_pre_tc(const uint16_t* x, const float* pre_in, const float* f
                           const float* alpha, const uint16_t* norm_w, int64_t T, int C, int iters,
                           float rms_eps, float norm_eps, float sk_eps, float* pre_out, float* post_out,
                           float* comb_out, uint16_t* layer_input, float* logits_out, void* workspace,
-                          cudaStream_t stream, int max_clusters, bool broadcast, bool gates_only) {
+                          cudaStream_t stream, int max_clusters, bool broadcast, bool gates_only,
+                          const void* packed) {
     PFN_encodeTiled enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     // x viewed as [T][4][C] bf16 (broadcast: [T][1][C], every stream's box
@@ -720,6 +744,7 @@ cudaError_t launch_pre_tc(const uint16_t* x, const float* pre_in, const float* f
     a.pre_out = pre_out; a.post_out = post_out; a.comb_out = comb_out;
     a.layer_input = layer_input; a.logits_out = logits_out;
     a.ws = static_cast<unsigned char*>(workspace);
+    a.packed = static_cast<const unsigned char*>(packed);
     a.ntiles = (int)((T + tc::kTile - 1) / tc::kTile);
     const int nclusters = a.ntiles < max_clusters ? a.ntiles : max_clusters;
     cudaLaunchConfig_t cfg = {};

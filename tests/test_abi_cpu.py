@@ -224,3 +224,25 @@ def test_seam_host_rejects_on_the_host(lib):
     assert lib.mhc_seam_host_workspace_bytes(0, 4, 5120) == 0
     assert lib.mhc_seam_host_workspace_bytes(16, 3, 5120) == 0
     assert lib.mhc_seam_host_workspace_bytes(16, 4, 5120) > 16 * 4 * 5120 * 2
+
+
+def test_packed_weights_host_checks(lib):
+    """Sizes and host-side rejections of the packed-weight calls (no device
+    here: a well-formed call finds none)."""
+    assert lib.mhc_pre_packed_bytes(4, 5120) == 16 * 20 * 9216
+    assert lib.mhc_pre_packed_bytes(4, 136) == 0          # not a tensor-core hidden size
+    assert lib.mhc_pre_packed_bytes(3, 5120) == 0
+    P = A + 0x8000000
+    assert lib.mhc_pre_pack(A + 0x200000, 4, 5120, P, 16 * 20 * 9216, None) == CUDA_ERR
+    assert lib.mhc_pre_pack(A + 0x200000, 4, 136, P, 1 << 20, None) == UNSUPPORTED
+    assert lib.mhc_pre_pack(A + 0x200000, 4, 5120, P + 16, 1 << 22, None) == INVALID   # not 256-aligned
+    assert lib.mhc_pre_pack(A + 0x200000, 4, 5120, P, 1024, None) == INVALID           # too small
+    assert lib.mhc_pre_pack(A + 0x200000, 4, 5120, A + 0x200000, 1 << 22, None) == INVALID   # overlaps fn
+    args = dict(x=A, pre_in=A + 0x100000, fn=A + 0x200000, packed=P, packed_bytes=16 * 20 * 9216,
+                bias=A + 0x3000000, alpha=A + 0x3001000, norm_weight=None, T=16, n=4, C=5120, iters=20,
+                rms_eps=1e-6, norm_eps=1e-6, sk_eps=1e-6, pre_out=A + 0x4000000, post_out=A + 0x4100000,
+                comb_out=A + 0x4200000, layer_input=A + 0x4300000, logits_out=None, stream=None)
+    assert lib.mhc_pre_delayed_packed(*args.values()) == CUDA_ERR
+    assert lib.mhc_pre_delayed_packed(*dict(args, packed=None).values()) == INVALID
+    assert lib.mhc_pre_delayed_packed(*dict(args, packed_bytes=1024).values()) == INVALID
+    assert lib.mhc_pre_delayed_packed(*dict(args, pre_out=P + 64).values()) == INVALID    # output inside packed

@@ -748,3 +748,20 @@ def test_seam_host_in_place_and_in_a_graph():
     assert torch.equal(out["x_new"], xn_ref)
     assert torch.equal(out["pre"], ref["pre"].cpu())
     g.close()
+
+
+@pytest.mark.parametrize("T,C,fold", [(4, 5120, True), (300, 5120, True), (1383, 5120, False), (700, 768, True),
+                                      (16384, 5120, True)])
+def test_packed_weights_are_bit_identical(T, C, fold):
+    """mhc_pre_delayed_packed (planes packed once by mhc_pre_pack, one copy
+    shared by the clusters, no per-call conversion) gives the bits of
+    mhc_pre_delayed; below 256 tokens it runs the cluster kernel on fn."""
+    gd = seam_inputs(T, C=C, seed=2500 + T, fold=fold, device="cuda")
+    packed = mhc.pre_pack(gd["fn"], C=C)
+    ref = mhc.pre_delayed(gd["x"], gd["pre_in"], gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"], return_logits=True)
+    got = mhc.pre_delayed_packed(gd["x"], gd["pre_in"], gd["fn"], packed, gd["bias"], gd["alpha"], gd["norm_w"],
+                                 return_logits=True)
+    torch.cuda.synchronize()
+    assert mhc.device_status() == 0
+    for k in ("pre", "post", "comb", "layer_input", "logits"):
+        assert torch.equal(got[k], ref[k]), k
