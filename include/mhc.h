@@ -39,8 +39,9 @@ typedef enum mhc_status {
  * mhc_pre_delayed -- the delayed mHC pre block ([A], commit message and
  * section "Why V4.1 cannot just reuse MHCPreOp": it collapses the sublayer's
  * input with the PREVIOUS seam's pre-mix and returns this seam's pre-mix;
- * "Approach": projection against fn plus row square-sums, post/comb gates and
- * every Sinkhorn iteration; "Result": the collapse is an fp32 multiply-and-sum;
+ * "Approach": the projection with each row's sum of squares, then the post
+ * and comb gates with all the Sinkhorn iterations; "Result": the collapse is
+ * a plain fp32 weighted sum, bit-exact between implementations;
  * [B] "Measurements": the optional RMSNorm fold x * rsqrt * norm_weight is
  * evaluated in fp32 and rounded once).  Per token t, with K = n*C and
  * x_flat[t][i*C + c] = x[t][i][c]:
@@ -209,8 +210,9 @@ mhc_status mhc_post_pre_delayed(const uint16_t *x, const uint16_t *y, const floa
                                 void *workspace, size_t workspace_bytes, void *stream);
 
 /*
- * Model-entry broadcast seam ([A] "Approach": the model-entry seam projects a
- * narrower operand, x, and AITER declines it; [A] "Test Plan": the delayed
+ * Model-entry broadcast seam ([A] "Approach": at the model's entry the
+ * projection's operand is x, narrower than the streams, and AITER declines
+ * that case; [A] "Test Plan": the delayed
  * block is tested with the carried pre-mix and with the model-entry one).
  * At the model's entry the n residual streams are n copies of one hidden
  * state x[t][c] (the embedding output), so these calls take x as [T, C] and

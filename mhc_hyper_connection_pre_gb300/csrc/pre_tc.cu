@@ -2,8 +2,9 @@
 // tensor cores (sm_103a), for prefill-sized token counts.
 //
 // Same method as pre_cluster.cu (vLLM page "Use AITER mHC for the delayed
-// pre block": projection against fn plus row square-sums, gates, Sinkhorn,
-// collapse with the previous seam's pre-mix; page "Fix TileLang mHC pre on
+// pre block", "Approach": the projection with each row's sum of squares,
+// the gates, the Sinkhorn iterations, the collapse with the previous seam's
+// pre-mix; page "Fix TileLang mHC pre on
 // 64-wide wavefronts", "Measurements": the fold rounded once).
 //
 // Why tensor cores: the projection is a dense contraction of 983,040 flop per

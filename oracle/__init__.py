@@ -107,7 +107,8 @@ def pre_delayed(x_bits, pre_in, fn, bias, alpha, norm_w_bits=None, *,
                 sinkhorn_eps=SINKHORN_EPS, nthreads=1) -> dict:
     """Delayed mHC pre block for every token (the #56503 page: the block
     collapses a sublayer's input with the previous seam's pre-mix and returns
-    this seam's pre-mix, post/comb gates and the collapsed layer_input; the
+    this seam's pre-mix, the post and comb gates and the collapsed
+    layer_input; the
     #56342 page, "Measurements": the optional RMSNorm fold, rounded once).
 
     x_bits: uint16 [T, n, C] (bf16 bits); pre_in: float32 [T, n];
@@ -171,8 +172,9 @@ def pre_nondelayed(x_bits, fn, bias, alpha, norm_w_bits=None, *, pre_mix=None, i
 
 def broadcast_streams(x_bits, n: int = 4) -> np.ndarray:
     """The model-entry residual: n copies of the hidden state x [T, C] as the
-    streams of a [T, n, C] residual (the #56503 page, "Approach": the
-    model-entry seam projects the narrower operand x)."""
+    streams of a [T, n, C] residual (the #56503 page, "Approach": at the
+    model's entry the projection's operand is x itself, narrower than the
+    streams)."""
     x_bits = _c(x_bits, np.uint16)
     T, C = x_bits.shape
     return np.ascontiguousarray(np.broadcast_to(x_bits[:, None, :], (T, n, C)))
@@ -193,8 +195,9 @@ def pre_nondelayed_broadcast(x_bits, fn, bias, alpha, norm_w_bits=None, n: int =
 def gates_from_logits(logits, n=4, *, iters=SINKHORN_ITERS,
                       sinkhorn_eps=SINKHORN_EPS) -> dict:
     """pre = sigmoid(l[:n]), post = 2 sigmoid(l[n:2n]), comb = Sinkhorn of
-    l[2n:] as an n x n row-major matrix (the #56503 page: "post/comb gates and
-    every Sinkhorn iteration", 20 iterations); fp64 from the given logits."""
+    l[2n:] as an n x n row-major matrix (the #56503 page, "Approach": one
+    stage forms the post and comb gates and runs all the Sinkhorn iterations,
+    20 of them); fp64 from the given logits."""
     lg = _c(logits, np.float64)
     M = 2 * n + n * n
     lg = lg.reshape(-1, M)

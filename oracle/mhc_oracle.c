@@ -12,8 +12,9 @@
  *    commit message and sections "Why V4.1 cannot just reuse MHCPreOp",
  *    "Approach", "Result", "Notes / follow-ups": the delayed pre collapses a
  *    sublayer's input with the previous seam's pre-mix and returns its own;
- *    projection against fn plus row square-sums; post/comb gates; 20 Sinkhorn
- *    iterations on a 4x4 comb; the collapse is an fp32 multiply-and-sum.
+ *    the projection with each row's sum of squares; the post and comb gates;
+ *    20 Sinkhorn iterations on a 4x4 comb; the collapse is a plain fp32
+ *    weighted sum, bit-exact between implementations.
  *  - "[ROCm][DSv4.1] Fix TileLang mHC pre on 64-wide wavefronts ..." (#56342),
  *    sections "The bug" and "Measurements": the fused RMSNorm fold computes
  *    x * rsqrt * norm_weight in fp32 and rounds once.
@@ -176,7 +177,7 @@ typedef struct {
 
 /* One token of the delayed pre block.
  * 1. r = 1/sqrt(mean_k x_flat[k]^2 + rms_eps), x_flat[i*C + c] = x[i][c]
- *    ("projection against fn plus row square-sums").
+ *    (the sums of squares come with the projection, [A] "Approach").
  * 2. l[m] = r * (sum_k x_flat[k] fn[m][k]) * alpha_seg(m) + bias[m], with
  *    alpha_seg = alpha[0] for m < n, alpha[1] for m < 2n, alpha[2] after.
  * 3. gates and comb as in gates_from_logits.

@@ -3,7 +3,7 @@
 Tolerances (the spec bars of this seam, restated):
   * collapse without the fold: bit-exact (the oracle's fp32 path, stream
     order, no fused multiply-add; the #56503 page reports the collapse as
-    bit-exact because it is the same fp32 multiply-and-sum);
+    bit-exact, being the same fp32 weighted sum in every implementation);
   * pre / post / comb: |gpu - oracle| <= 2e-5 |oracle| + 1e-37 (fp32 gates vs
     the fp64 oracle);
   * bf16 outputs (folded layer_input, post): within 1 bf16 ulp of the

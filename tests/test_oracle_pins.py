@@ -516,7 +516,7 @@ def _bcast_case(T=5, C=96, seed=21):
 
 
 def test_broadcast_projection_narrows_to_c_columns():
-    """The model-entry seam projects the narrower operand: with every stream
+    """At the model's entry the projection's operand narrows to x: with every stream
     equal to x, x_flat . fn[m] = x . (sum_i fn[m][iC:(i+1)C]) and the RMS
     over K = 4C equals the RMS over C, so the logits follow from a [24, C]
     matmul against the stream-summed fn (numpy, fp64).  A broadcast along the
