@@ -367,6 +367,19 @@ def run_ours(args, rank, world, local):
                                    "frac_of_hbm_peak": round(nbytes / us / 1e3 / hbm_peak, 4)}
         assert mhc.device_status() == 0, "a bounded in-kernel wait timed out"
         del xe, oe, xne, packed
+        # the stress workload: T = 65536, comb logits driven to +-30 and beyond,
+        # 1 % of the rows scaled by 1e3 and 1 % all zero
+        Ts = 65536
+        ds = seam_inputs(Ts, seed=0, fold=True, stress=True, device=f"cuda:{local}")
+        os_ = mhc.pre_delayed(ds["x"], ds["pre_in"], ds["fn"], ds["bias"], ds["alpha"], ds["norm_w"])
+        us = timed(lambda: mhc.pre_delayed(ds["x"], ds["pre_in"], ds["fn"], ds["bias"], ds["alpha"],
+                                           ds["norm_w"], out=os_), reps=10)
+        nb = pre_bytes(Ts)
+        other_prefill["mhc_pre_delayed_stress_T65536"] = {
+            "us": round(us, 2), "bytes": nb, "gbs": round(nb / us / 1e3, 1),
+            "frac_of_hbm_peak": round(nb / us / 1e3 / hbm_peak, 4)}
+        assert mhc.device_status() == 0, "a bounded in-kernel wait timed out"
+        del ds, os_
 
     # ---- decode sweep and the 80-seam chain (rank 0 only)
     decode = chain = None
