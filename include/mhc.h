@@ -7,8 +7,10 @@
  *   [B] "[ROCm][DSv4.1] Fix TileLang mHC pre on 64-wide wavefronts and use the
  *        fused kernels on the AMD path" (#56342)
  * Every pointer argument is a caller-owned DEVICE pointer (CUDA global
- * memory) unless stated otherwise; the library never allocates, frees,
- * synchronises or copies between host and device inside a call.  Calls are
+ * memory) unless stated otherwise; the library never allocates device
+ * memory, frees or synchronises inside a call, and only mhc_seam_host copies
+ * between host and device (its purpose; on two library streams created once
+ * per device).  Calls are
  * asynchronous on the given stream (a cudaStream_t passed as void*; NULL is
  * the legacy default stream).  Arguments are checked on the host before any
  * launch: a rejected call launches nothing and returns the status.
