@@ -254,7 +254,16 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
         *abort = 0;
         fence_mbar_init_cluster();
         fence_proxy_async_smem();
-        // the first ring slots' x boxes do not depend on fn: start them now
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+
+    // ---- fn K-slice -> three bf16 planes in the operand layout, written to
+    //      this CTA's workspace region (unless packed ahead of the call)
+    if (!a.packed) write_planes(a.fn, C, c0, ngroups, wreg, warp, lane);
+    // the first ring slots' x boxes do not depend on fn: start them now,
+    // after this CTA's fn reads (issued at the start they slowed those by
+    // 2 us) and still well before the planes can be loaded
+    if (tid == 0) {
         const uint64_t pol_x = policy_evict_first();
         for (uint32_t q = 0; q < early; ++q) {
             const int tile = cid + (int)(q / ngroups) * ncl, grp = (int)(q % ngroups);
@@ -265,11 +274,6 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
                                  tile * kTile, &full[q], pol_x);
         }
     }
-    if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
-
-    // ---- fn K-slice -> three bf16 planes in the operand layout, written to
-    //      this CTA's workspace region (unless packed ahead of the call)
-    if (!a.packed) write_planes(a.fn, C, c0, ngroups, wreg, warp, lane);
     if (fold)
         for (int i = tid; i < slice / 8; i += kThreads)
             reinterpret_cast<uint4*>(nw_s)[i] = __ldg(reinterpret_cast<const uint4*>(a.norm_w + c0) + i);
