@@ -33,6 +33,9 @@ cudaError_t launch_pre_tc(const uint16_t* x, const float* pre_in, const float* f
                           cudaStream_t stream, int max_clusters, bool broadcast, bool gates_only,
                           const void* packed);
 size_t pre_tc_packed_bytes(int C);
+cudaError_t launch_collapse_fold(const uint16_t* x, const float* pre, const uint16_t* norm_w, int64_t T, int C,
+                                 bool broadcast, int clusters, float norm_eps, uint16_t* out, cudaStream_t stream,
+                                 int num_sms);
 cudaError_t launch_pre_tc_pack(const float* fn, int C, void* out, cudaStream_t stream);
 cudaError_t read_device_status(unsigned int* status);
 cudaError_t read_decode_status(unsigned int* status);
@@ -253,18 +256,24 @@ mhc_status pre_entry(const uint16_t* x, const float* pre_in, const float* fn, co
             if (workspace_bytes < need || (need && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))))
                 return MHC_ERR_INVALID_ARGUMENT;
             if (nondelayed) {
-                // pass 1: the gates only (no collapse, fold or layer_input);
-                // pass 2: the delayed block with pre_in = the pre-mix of pass
-                // 1, which reproduces the gates bit for bit
-                float* pre1 = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + planes);
-                cudaError_t e = mhc::launch_pre_tc(x, pre1, fn, bias, alpha, norm_weight, T, C, sinkhorn_iters,
-                                                   rms_eps, norm_eps, sinkhorn_eps, pre1, post_out, comb_out,
+                // pass 1: the gates only (no collapse, fold or layer_input),
+                // its unused pre_in pointed at the workspace scratch; pass 2:
+                // the collapse and fold with pass 1's pre as an HBM stream,
+                // in the tensor-core kernel's order (so the same bits as the
+                // delayed block fed that pre)
+                float* scratch = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + planes);
+                cudaError_t e = mhc::launch_pre_tc(x, scratch, fn, bias, alpha, norm_weight, T, C, sinkhorn_iters,
+                                                   rms_eps, norm_eps, sinkhorn_eps, pre_out, post_out, comb_out,
                                                    layer_input, logits_out, workspace, s, tcc, bcast, true,
                                                    nullptr);
-                if (e == cudaSuccess)
-                    e = mhc::launch_pre_tc(x, pre1, fn, bias, alpha, norm_weight, T, C, sinkhorn_iters, rms_eps,
-                                           norm_eps, sinkhorn_eps, pre_out, post_out, comb_out, layer_input,
-                                           logits_out, workspace, s, tcc, bcast, false, nullptr);
+                if (e == cudaSuccess) {
+                    const int64_t ntiles = (T + 127) / 128;
+                    const int ncl = ntiles < tcc ? (int)ntiles : tcc;
+                    const int sms = num_sms(dev);
+                    e = sms > 0 ? mhc::launch_collapse_fold(x, pre_out, norm_weight, T, C, bcast, ncl, norm_eps,
+                                                            layer_input, s, sms)
+                                : cudaErrorInvalidValue;
+                }
                 return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA;
             }
             const uint16_t* xin = x;

@@ -297,12 +297,15 @@ def test_fused_seam_is_one_launch_in_a_graph():
 
 @pytest.mark.parametrize("T,C,fold", [(1, 5120, True), (7, 5120, False), (33, 5120, True), (128, 5120, False),
                                       (100, 1000, True), (300, 1000, False), (300, 5120, True), (1000, 5120, False),
-                                      (5, 8, True)])
+                                      (5, 8, True), (2000, 768, True), (2000, 768, False), (4097, 4096, True)])
 def test_nondelayed_pre_equals_delayed_with_its_own_pre(T, C, fold):
     """mhc_pre's gates are those of mhc_pre_delayed (they do not depend on the
     incoming pre-mix), and its layer input is bit for bit the delayed call's
     with pre_in set to the pre it returned: the cluster kernel below 256
-    tokens, the two-pass tensor-core path above, multi-round tiles at C=1000."""
+    tokens, the two-pass path above (gates-only tensor-core pass, then the
+    streaming collapse in the tensor-core kernel's order), multi-round tiles
+    at C=1000; C=768 has an odd number of stages per slice and several
+    rounds per cluster at T=2000, so stage groups alternate between rounds."""
     d = seam_inputs(T, C=C, seed=1700 + T + C, fold=fold)
     gd = _to_dev(d)
     got = mhc.pre(gd["x"], gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"], return_logits=True)
