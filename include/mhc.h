@@ -168,8 +168,10 @@ mhc_status mhc_post(const uint16_t *x, const uint16_t *y, const float *comb,
  * other arguments as mhc_pre_delayed.  Below 256 tokens (and for hidden sizes
  * the tensor-core kernel does not take) one kernel, where the finalising CTA
  * sends each token's pre to the cluster before the collapse; from 256 tokens
- * two tensor-core passes (the first for the gates; its pre-mix goes to a
- * scratch area of the workspace, so mhc_pre_workspace_bytes covers it).
+ * two launches: the tensor-core kernel for the gates only, then a streaming
+ * collapse and fold with the pre it wrote, in the tensor-core kernel's order
+ * of summation (mhc_pre_workspace_bytes covers both: the planes plus T * 16
+ * bytes of scratch).
  */
 mhc_status mhc_pre(const uint16_t *x, const float *fn, const float *bias, const float *alpha,
                    const uint16_t *norm_weight, int64_t T, int n, int C, int sinkhorn_iters,
