@@ -32,7 +32,7 @@ extern "C" {
 typedef enum mhc_status {
     MHC_OK = 0,
     MHC_ERR_INVALID_ARGUMENT = 1, /* NULL, misaligned or aliasing pointer, bad count   */
-    MHC_ERR_UNSUPPORTED = 2,      /* valid but outside the shapes this build handles   */
+    MHC_ERR_UNSUPPORTED = 2,      /* valid but outside the shapes this library handles */
     MHC_ERR_CUDA = 3,             /* a CUDA runtime call or launch failed               */
     MHC_ERR_TIMEOUT = 4           /* a bounded device-side wait gave up (see below)      */
 } mhc_status;
@@ -68,7 +68,7 @@ typedef enum mhc_status {
  *  alpha        [3]       fp32   pre / post / comb logit scales
  *  norm_weight  [C] bf16 or NULL (NULL: no RMSNorm fold)
  *  T            tokens, >= 0 (T == 0 launches nothing and returns MHC_OK)
- *  n            streams; this build supports n == 4 only
+ *  n            streams; this library supports n == 4 only
  *  C            hidden size; multiple of 8, 8 <= C <= 6144
  *  sinkhorn_iters >= 1 (the pages use 20)
  *  rms_eps, norm_eps, sinkhorn_eps  >= 0 (the pages' workload: 1e-6 each)
@@ -182,9 +182,8 @@ mhc_status mhc_pre(const uint16_t *x, const float *fn, const float *bias, const 
 /*
  * mhc_post_pre_delayed -- one seam boundary in a single call: the PREVIOUS
  * seam's post (as mhc_post, on x, y, comb, post) followed by THIS seam's
- * delayed pre (as mhc_pre_delayed) on its result x_new.  The survey of the
- * pages ranks this fusion as the next step after the two blocks: a decoder
- * runs ... pre(s) -> sublayer -> post(s) -> pre(s+1) ..., and post(s) and
+ * delayed pre (as mhc_pre_delayed) on its result x_new.  A decoder runs
+ * ... pre(s) -> sublayer -> post(s) -> pre(s+1) ..., and post(s) and
  * pre(s+1) meet at x_new ([A] "Result": the seam's launch count is the
  * figure the pages track; the next seam's pre reads exactly the x_new the
  * post writes).

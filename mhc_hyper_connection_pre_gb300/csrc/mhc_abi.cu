@@ -135,7 +135,7 @@ const char* mhc_status_string(mhc_status s) {
     switch (s) {
         case MHC_OK: return "MHC_OK";
         case MHC_ERR_INVALID_ARGUMENT: return "MHC_ERR_INVALID_ARGUMENT: null, misaligned or overlapping pointer, or bad count";
-        case MHC_ERR_UNSUPPORTED: return "MHC_ERR_UNSUPPORTED: shape outside this build (n must be 4, C a multiple of 8 up to 6144)";
+        case MHC_ERR_UNSUPPORTED: return "MHC_ERR_UNSUPPORTED: shape this library does not handle (n must be 4, C a multiple of 8 up to 6144)";
         case MHC_ERR_CUDA: return "MHC_ERR_CUDA: a CUDA runtime call or kernel launch failed";
         case MHC_ERR_TIMEOUT: return "MHC_ERR_TIMEOUT: a bounded device-side wait gave up";
     }

@@ -1,6 +1,6 @@
 """Comparison rules between the CUDA path and the CPU oracle.
 
-Tolerances (the spec bars of this seam, restated):
+Tolerances (the seam's accuracy bars, restated):
   * collapse without the fold: bit-exact (the oracle's fp32 path, stream
     order, no fused multiply-add; the #56503 page reports the collapse as
     bit-exact, being the same fp32 weighted sum in every implementation);
