@@ -39,6 +39,7 @@ cudaError_t launch_collapse_fold(const uint16_t* x, const float* pre, const uint
 cudaError_t launch_pre_tc_pack(const float* fn, int C, void* out, cudaStream_t stream);
 cudaError_t read_device_status(unsigned int* status);
 cudaError_t read_decode_status(unsigned int* status);
+cudaError_t read_collapse_status(unsigned int* status);
 }  // namespace mhc
 
 namespace {
@@ -148,10 +149,11 @@ int mhc_set_launch_overlap(int enable) { return g_launch_overlap.exchange(enable
 
 mhc_status mhc_device_status(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return MHC_ERR_CUDA;
-    unsigned int v = 0, w = 0;
+    unsigned int v = 0, w = 0, c = 0;
     if (mhc::read_device_status(&v) != cudaSuccess) return MHC_ERR_CUDA;
     if (mhc::read_decode_status(&w) != cudaSuccess) return MHC_ERR_CUDA;
-    return (v | w) ? MHC_ERR_TIMEOUT : MHC_OK;
+    if (mhc::read_collapse_status(&c) != cudaSuccess) return MHC_ERR_CUDA;
+    return (v | w | c) ? MHC_ERR_TIMEOUT : MHC_OK;
 }
 
 mhc_status mhc_pre_delayed_plan(int64_t T, int n, int C, int* kernel, int* grid, int* cluster,

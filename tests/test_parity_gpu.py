@@ -297,7 +297,8 @@ def test_fused_seam_is_one_launch_in_a_graph():
 
 @pytest.mark.parametrize("T,C,fold", [(1, 5120, True), (7, 5120, False), (33, 5120, True), (128, 5120, False),
                                       (100, 1000, True), (300, 1000, False), (300, 5120, True), (1000, 5120, False),
-                                      (5, 8, True), (2000, 768, True), (2000, 768, False), (4097, 4096, True)])
+                                      (5, 8, True), (2000, 768, True), (2000, 768, False), (4097, 4096, True),
+                                      (600, 6144, True), (600, 6144, False)])
 def test_nondelayed_pre_equals_delayed_with_its_own_pre(T, C, fold):
     """mhc_pre's gates are those of mhc_pre_delayed (they do not depend on the
     incoming pre-mix), and its layer input is bit for bit the delayed call's
@@ -305,7 +306,9 @@ def test_nondelayed_pre_equals_delayed_with_its_own_pre(T, C, fold):
     tokens, the two-pass path above (gates-only tensor-core pass, then the
     streaming collapse in the tensor-core kernel's order), multi-round tiles
     at C=1000; C=768 has an odd number of stages per slice and several
-    rounds per cluster at T=2000, so stage groups alternate between rounds."""
+    rounds per cluster at T=2000, so stage groups alternate between rounds;
+    C=6144 (the widest residual) streams with one CTA per SM under the fold
+    and two without."""
     d = seam_inputs(T, C=C, seed=1700 + T + C, fold=fold)
     gd = _to_dev(d)
     got = mhc.pre(gd["x"], gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"], return_logits=True)
@@ -368,7 +371,8 @@ def _bcast_case(T, C, fold, seed):
 
 
 @pytest.mark.parametrize("T,C,fold", [(1, 5120, True), (7, 5120, False), (33, 5120, True), (128, 5120, False),
-                                      (300, 1000, True), (300, 5120, True), (1000, 5120, False), (5, 8, True)])
+                                      (300, 1000, True), (300, 5120, True), (1000, 5120, False), (5, 8, True),
+                                      (700, 6144, True)])
 def test_broadcast_pre_is_bit_identical_to_the_copied_residual(T, C, fold):
     """mhc_pre_delayed_broadcast / mhc_pre_broadcast on x [T, C] give every
     output bit for bit as the four-stream calls on x copied into four
