@@ -329,7 +329,7 @@ def run_ours(args, rank, world, local):
     # ---- the other prefill entry points at the same T (rank 0 only): the
     # model-entry broadcast seam and the non-delayed pre
     other_prefill = None
-    if rank == 0 and not args.skip_decode:
+    if rank == 0 and (not args.skip_decode or args.other_prefill):
         xe = x[:, 0, :].contiguous()
         oe = {k: torch.empty_like(v) for k, v in outs[0].items()}
         xne = torch.empty_like(x)
@@ -609,6 +609,9 @@ def main():
     ap.add_argument("--skip-decode", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--other-prefill", action="store_true",
+                    help="time the other prefill entry points (broadcast seam, mhc_pre, packed fn, the stress "
+                         "workload) even with --skip-decode")
     ap.add_argument("--tokens", type=int, default=T_PREFILL,
                     help="tokens per rank (default 16384; smaller only for profiling)")
     args = ap.parse_args()
