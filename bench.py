@@ -354,6 +354,12 @@ def run_ours(args, rank, world, local):
             "mhc_post_broadcast": (lambda: mhc.post_broadcast(xe, y, oe["comb"], oe["post"], out=xne),
                                    T * POST_BCAST_BYTES_PER_TOKEN),
             "mhc_pre": (lambda: mhc.pre(x, d["fn"], d["bias"], d["alpha"], d["norm_w"], out=oe), pre_bytes(T)),
+            # post of one seam and the next seam's delayed pre in one call; the
+            # bytes are the fused op's own (the pre consumes x_new without
+            # reading it back), so the fraction shows what a one-pass kernel would gain
+            "mhc_post_pre_delayed": (lambda: mhc.post_pre_delayed(
+                x, y, outs[0]["comb"], outs[0]["post"], pre_in[0], d["fn"], d["bias"], d["alpha"], d["norm_w"],
+                x_new=xne, out=oe), post_bytes(T) + pre_bytes(T) - T * 40960),
             # fn's planes packed once ahead (a weight transform, outside the timing)
             "mhc_pre_delayed_packed": (lambda: mhc.pre_delayed_packed(x, pre_in[0], d["fn"], packed, d["bias"],
                                                                       d["alpha"], d["norm_w"], out=oe),

@@ -298,7 +298,7 @@ def test_fused_seam_is_one_launch_in_a_graph():
 @pytest.mark.parametrize("T,C,fold", [(1, 5120, True), (7, 5120, False), (33, 5120, True), (128, 5120, False),
                                       (100, 1000, True), (300, 1000, False), (300, 5120, True), (1000, 5120, False),
                                       (5, 8, True), (2000, 768, True), (2000, 768, False), (4097, 4096, True),
-                                      (600, 6144, True), (600, 6144, False)])
+                                      (600, 6144, True), (600, 6144, False), (256, 5120, True), (257, 2048, False)])
 def test_nondelayed_pre_equals_delayed_with_its_own_pre(T, C, fold):
     """mhc_pre's gates are those of mhc_pre_delayed (they do not depend on the
     incoming pre-mix), and its layer input is bit for bit the delayed call's
