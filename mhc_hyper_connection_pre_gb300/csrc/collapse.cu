@@ -428,6 +428,10 @@ cudaError_t launch_collapse_fold(const uint16_t* x, const float* pre, const uint
                                  int num_sms) {
     if (T <= 0) return cudaSuccess;
     if (T > INT32_MAX) return cudaErrorInvalidValue;   // far beyond any device's memory
+    // the slice and stage arithmetic needs C a multiple of 256, the fold
+    // kernel at most two chunks per consumer thread, the round mapping a cluster
+    if (C <= 0 || C % 256 != 0 || C / 8 > kPipeMaxChunks * kPipeConsumers || clusters < 1)
+        return cudaErrorInvalidValue;
     if (norm_w)
         return broadcast ? launch_pipe<true>(x, pre, norm_w, T, C, clusters, norm_eps, out, stream, num_sms)
                          : launch_pipe<false>(x, pre, norm_w, T, C, clusters, norm_eps, out, stream, num_sms);
