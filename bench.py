@@ -554,6 +554,10 @@ def run_ours(args, rank, world, local):
         "clocks": clk.summary(),
         "other_prefill": other_prefill,
         "decode_graph": decode,
+        "decode_graph_method": (f"per T: {DECODE_REPS} back-to-back calls captured in one CUDA graph, "
+                                "replayed 50 times, 5 repeats, median of the repeats / (50 x "
+                                f"{DECODE_REPS}) = microseconds per call; a graph holding one call "
+                                "would time this host's graph-launch rate (about 14 us), not the GPU"),
         "decode_chain_80": chain,
     }
     if rank == 0:

@@ -12,8 +12,10 @@
  * between host and device (its purpose; on two library streams created once
  * per device).  Calls are
  * asynchronous on the given stream (a cudaStream_t passed as void*; NULL is
- * the legacy default stream).  Arguments are checked on the host before any
- * launch: a rejected call launches nothing and returns the status.
+ * the legacy default stream).  Every call works on the CURRENT CUDA device:
+ * the stream and every device pointer must belong to it.  Arguments are
+ * checked on the host before any launch: a rejected call launches nothing
+ * and returns the status.
  *
  * Types: bf16 tensors are passed as uint16_t bit patterns; fp32 as float.
  * All tensors are dense, row-major, and every array pointer must be 16-byte
@@ -129,7 +131,10 @@ size_t mhc_pre_workspace_bytes(int64_t T, int n, int C);
  * rewrites the part it reads before reading it.  Every call shares the one
  * array: calls whose kernels can overlap on the GPU (different streams, or
  * graphs replayed concurrently) race on it and must be serialised by the
- * caller.  Errors as mhc_pre_delayed.
+ * caller.  The array's address belongs to the current device, so x must be
+ * device memory of the current device and the stream (when not NULL) a
+ * stream of it: otherwise MHC_ERR_INVALID_ARGUMENT, returned before anything
+ * is set up or launched.  Other errors as mhc_pre_delayed.
  */
 #define MHC_NOALLOC_SCRATCH_BYTES 5898240u
 mhc_status mhc_pre_delayed_noalloc(const uint16_t *x, const float *pre_in, const float *fn,
@@ -336,8 +341,13 @@ const char *mhc_status_string(mhc_status status);
  * Device status of the current device: synchronises the device, then reads
  * and clears the library's device-side status word.  MHC_ERR_TIMEOUT means a
  * bounded wait inside a kernel gave up since the last call (that launch's
- * outputs are garbage; the kernel still released its resources and returned).
- * MHC_ERR_CUDA if the synchronisation or the read failed.
+ * outputs are garbage).  After such a timeout the kernel stops issuing loads,
+ * still waits -- with bounded waits the timeout does not cut short -- for
+ * its own TMA and bulk loads, its tensor-core MMAs and the last bytes its
+ * cluster peers push into it, then frees its tensor memory and returns.
+ * Should one of those drain waits also give up, the kernel returns anyway
+ * (a copy still in flight is then not waited for).  No test provokes a
+ * timeout.  MHC_ERR_CUDA if the synchronisation or the read failed.
  */
 mhc_status mhc_device_status(void);
 

@@ -120,19 +120,29 @@ def _dev_ptr(t: torch.Tensor | None, name: str, dtype: torch.dtype, device) -> i
     return t.data_ptr()
 
 
-def workspace_for(T: int, n: int, C: int, device) -> torch.Tensor | None:
+def _device_index(device) -> int:
+    d = torch.device(device)
+    return d.index if d.index is not None else torch.cuda.current_device()
+
+
+def workspace_for(T: int, n: int, C: int, device, stream=None) -> torch.Tensor | None:
     """A cached device workspace big enough for ``mhc_pre_delayed`` at this
-    shape (None when the shape needs none).  One buffer per device, grown on
-    demand; calls that may run concurrently on different streams must pass
-    their own ``workspace=``."""
-    need = int(load_library().mhc_pre_workspace_bytes(T, n, C))
-    if need == 0:
-        return None
-    key = torch.device(device).index if torch.device(device).index is not None else torch.cuda.current_device()
-    buf = _workspaces.get(key)
-    if buf is None or buf.numel() < need:
-        buf = torch.empty(need, dtype=torch.uint8, device=torch.device("cuda", key))
-        _workspaces[key] = buf
+    shape (None when the shape needs none).  One buffer per (device, stream),
+    grown on demand and allocated on that stream, so calls on different
+    streams never share one; ``stream`` defaults to the device's current
+    stream."""
+    dev = _device_index(device)
+    with torch.cuda.device(dev):
+        need = int(load_library().mhc_pre_workspace_bytes(T, n, C))
+        if need == 0:
+            return None
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        key = (dev, s.cuda_stream)
+        buf = _workspaces.get(key)
+        if buf is None or buf.numel() < need:
+            with torch.cuda.stream(s):
+                buf = torch.empty(need, dtype=torch.uint8, device=torch.device("cuda", dev))
+            _workspaces[key] = buf
     return buf
 
 
@@ -182,13 +192,14 @@ def _pre_call(fname: str, x: torch.Tensor, pre_in: torch.Tensor | None, fn: torc
             _dev_ptr(o["layer_input"], "layer_input", torch.bfloat16, dev),
             _dev_ptr(o.get("logits"), "logits", torch.float32, dev)]
     if workspace is None:
-        workspace = workspace_for(T, n, C, dev)
+        workspace = workspace_for(T, n, C, dev, stream)
     ws_ptr, ws_bytes = None, 0
     if workspace is not None:
         ws_ptr = _dev_ptr(workspace, "workspace", torch.uint8, dev)
         ws_bytes = workspace.numel()
-    st = getattr(lib, fname)(*args, T, n, C, int(sinkhorn_iters), float(rms_eps), float(norm_eps),
-                             float(sinkhorn_eps), *outs, ws_ptr, ws_bytes, _stream_ptr(stream, dev))
+    with torch.cuda.device(dev):
+        st = getattr(lib, fname)(*args, T, n, C, int(sinkhorn_iters), float(rms_eps), float(norm_eps),
+                                 float(sinkhorn_eps), *outs, ws_ptr, ws_bytes, _stream_ptr(stream, dev))
     _check(fname, st)
     return o
 
@@ -250,8 +261,9 @@ def pre_pack(fn: torch.Tensor, n: int = 4, C: int | None = None, *, out: torch.T
     dev = fn.device
     if out is None:
         out = torch.empty(need, dtype=torch.uint8, device=dev)
-    st = lib.mhc_pre_pack(_dev_ptr(fn, "fn", torch.float32, dev), n, C, _dev_ptr(out, "packed", torch.uint8, dev),
-                          out.numel(), _stream_ptr(stream, dev))
+    with torch.cuda.device(dev):
+        st = lib.mhc_pre_pack(_dev_ptr(fn, "fn", torch.float32, dev), n, C,
+                              _dev_ptr(out, "packed", torch.uint8, dev), out.numel(), _stream_ptr(stream, dev))
     _check("mhc_pre_pack", st)
     return out
 
@@ -273,15 +285,16 @@ def pre_delayed_packed(x: torch.Tensor, pre_in: torch.Tensor, fn: torch.Tensor, 
         raise ValueError("pre_in / fn / bias / alpha have the wrong number of elements")
     if norm_weight is not None and norm_weight.numel() != C:
         raise ValueError("norm_weight must have C elements")
-    st = lib.mhc_pre_delayed_packed(
-        _dev_ptr(x, "x", torch.bfloat16, dev), _dev_ptr(pre_in, "pre_in", torch.float32, dev),
-        _dev_ptr(fn, "fn", torch.float32, dev), _dev_ptr(packed, "packed", torch.uint8, dev), packed.numel(),
-        _dev_ptr(bias, "bias", torch.float32, dev), _dev_ptr(alpha, "alpha", torch.float32, dev),
-        _dev_ptr(norm_weight, "norm_weight", torch.bfloat16, dev), T, n, C, int(sinkhorn_iters), float(rms_eps),
-        float(norm_eps), float(sinkhorn_eps), _dev_ptr(o["pre"], "pre", torch.float32, dev),
-        _dev_ptr(o["post"], "post", torch.float32, dev), _dev_ptr(o["comb"], "comb", torch.float32, dev),
-        _dev_ptr(o["layer_input"], "layer_input", torch.bfloat16, dev),
-        _dev_ptr(o.get("logits"), "logits", torch.float32, dev), _stream_ptr(stream, dev))
+    with torch.cuda.device(dev):
+        st = lib.mhc_pre_delayed_packed(
+            _dev_ptr(x, "x", torch.bfloat16, dev), _dev_ptr(pre_in, "pre_in", torch.float32, dev),
+            _dev_ptr(fn, "fn", torch.float32, dev), _dev_ptr(packed, "packed", torch.uint8, dev), packed.numel(),
+            _dev_ptr(bias, "bias", torch.float32, dev), _dev_ptr(alpha, "alpha", torch.float32, dev),
+            _dev_ptr(norm_weight, "norm_weight", torch.bfloat16, dev), T, n, C, int(sinkhorn_iters),
+            float(rms_eps), float(norm_eps), float(sinkhorn_eps), _dev_ptr(o["pre"], "pre", torch.float32, dev),
+            _dev_ptr(o["post"], "post", torch.float32, dev), _dev_ptr(o["comb"], "comb", torch.float32, dev),
+            _dev_ptr(o["layer_input"], "layer_input", torch.bfloat16, dev),
+            _dev_ptr(o.get("logits"), "logits", torch.float32, dev), _stream_ptr(stream, dev))
     _check("mhc_pre_delayed_packed", st)
     return o
 
@@ -356,13 +369,14 @@ def post_pre_delayed(x: torch.Tensor, y: torch.Tensor, comb: torch.Tensor, post:
             _dev_ptr(o["layer_input"], "layer_input", torch.bfloat16, dev),
             _dev_ptr(o.get("logits"), "logits", torch.float32, dev)]
     if workspace is None:
-        workspace = workspace_for(T, n, C, dev)
+        workspace = workspace_for(T, n, C, dev, stream)
     ws_ptr, ws_bytes = None, 0
     if workspace is not None:
         ws_ptr = _dev_ptr(workspace, "workspace", torch.uint8, dev)
         ws_bytes = workspace.numel()
-    st = lib.mhc_post_pre_delayed(*args, T, n, C, int(sinkhorn_iters), float(rms_eps), float(norm_eps),
-                                  float(sinkhorn_eps), *outs, ws_ptr, ws_bytes, _stream_ptr(stream, dev))
+    with torch.cuda.device(dev):
+        st = lib.mhc_post_pre_delayed(*args, T, n, C, int(sinkhorn_iters), float(rms_eps), float(norm_eps),
+                                      float(sinkhorn_eps), *outs, ws_ptr, ws_bytes, _stream_ptr(stream, dev))
     _check("mhc_post_pre_delayed", st)
     o["x_new"] = x_new
     return o
@@ -393,8 +407,10 @@ def pre_delayed_noalloc(x: torch.Tensor, pre_in: torch.Tensor, fn: torch.Tensor,
             _dev_ptr(out["comb"], "comb", torch.float32, dev),
             _dev_ptr(out["layer_input"], "layer_input", torch.bfloat16, dev),
             _dev_ptr(out.get("logits") if return_logits else None, "logits", torch.float32, dev)]
-    st = lib.mhc_pre_delayed_noalloc(*args, T, n, C, int(sinkhorn_iters), float(rms_eps), float(norm_eps),
-                                     float(sinkhorn_eps), *outs, _stream_ptr(stream, dev))
+    # the library's scratch address belongs to the current device: make x's current
+    with torch.cuda.device(dev):
+        st = lib.mhc_pre_delayed_noalloc(*args, T, n, C, int(sinkhorn_iters), float(rms_eps), float(norm_eps),
+                                         float(sinkhorn_eps), *outs, _stream_ptr(stream, dev))
     _check("mhc_pre_delayed_noalloc", st)
     return out
 
@@ -405,10 +421,11 @@ def _post_call(fname: str, x: torch.Tensor, y: torch.Tensor, comb: torch.Tensor,
     if y.numel() != T * C or comb.numel() != T * n * n or post_gate.numel() != T * n or \
             tuple(out.shape) != (T, n, C):
         raise ValueError("y / comb / post / out have the wrong shape")
-    st = getattr(load_library(), fname)(
-        _dev_ptr(x, "x", torch.bfloat16, dev), _dev_ptr(y, "y", torch.bfloat16, dev),
-        _dev_ptr(comb, "comb", torch.float32, dev), _dev_ptr(post_gate, "post", torch.float32, dev), T, n, C,
-        _dev_ptr(out, "out", torch.bfloat16, dev), _stream_ptr(stream, dev))
+    with torch.cuda.device(dev):
+        st = getattr(load_library(), fname)(
+            _dev_ptr(x, "x", torch.bfloat16, dev), _dev_ptr(y, "y", torch.bfloat16, dev),
+            _dev_ptr(comb, "comb", torch.float32, dev), _dev_ptr(post_gate, "post", torch.float32, dev), T, n, C,
+            _dev_ptr(out, "out", torch.bfloat16, dev), _stream_ptr(stream, dev))
     _check(fname, st)
     return out
 
@@ -470,22 +487,27 @@ def seam_host(x: torch.Tensor, y: torch.Tensor, pre_in: torch.Tensor, fn: torch.
             shp, dt = shapes[k]
             o[k] = torch.empty(shp, dtype=dt, pin_memory=True)
     if workspace is None:
-        need = int(lib.mhc_seam_host_workspace_bytes(T, n, C))
-        key = ("seam_host", dev.index if dev.index is not None else torch.cuda.current_device())
-        workspace = _workspaces.get(key)
-        if workspace is None or workspace.numel() < need:
-            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
-            _workspaces[key] = workspace
-    st = lib.mhc_seam_host(
-        _host_ptr(x, "x", torch.bfloat16), _host_ptr(y, "y", torch.bfloat16),
-        _host_ptr(pre_in, "pre_in", torch.float32), _dev_ptr(fn, "fn", torch.float32, dev),
-        _dev_ptr(bias, "bias", torch.float32, dev), _dev_ptr(alpha, "alpha", torch.float32, dev),
-        _dev_ptr(norm_weight, "norm_weight", torch.bfloat16, dev), T, n, C, int(sinkhorn_iters), float(rms_eps),
-        float(norm_eps), float(sinkhorn_eps), _host_ptr(o["x_new"], "x_new", torch.bfloat16),
-        _host_ptr(o["pre"], "pre", torch.float32), _host_ptr(o.get("post"), "post", torch.float32),
-        _host_ptr(o.get("comb"), "comb", torch.float32),
-        _host_ptr(o.get("layer_input"), "layer_input", torch.bfloat16),
-        _dev_ptr(workspace, "workspace", torch.uint8, dev), workspace.numel(), _stream_ptr(stream, dev))
+        di = _device_index(dev)
+        with torch.cuda.device(di):
+            need = int(lib.mhc_seam_host_workspace_bytes(T, n, C))
+            s = stream if stream is not None else torch.cuda.current_stream(di)
+            key = ("seam_host", di, s.cuda_stream)
+            workspace = _workspaces.get(key)
+            if workspace is None or workspace.numel() < need:
+                with torch.cuda.stream(s):
+                    workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=torch.device("cuda", di))
+                _workspaces[key] = workspace
+    with torch.cuda.device(dev):
+        st = lib.mhc_seam_host(
+            _host_ptr(x, "x", torch.bfloat16), _host_ptr(y, "y", torch.bfloat16),
+            _host_ptr(pre_in, "pre_in", torch.float32), _dev_ptr(fn, "fn", torch.float32, dev),
+            _dev_ptr(bias, "bias", torch.float32, dev), _dev_ptr(alpha, "alpha", torch.float32, dev),
+            _dev_ptr(norm_weight, "norm_weight", torch.bfloat16, dev), T, n, C, int(sinkhorn_iters),
+            float(rms_eps), float(norm_eps), float(sinkhorn_eps), _host_ptr(o["x_new"], "x_new", torch.bfloat16),
+            _host_ptr(o["pre"], "pre", torch.float32), _host_ptr(o.get("post"), "post", torch.float32),
+            _host_ptr(o.get("comb"), "comb", torch.float32),
+            _host_ptr(o.get("layer_input"), "layer_input", torch.bfloat16),
+            _dev_ptr(workspace, "workspace", torch.uint8, dev), workspace.numel(), _stream_ptr(stream, dev))
     _check("mhc_seam_host", st)
     return o
 

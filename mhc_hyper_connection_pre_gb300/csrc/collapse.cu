@@ -44,17 +44,6 @@ namespace {
 constexpr int kMaxSlots = 8;
 constexpr int kConsumerBar = 1;                // named barrier of the fold kernel's consumer warps
 
-// Bounded wait that ignores the abort flag: the producer's last look at its
-// own copies before it exits.
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
-    const uint32_t a = smem_u32(bar);
-    for (int i = 0; i < kSpinLimit; ++i) {
-        if (mbar_try_wait(a, parity)) return;
-        if (i > 32) __nanosleep(256);
-    }
-    atomicOr(&g_device_status, kDeviceTimeout);
-}
-
 // The producer thread: the CTA's k-th token (t = b + k G) into slot k % slots
 // once every consumer warp has released the slot's previous token; then a
 // bounded look at the last copy into each slot, which may still be in
@@ -68,6 +57,10 @@ __device__ __forceinline__ void produce(const uint16_t* x, const float* pre, int
     uint32_t n = 0;                               // the slot's round
     for (; k < K; ++k) {
         if (n > 0 && !mbar_wait(&empty[s], (n - 1) & 1u, abort)) break;
+        // the slot's previous copy has landed (consumers that timed out may
+        // release a slot without waiting for it): never two copies in flight
+        // into one slot
+        if (n > 0) mbar_wait_drain(&full[s], (n - 1) & 1u);
         const int64_t t = b + (int64_t)k * G;
         mbar_arrive_expect_tx(&full[s], slot_bytes + 16u);
         bulk_load_hint(ring + (size_t)s * slot_bytes, x + t * (BCAST ? (int64_t)C : 4 * (int64_t)C), slot_bytes,
@@ -79,7 +72,7 @@ __device__ __forceinline__ void produce(const uint16_t* x, const float* pre, int
     int js = k < slots ? 0 : s;
     uint32_t jn = k < slots ? 0u : n - 1;
     for (int c = 0; c < (k < slots ? k : slots); ++c) {
-        drain_wait(&full[js], jn & 1u);
+        mbar_wait_drain(&full[js], jn & 1u);   // not cut short by a timeout
         if (++js == slots) js = 0, ++jn;
     }
 }

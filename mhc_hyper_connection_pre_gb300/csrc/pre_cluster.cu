@@ -627,6 +627,32 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
     if (!arrived) cluster_arrive_relaxed();  // (a CTA with no tile)
     cp_async_wait_all();
     if (fused) bulk_wait_all();   // x_new copies complete before the CTA leaves
+    // After a timeout the inbox waits above may have been cut short: the last
+    // phase of each inbox barrier (peers push every tile's bytes whatever
+    // happened) is waited for again, uncut, before this CTA leaves.
+    __syncthreads();
+    if (*abort && tid == 0) {
+        const int64_t nrounds = cid < a.ntiles ? (a.ntiles - 1 - cid) / ncl + 1 : 0;
+        bool seen[2 + 2 * kSlots] = {};
+        for (int64_t r = nrounds - 1; r >= 0 && r >= nrounds - 4; --r) {
+            const int p = (int)(r & 1);
+            const uint32_t ph = (uint32_t)(r >> 1) & 1u;
+            const int n = tile_tokens(cid + r * ncl);
+            if (!seen[p]) {
+                seen[p] = true;
+                mbar_wait_drain<true>(&sq_full[p], ph);
+                if (nondel) {
+                    mbar_wait_drain<true>(&pre_full[p], ph);
+                    mbar_wait_drain<true>(&sh_full[p], ph);
+                }
+            }
+            for (int s = 0; s < kSlots; ++s)
+                if (kCtas * s + rank < n && !seen[2 + p * kSlots + s]) {
+                    seen[2 + p * kSlots + s] = true;
+                    mbar_wait_drain<true>(&dots_full[p * kSlots + s], ph);
+                }
+        }
+    }
     cluster_wait_acquire();  // no CTA leaves while a peer may still push into it
 }
 

@@ -39,6 +39,11 @@ namespace {
 
 constexpr int kNoAllocClusters = 2;
 constexpr size_t kNoAllocBytes = MHC_NOALLOC_SCRATCH_BYTES;
+// Every shape the entry point accepts fits: C is at most 5120 (the
+// tensor-core kernel's limit, checked first), i.e. at most 20 stages of
+// 9 KB of planes per CTA, for at most kNoAllocClusters clusters of 16 CTAs.
+static_assert((size_t)kNoAllocClusters * 16 * 20 * 9216 <= kNoAllocBytes,
+              "the scratch array holds the planes of every accepted shape");
 
 // The scratch itself.  Its name is a host-side stand-in in host code, not a
 // device address: host code uses the address cudaGetSymbolAddress returns.
@@ -106,13 +111,32 @@ extern "C" mhc_status mhc_pre_delayed_noalloc(const uint16_t* x, const float* pr
         for (const R& o2 : outs)
             if (&o != &o2 && overlaps(o.p, o.n, o2.p, o2.n)) return MHC_ERR_INVALID_ARGUMENT;
     }
+    // the planes of at most kNoAllocClusters clusters fit the array (host
+    // arithmetic only: nothing has been set up or launched yet)
+    if (mhc::pre_tc_workspace_bytes(T, C, kNoAllocClusters) > kNoAllocBytes) return MHC_ERR_UNSUPPORTED;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MHC_ERR_CUDA;
+    // The scratch address below belongs to the current device: x and the
+    // stream must belong to it too, or the kernel would run on another GPU
+    // with this one's address.  Checked before anything is set up or launched.
+    cudaPointerAttributes pa = {};
+    if (cudaPointerGetAttributes(&pa, x) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return MHC_ERR_INVALID_ARGUMENT;
+    }
+    if ((pa.type != cudaMemoryTypeDevice && pa.type != cudaMemoryTypeManaged) || pa.device != dev)
+        return MHC_ERR_INVALID_ARGUMENT;
+    if (stream) {
+        int sdev = -1;
+        if (cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &sdev) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return MHC_ERR_INVALID_ARGUMENT;
+        }
+        if (sdev != dev) return MHC_ERR_INVALID_ARGUMENT;
+    }
     void* scratch = nullptr;
     int clusters = 0;
     if (!setup(dev, &scratch, &clusters)) return MHC_ERR_CUDA;
-    // the shapes above always fit; the check keeps the stated limit explicit
-    if (mhc::pre_tc_workspace_bytes(T, C, clusters) > kNoAllocBytes) return MHC_ERR_UNSUPPORTED;
     cudaError_t e = mhc::launch_pre_tc(x, pre_in, fn, bias, alpha, norm_weight, T, C, sinkhorn_iters, rms_eps,
                                        norm_eps, sinkhorn_eps, pre_out, post_out, comb_out, layer_input,
                                        logits_out, scratch, static_cast<cudaStream_t>(stream), clusters, false,

@@ -295,7 +295,12 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
             for (; g < total_stages && !*abort; ++g) {
                 const int tile = cid + (int)(g / ngroups) * ncl, grp = (int)(g % ngroups);
                 const int s = g % kStages;
-                mbar_wait(&empty[s], ((g / kStages) & 1) ^ 1, abort);
+                if (!mbar_wait(&empty[s], ((g / kStages) & 1) ^ 1, abort)) break;
+                // The slot's previous load has landed: always true once its
+                // consumers released it normally, but after a timeout they
+                // release it without waiting, and a second copy must never
+                // be in flight into the same slot.
+                mbar_wait_drain(&full[s], ((g / kStages) & 1) ^ 1);
                 unsigned char* slot = stages + s * kSlotBytes;
                 mbar_arrive_expect_tx(&full[s], slot_bytes);
 #pragma unroll
@@ -304,9 +309,10 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
                                      pol_x);
                 bulk_load_hint(slot + kXBytes, wreg + grp * kWStage, kWStage, &full[s], pol_w);
             }
-            // drain: the last load of every slot has landed before the CTA exits
+            // drain: the last load of every slot has landed before the CTA
+            // exits (waits that a timeout does not cut short)
             for (uint32_t k = (g > (uint32_t)kStages ? g - kStages : 0); k < g; ++k)
-                mbar_wait(&full[k % kStages], (k / kStages) & 1, abort);
+                mbar_wait_drain(&full[k % kStages], (k / kStages) & 1);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -336,8 +342,9 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
                 }
                 mma_commit(&dfull[d]);
             }
+            // every MMA has completed before TMEM is freed, also after a timeout
             mma_commit(drain);
-            mbar_wait(drain, 0, abort);
+            mbar_wait_drain(drain, 0);
         }
         __syncwarp();
     } else if (warp < kFinWarp) {
@@ -632,6 +639,17 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
 
     tc_fence_before();
     __syncthreads();
+    // After a timeout the waits above may have been cut short: before this
+    // CTA leaves, the last phase of each inbox (every peer pushes its bytes
+    // for every tile whatever happened) is waited for again, uncut.
+    if (*abort && my_tiles > 0) {
+        const uint32_t lp = (uint32_t)(my_tiles - 1) & 1u;
+        if (warp == kFinWarp && lane == 0) {
+            mbar_wait_drain<true>(sq_full, lp);
+            mbar_wait_drain<true>(dots_full, lp);
+        }
+        if (warp == 2 && lane == 0) mbar_wait_drain<true>(scale_full, lp);
+    }
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);

@@ -2,7 +2,7 @@
 // sm_103a) features the tensor-core pre kernel uses: mbarriers (local and
 // cluster-remote), TMA tensor loads, tcgen05 tensor-memory allocation, MMA,
 // commit, loads and stores, and cluster addressing.  Every wait is bounded:
-// after kSpinLimit polls it records MHC_DEVICE_TIMEOUT in the device status
+// after kSpinLimit polls it records kDeviceTimeout in the device status
 // word and returns false instead of spinning forever.
 #pragma once
 
@@ -69,6 +69,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
     atomicOr(&g_device_status, kDeviceTimeout);
     *abort = 1;
+    return false;
+}
+// Bounded wait that ignores the abort flag, for the waits a CTA still owes
+// after a timeout before it may free what it holds or exit: its own TMA and
+// bulk loads have landed, its MMAs have completed, the last bytes pushed
+// into its inboxes have arrived.  In a run without a timeout these phases
+// have already completed and the first poll succeeds.  Gives up (and
+// records the timeout) after kSpinLimit polls like mbar_wait.
+template <bool kClusterAcquire = false>
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+    const uint32_t a = smem_u32(bar);
+    for (int i = 0; i < kSpinLimit; ++i) {
+        bool ok = kClusterAcquire ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity);
+        if (ok) return true;
+        if (i > 32) __nanosleep(256);
+    }
+    atomicOr(&g_device_status, kDeviceTimeout);
     return false;
 }
 

@@ -45,16 +45,31 @@ def assert_gates(g: np.ndarray, o: np.ndarray, what: str, rel: float = REL_GATES
                              f"gpu={g[tuple(i)]!r} oracle={o[tuple(i)]!r}; worst rel {worst:.3e}")
 
 
-def assert_bf16(g_bits: np.ndarray, o_bits: np.ndarray, what: str, abs_scale: np.ndarray | None = None):
+def assert_bf16(g_bits: np.ndarray, o_bits: np.ndarray, what: str, abs_scale: np.ndarray | None = None) -> int:
+    """Within 1 bf16 ulp of the oracle's rounded value.  With ``abs_scale``
+    (the sum of the absolute terms of a post output), an element beyond
+    1 ulp still passes when |gpu - oracle| <= 2^-20 abs_scale: the fp32
+    accumulation of the five post terms (four products and one fused
+    multiply-add chain) is accurate to about 5 * 2^-24 of that sum, so where
+    the exact result nearly cancels, 1 bf16 ulp of the tiny result is below
+    what any fp32 evaluation can reach.  Returns how many elements passed
+    only by that allowance (and prints the count when it is not zero)."""
     d = ulp_distance_bf16(g_bits, o_bits)
     bad = d > 1
+    allowed = 0
     if abs_scale is not None and np.any(bad):
         diff = np.abs(oracle.bf16_to_f64(g_bits) - oracle.bf16_to_f64(o_bits))
-        bad &= diff > 2.0 ** -20 * abs_scale
+        within = diff <= 2.0 ** -20 * abs_scale
+        allowed = int(np.count_nonzero(bad & within))
+        bad &= ~within
     if np.any(bad):
         i = np.argwhere(bad)[0]
         raise AssertionError(f"{what}: {bad.sum()} elements beyond 1 bf16 ulp; first at {tuple(i)} "
                              f"gpu=0x{int(g_bits[tuple(i)]):04x} oracle=0x{int(o_bits[tuple(i)]):04x}")
+    if allowed:
+        print(f"{what}: {allowed} of {d.size} elements beyond 1 bf16 ulp, within the fp32 cancellation "
+              f"allowance 2^-20 * sum|terms|")
+    return allowed
 
 
 def assert_bitexact(g_bits: np.ndarray, o_bits: np.ndarray, what: str):

@@ -580,12 +580,116 @@ def test_fused_chain_matches_and_overlaps_exactly(T):
         mhc.set_launch_overlap(prev)
 
 
+def _stub_sublayer_oracle(li_bits: np.ndarray, d_bits: np.ndarray) -> np.ndarray:
+    """The chain's synthetic sublayer y = bf16(float(layer_input) + D_s): the
+    two bf16 values added in fp32, the sum rounded once to bf16."""
+    s32 = (oracle.bf16_to_f64(li_bits).astype(np.float32) + oracle.bf16_to_f64(d_bits).astype(np.float32))
+    return oracle.bf16_round(s32.astype(np.float64))
+
+
+def test_config3_decode_chain_against_the_oracle():
+    """The full-model decode step: 80 seams at T = 4, each with its own
+    weights, the pre-mix carried seam to seam (delayed), a synthetic
+    sublayer between pre and post (the #56503 page: 80 seams per decode
+    step).  Every seam's outputs are checked against the oracle fed that
+    seam's GPU inputs (x and pre-mix): logits within the fp32 dot bound,
+    gates within 2e-5, layer_input within 1 bf16 ulp, x_new within 1 ulp.
+    The same chain captured in one CUDA graph (as the benchmark runs it) gives
+    the eager chain's bits.  The drift of the final x against a chain run
+    wholly in the oracle is reported."""
+    seams, T, C = 80, 4, 5120
+    params_cpu = [chain_seam_params(si) for si in range(seams)]
+    deltas_cpu = [chain_stub_delta(si, T=T) for si in range(seams)]
+    params = [_to_dev(p) for p in params_cpu]
+    deltas = [dl.cuda() for dl in deltas_cpu]
+    d0 = seam_inputs(T, seed=0)
+    cx = d0["x"].cuda()
+    cp = [d0["pre_in"].cuda(), torch.empty(T, 4, device="cuda")]
+    co = {"post": torch.empty(T, 4, device="cuda"), "comb": torch.empty(T, 4, 4, device="cuda"),
+          "layer_input": torch.empty(T, C, dtype=torch.bfloat16, device="cuda"),
+          "logits": torch.empty(T, 24, device="cuda")}
+    cy = torch.empty(T, C, dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+
+    def seam(si, st):
+        p = params[si]
+        o = dict(co, pre=cp[(si + 1) & 1])
+        mhc.pre_delayed(cx, cp[si & 1], p["fn"], p["bias"], p["alpha"], p["norm_w"], out=o, stream=st)
+        with torch.cuda.stream(st):
+            torch.add(co["layer_input"], deltas[si], out=cy)
+        mhc.post(cx, cy, co["comb"], co["post"], out=cx, stream=st)
+
+    snaps = []
+    for si in range(seams):
+        x_in, p_in = bf16_bits(cx), cp[si & 1].cpu().numpy().copy()
+        seam(si, s)
+        s.synchronize()
+        snaps.append({"x": x_in, "pre_in": p_in, "pre": cp[(si + 1) & 1].cpu().numpy().copy(),
+                      "post": co["post"].cpu().numpy().copy(), "comb": co["comb"].cpu().numpy().copy(),
+                      "logits": co["logits"].cpu().numpy().copy(), "layer_input": bf16_bits(co["layer_input"]),
+                      "y": bf16_bits(cy), "x_new": bf16_bits(cx)})
+    assert mhc.device_status() == 0
+    eager_final = cx.clone()
+
+    # the graph-captured chain from the same start
+    cx.copy_(d0["x"].cuda())
+    cp[0].copy_(d0["pre_in"].cuda())
+    torch.cuda.synchronize()
+    g = SeamGraph(lambda st: [seam(si, st) for si in range(seams)], s)
+    g.replay(1)
+    s.synchronize()
+    assert mhc.device_status() == 0
+    assert torch.equal(cx, eager_final), "graph-captured chain differs from the eager chain"
+    g.close()
+
+    for si, sn in enumerate(snaps):
+        p = params_cpu[si]
+        o = oracle.pre_delayed(sn["x"], sn["pre_in"], p["fn"].numpy(), p["bias"].numpy(), p["alpha"].numpy(),
+                               bf16_bits(p["norm_w"]), nthreads=NTHREADS)
+        what = f"seam {si}: "
+        bound = logit_bound(sn["x"], p["fn"].numpy(), p["alpha"].numpy(), o["logits"])
+        assert_logits(sn["logits"], o["logits"], bound, what + "logits")
+        assert_gates(sn["pre"], o["pre"], what + "pre")
+        assert_gates(sn["post"], o["post"], what + "post")
+        assert_gates(sn["comb"], o["comb"], what + "comb")
+        assert_bf16(sn["layer_input"], o["layer_input"], what + "layer_input")
+        assert np.array_equal(sn["y"], _stub_sublayer_oracle(sn["layer_input"], bf16_bits(deltas_cpu[si])))
+        xo, _ = oracle.post(sn["x"], sn["y"], sn["comb"], sn["post"])
+        assert_bf16(sn["x_new"], xo, what + "x_new",
+                    abs_scale=post_abs_scale(sn["x"], sn["y"], sn["comb"], sn["post"]))
+
+    # the whole chain in the oracle, for the drift report
+    x, pin = bf16_bits(d0["x"]), d0["pre_in"].numpy()
+    for si in range(seams):
+        p = params_cpu[si]
+        o = oracle.pre_delayed(x, pin, p["fn"].numpy(), p["bias"].numpy(), p["alpha"].numpy(),
+                               bf16_bits(p["norm_w"]), nthreads=NTHREADS)
+        y = _stub_sublayer_oracle(o["layer_input"], bf16_bits(deltas_cpu[si]))
+        x, _ = oracle.post(x, y, o["comb"], o["post"])
+        pin = o["pre"]
+    from parity import ulp_distance_bf16
+    dist = ulp_distance_bf16(snaps[-1]["x_new"], x)
+    hist = {int(k): int(v) for k, v in zip(*np.unique(np.minimum(dist, 8), return_counts=True))}
+    print(f"\n80-seam chain, final x against the all-oracle chain: ulp histogram "
+          f"(8 = 8 or more) {hist}; max {int(dist.max())}")
+    assert np.median(dist) <= 1
+
+
 # ------------------------------------------------- stress and full sizes ---
 
-def _check_comb_properties(comb: np.ndarray):
-    assert np.all(np.isfinite(comb))
-    assert np.all(comb >= 0)
-    np.testing.assert_allclose(comb.sum(1), 1.0, atol=1e-5)   # columns, fp32
+def _check_comb_properties(comb: np.ndarray, rows: bool = True):
+    """The Sinkhorn invariants on every token: finite, non-negative, column
+    sums 1 within 1e-6 (the last step normalises columns), and -- where the
+    method's 20 iterations converge that far, i.e. not on the stress
+    distribution -- row sums 1 within 1e-3.  Sums in fp64 of the fp32 comb."""
+    c = comb.astype(np.float64)
+    assert np.all(np.isfinite(c))
+    assert np.all(c >= 0)
+    col = np.abs(c.sum(1) - 1.0)
+    assert col.max() <= 1e-6, f"column sums off by up to {col.max():.3e}"
+    if rows:
+        row = np.abs(c.sum(2) - 1.0)
+        assert row.max() <= 1e-3, f"row sums off by up to {row.max():.3e}"
 
 
 def test_stress_small_layered():
@@ -606,7 +710,7 @@ def test_stress_small_layered():
     assert_gates(g["post"].numpy(), o["post"], "post")
     assert_bf16(g["layer_input"].view(torch.int16).numpy().view(np.uint16), o["layer_input"],
                 "layer_input")
-    _check_comb_properties(g["comb"].numpy())
+    _check_comb_properties(g["comb"].numpy(), rows=False)
     zero = np.all(xb.reshape(T, -1) == 0, axis=1)
     assert zero.sum() == T // 100
     assert np.all(g["layer_input"].view(torch.int16).numpy()[zero] == 0)
@@ -652,7 +756,17 @@ def test_config4_stress_full_size_sampled():
     for k in g:
         if g[k].dtype == torch.float32:
             assert torch.isfinite(g[k]).all(), k
-    _check_comb_properties(g["comb"].numpy())
+    # Sinkhorn invariants on all 65,536 tokens.  Twenty iterations do not
+    # bring the row sums of these +-300 comb logits within 1e-3 even in exact
+    # arithmetic (the oracle's own rows are off by 0.03 typically), so the
+    # rows are held to the oracle's Sinkhorn of the GPU's own logits instead:
+    # the whole comb within 2e-5 on every token, and the row sums with it.
+    comb = g["comb"].numpy()
+    _check_comb_properties(comb, rows=False)
+    og_all = oracle.gates_from_logits(g["logits"].numpy().astype(np.float64))
+    assert_gates(comb, og_all["comb"], "comb (every token, from gpu logits)")
+    row_gap = np.abs(comb.astype(np.float64).sum(2) - og_all["comb"].sum(2))
+    assert row_gap.max() <= 1e-5, f"row sums differ from the oracle's by up to {row_gap.max():.3e}"
     xr = gd["x"].reshape(T, -1)
     zero = (xr == 0).all(1)
     big = xr.abs().amax(1) > 100
