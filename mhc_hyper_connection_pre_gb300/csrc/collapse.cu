@@ -56,11 +56,11 @@ __device__ __forceinline__ void produce(const uint16_t* x, const float* pre, int
     int k = 0, s = 0;
     uint32_t n = 0;                               // the slot's round
     for (; k < K; ++k) {
-        if (n > 0 && !mbar_wait(&empty[s], (n - 1) & 1u, abort)) break;
-        // the slot's previous copy has landed (consumers that timed out may
-        // release a slot without waiting for it): never two copies in flight
-        // into one slot
-        if (n > 0) mbar_wait_drain(&full[s], (n - 1) & 1u);
+        // consumers that timed out release slots without waiting for their
+        // copies: nothing is issued once the flag is up (read after the
+        // empty wait, which acquires the release that followed raising it),
+        // so never two copies are in flight into one slot
+        if (n > 0 && (!mbar_wait(&empty[s], (n - 1) & 1u, abort) || *abort)) break;
         const int64_t t = b + (int64_t)k * G;
         mbar_arrive_expect_tx(&full[s], slot_bytes + 16u);
         bulk_load_hint(ring + (size_t)s * slot_bytes, x + t * (BCAST ? (int64_t)C : 4 * (int64_t)C), slot_bytes,

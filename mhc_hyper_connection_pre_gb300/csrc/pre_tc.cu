@@ -268,10 +268,7 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
         for (uint32_t q = 0; q < early; ++q) {
             const int tile = cid + (int)(q / ngroups) * ncl, grp = (int)(q % ngroups);
             mbar_arrive_expect_tx(&full[q], slot_bytes);
-#pragma unroll
-            for (int st = 0; st < nbox; ++st)
-                tma_load_3d_hint(stages + q * kSlotBytes + st * kBoxBytes, &xmap, c0 + kCols * grp, st,
-                                 tile * kTile, &full[q], pol_x);
+            tma_load_3d_hint(stages + q * kSlotBytes, &xmap, c0 + kCols * grp, tile * kTile, 0, &full[q], pol_x);
         }
     }
     if (fold)
@@ -295,18 +292,15 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
             for (; g < total_stages && !*abort; ++g) {
                 const int tile = cid + (int)(g / ngroups) * ncl, grp = (int)(g % ngroups);
                 const int s = g % kStages;
-                if (!mbar_wait(&empty[s], ((g / kStages) & 1) ^ 1, abort)) break;
-                // The slot's previous load has landed: always true once its
-                // consumers released it normally, but after a timeout they
-                // release it without waiting, and a second copy must never
-                // be in flight into the same slot.
-                mbar_wait_drain(&full[s], ((g / kStages) & 1) ^ 1);
+                // After a timeout consumers release slots without waiting for
+                // their data: a second copy must never be in flight into one
+                // slot, so nothing is issued once the flag is up.  (A consumer
+                // raises the flag before any early release, and the empty
+                // wait acquires that release, so the read below sees it.)
+                if (!mbar_wait(&empty[s], ((g / kStages) & 1) ^ 1, abort) || *abort) break;
                 unsigned char* slot = stages + s * kSlotBytes;
                 mbar_arrive_expect_tx(&full[s], slot_bytes);
-#pragma unroll
-                for (int st = 0; st < nbox; ++st)
-                    tma_load_3d_hint(slot + st * kBoxBytes, &xmap, c0 + kCols * grp, st, tile * kTile, &full[s],
-                                     pol_x);
+                tma_load_3d_hint(slot, &xmap, c0 + kCols * grp, tile * kTile, 0, &full[s], pol_x);
                 bulk_load_hint(slot + kXBytes, wreg + grp * kWStage, kWStage, &full[s], pol_w);
             }
             // drain: the last load of every slot has landed before the CTA
@@ -737,14 +731,17 @@ cudaError_t launch_pre_tc(const uint16_t* x, const float* pre_in, const float* f
                           const void* packed) {
     PFN_encodeTiled enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
-    // x viewed as [T][4][C] bf16 (broadcast: [T][1][C], every stream's box
-    // taken at stream 0); box = 16 columns (32 B) x 1 stream x 128 tokens,
-    // written to shared memory with the 32-byte swizzle the MMA reads.
+    // x viewed as (column, token, stream) -- the token stride 4C and the
+    // stream stride C elements (broadcast: one stream) -- so that one box of
+    // 16 columns (32 B) x 128 tokens x all streams lands in shared memory as
+    // one 4 KB tile per stream, 32-byte swizzled as the MMA reads it: a
+    // single TMA instruction per stage (the producer's issue time per stage
+    // is on the kernel's critical path).
     alignas(64) CUtensorMap map;
     const cuuint64_t ns = broadcast ? 1 : 4;
-    const cuuint64_t dims[3] = {(cuuint64_t)C, ns, (cuuint64_t)T};
-    const cuuint64_t strides[2] = {(cuuint64_t)C * 2, (cuuint64_t)C * 2 * ns};
-    const cuuint32_t box[3] = {(cuuint32_t)tc::kCols, 1, (cuuint32_t)tc::kTile};
+    const cuuint64_t dims[3] = {(cuuint64_t)C, (cuuint64_t)T, ns};
+    const cuuint64_t strides[2] = {(cuuint64_t)C * 2 * ns, (cuuint64_t)C * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)tc::kCols, (cuuint32_t)tc::kTile, (cuuint32_t)ns};
     const cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(x), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,

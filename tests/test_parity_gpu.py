@@ -677,19 +677,29 @@ def test_config3_decode_chain_against_the_oracle():
 
 # ------------------------------------------------- stress and full sizes ---
 
-def _check_comb_properties(comb: np.ndarray, rows: bool = True):
+def _check_comb_properties(comb: np.ndarray, logits: np.ndarray):
     """The Sinkhorn invariants on every token: finite, non-negative, column
-    sums 1 within 1e-6 (the last step normalises columns), and -- where the
-    method's 20 iterations converge that far, i.e. not on the stress
-    distribution -- row sums 1 within 1e-3.  Sums in fp64 of the fp32 comb."""
+    sums 1 within 1e-6 (the last step normalises columns; sums in fp64 of the
+    fp32 comb).  Row sums: twenty iterations do not bring every row within
+    1e-3 even in exact arithmetic once the comb logits reach the tens (the
+    C = 5120 workloads: about a third of the tokens at config 2, most of
+    them under stress), so every token's comb is held to the oracle's
+    Sinkhorn of the GPU's own logits -- within 2e-5 per entry, row sums
+    within 1e-5 of the oracle's -- and the 1e-3 row bar to the tokens where
+    the oracle itself meets it."""
     c = comb.astype(np.float64)
     assert np.all(np.isfinite(c))
     assert np.all(c >= 0)
     col = np.abs(c.sum(1) - 1.0)
     assert col.max() <= 1e-6, f"column sums off by up to {col.max():.3e}"
-    if rows:
-        row = np.abs(c.sum(2) - 1.0)
-        assert row.max() <= 1e-3, f"row sums off by up to {row.max():.3e}"
+    og = oracle.gates_from_logits(np.asarray(logits, np.float64))["comb"]
+    assert_gates(comb, og, "comb (every token, from gpu logits)")
+    orow = og.sum(2)
+    row_gap = np.abs(c.sum(2) - orow)
+    assert row_gap.max() <= 1e-5, f"row sums differ from the oracle's by up to {row_gap.max():.3e}"
+    conv = np.all(np.abs(orow - 1.0) <= 1e-3, axis=1)
+    row = np.abs(c.sum(2) - 1.0)[conv]
+    assert row.size == 0 or row.max() <= 1e-3 + 1e-5, f"row sums off by up to {row.max():.3e}"
 
 
 def test_stress_small_layered():
@@ -710,7 +720,7 @@ def test_stress_small_layered():
     assert_gates(g["post"].numpy(), o["post"], "post")
     assert_bf16(g["layer_input"].view(torch.int16).numpy().view(np.uint16), o["layer_input"],
                 "layer_input")
-    _check_comb_properties(g["comb"].numpy(), rows=False)
+    _check_comb_properties(g["comb"].numpy(), g["logits"].numpy())
     zero = np.all(xb.reshape(T, -1) == 0, axis=1)
     assert zero.sum() == T // 100
     assert np.all(g["layer_input"].view(torch.int16).numpy()[zero] == 0)
@@ -738,7 +748,7 @@ def test_config2_prefill_full_size_sampled():
     g = {k: v.cpu() for k, v in out.items()}
     o, xb = _oracle_pre(gd, rows)
     _check_pre(g, o, xb, gd, fold=True, rows=rows)
-    _check_comb_properties(g["comb"].numpy())
+    _check_comb_properties(g["comb"].numpy(), g["logits"].numpy())
     comb, pg = g["comb"].numpy()[rows], g["post"].numpy()[rows]
     yb = bf16_bits(gd["y"])[rows]
     o_bits, _ = oracle.post(xb, yb, comb, pg)
@@ -756,17 +766,10 @@ def test_config4_stress_full_size_sampled():
     for k in g:
         if g[k].dtype == torch.float32:
             assert torch.isfinite(g[k]).all(), k
-    # Sinkhorn invariants on all 65,536 tokens.  Twenty iterations do not
-    # bring the row sums of these +-300 comb logits within 1e-3 even in exact
-    # arithmetic (the oracle's own rows are off by 0.03 typically), so the
-    # rows are held to the oracle's Sinkhorn of the GPU's own logits instead:
-    # the whole comb within 2e-5 on every token, and the row sums with it.
-    comb = g["comb"].numpy()
-    _check_comb_properties(comb, rows=False)
-    og_all = oracle.gates_from_logits(g["logits"].numpy().astype(np.float64))
-    assert_gates(comb, og_all["comb"], "comb (every token, from gpu logits)")
-    row_gap = np.abs(comb.astype(np.float64).sum(2) - og_all["comb"].sum(2))
-    assert row_gap.max() <= 1e-5, f"row sums differ from the oracle's by up to {row_gap.max():.3e}"
+    # Sinkhorn invariants on all 65,536 tokens (rows held to the oracle's
+    # Sinkhorn of the GPU's logits: the +-300 stress logits do not converge
+    # in 20 iterations even in exact arithmetic)
+    _check_comb_properties(g["comb"].numpy(), g["logits"].numpy())
     xr = gd["x"].reshape(T, -1)
     zero = (xr == 0).all(1)
     big = xr.abs().amax(1) > 100

@@ -143,4 +143,4 @@ def test_noalloc_allocates_nothing_and_checks_the_device(lib):
     assert mhc.device_status() == 0
     hx = d["x"].pin_memory()
     bad = dict(g, x=hx)
-    assert _noalloc(lib, bad, o) == INVALID
+    assert _noalloc(lib, bad, o, stream=torch.cuda.current_stream().cuda_stream) == INVALID
