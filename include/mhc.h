@@ -309,7 +309,7 @@ mhc_status mhc_seam_host(const uint16_t *x_h, const uint16_t *y_h, const float *
  * conversion disappears.
  *
  * mhc_pre_packed_bytes -- size of the packed planes for (n, C): 16 regions
- *   of C/256 x 9 KB (2.95 MB at C = 5120); 0 when the tensor-core kernel does
+ *   of ceil(C/512) x 18 KB (2.95 MB at C = 5120); 0 when the tensor-core kernel does
  *   not take C (C a multiple of 256 up to 5120, n == 4).  Host only.
  * mhc_pre_pack -- write the planes of fn [2n+n^2, n*C] fp32 (device) to
  *   packed (device, 256-byte aligned, at least mhc_pre_packed_bytes; must not

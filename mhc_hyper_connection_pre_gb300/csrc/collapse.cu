@@ -11,10 +11,11 @@
 // pre), so this kernel repeats that kernel's arithmetic in the same order:
 //  * h = ((p0 x0 + p1 x1) + p2 x2) + p3 x3, every product and sum rounded;
 //  * sum h^2: the tensor-core kernel splits the C columns into 16 slices (one
-//    per CTA of a cluster) of C/256 stages of 16 columns; a stage belongs to
-//    token-row group (it * stages + stage) & 1, `it` being the tile's round
-//    in its cluster (tile / clusters); each group accumulates its stages in
-//    order with a packed fma (even and odd columns in the two lanes), adds
+//    per CTA of a cluster) of ceil(C/512) stages of 32 columns (the last one
+//    16 when C/16 is an odd multiple of 16); a stage belongs to token-row
+//    group (it * stages + stage) & 1, `it` being the tile's round in its
+//    cluster (tile / clusters); each group accumulates its stages' columns
+//    in order with a packed fma (even and odd columns in the two lanes), adds
 //    the two lanes, and the finaliser sums the 32 partials in (slice, group)
 //    order.  Here lane q = 2 * slice + group of a warp forms partial q the
 //    same way, and every lane sums the 32 partials in lane order;
@@ -257,7 +258,7 @@ collapse_fold_pipe_kernel(const uint16_t* __restrict__ x, const float* __restric
     uint64_t* sready = hfull + kParks;
     volatile int* abort = reinterpret_cast<volatile int*>(sready + kParks);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int slice = C / 16, stages = slice / 16, chunks = C / 8, spc = slice / 8;
+    const int slice = C / 16, stages = (slice + 31) / 32, chunks = C / 8, spc = slice / 8;
     const uint32_t row_bytes = 2u * (uint32_t)C;
     const int G = (int)gridDim.x, b = (int)blockIdx.x;
     const int K = b < T ? (T - 1 - b) / G + 1 : 0;         // this CTA's tokens: b, b + G, ...
@@ -298,13 +299,17 @@ collapse_fold_pipe_kernel(const uint16_t* __restrict__ x, const float* __restric
             f32x2 sh2 = make_f32x2(0.f, 0.f);
 #pragma unroll 2
             for (int stg = first; stg < stages; stg += 2) {
-                // the stage's 16 columns: chunks 2 stg and 2 stg + 1 of the slice
-                const float4 v[4] = {hA[2 * stg], hB[2 * stg], hA[2 * stg + 1], hB[2 * stg + 1]};
+                // the stage's 32 columns (16 in a half last stage): chunks
+                // 4 stg .. 4 stg + 3 of the slice, each as its two halves
+                const int c8end = 4 * stg + (spc - 4 * stg < 4 ? spc - 4 * stg : 4);
+                for (int c8 = 4 * stg; c8 < c8end; ++c8) {
+                    const float4 v[2] = {hA[c8], hB[c8]};
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const f32x2 a = make_f32x2(v[c].x, v[c].y), bb = make_f32x2(v[c].z, v[c].w);
-                    sh2 = fma_rn2(a, a, sh2);
-                    sh2 = fma_rn2(bb, bb, sh2);
+                    for (int c = 0; c < 2; ++c) {
+                        const f32x2 a = make_f32x2(v[c].x, v[c].y), bb = make_f32x2(v[c].z, v[c].w);
+                        sh2 = fma_rn2(a, a, sh2);
+                        sh2 = fma_rn2(bb, bb, sh2);
+                    }
                 }
             }
             float a0, a1;

@@ -13,7 +13,7 @@
 // allocating routine.
 //
 // Limit: the array holds the fn planes for at most kNoAllocClusters 16-CTA
-// clusters (2 x 16 x 20 x 9 KB = 5,898,240 bytes for C = 5120), so the kernel
+// clusters (2 x 16 x 10 x 18 KB = 5,898,240 bytes for C = 5120), so the kernel
 // runs on at most 32 SMs here: correct for any token count, slower for large
 // ones than mhc_pre_delayed on the whole GPU.  Every GPU that loads the
 // library holds the array until the process exits.
@@ -40,9 +40,9 @@ namespace {
 constexpr int kNoAllocClusters = 2;
 constexpr size_t kNoAllocBytes = MHC_NOALLOC_SCRATCH_BYTES;
 // Every shape the entry point accepts fits: C is at most 5120 (the
-// tensor-core kernel's limit, checked first), i.e. at most 20 stages of
-// 9 KB of planes per CTA, for at most kNoAllocClusters clusters of 16 CTAs.
-static_assert((size_t)kNoAllocClusters * 16 * 20 * 9216 <= kNoAllocBytes,
+// tensor-core kernel's limit, checked first), i.e. at most 10 stages of
+// 18 KB of planes per CTA, for at most kNoAllocClusters clusters of 16 CTAs.
+static_assert((size_t)kNoAllocClusters * 16 * 10 * 18432 <= kNoAllocBytes,
               "the scratch array holds the planes of every accepted shape");
 
 // The scratch itself.  Its name is a host-side stand-in in host code, not a

@@ -60,15 +60,16 @@ namespace tc {
 
 constexpr int kCtas = 16;                         // CTAs per cluster = column slices
 constexpr int kTile = 128;                        // tokens per tile = MMA M
-constexpr int kStages = 8;                        // shared-memory ring depth
+constexpr int kStages = 4;                        // shared-memory ring depth
 static_assert(kStages % 2 == 0, "each ring slot must always belong to the same token-row group");
-constexpr int kCols = 16;                         // columns per stream per stage
-constexpr int kBoxBytes = kTile * kCols * 2;      // 4 KB: one stream of one stage
-constexpr int kXBytes = 4 * kBoxBytes;            // 16 KB of x per stage
-constexpr int kMaxGroups = 20;                    // stages per tile (C <= 5120)
-constexpr int kWBlock = 9 * 256;                  // per (stage, stream): 9 row-atoms of 8 x 32 B
-constexpr int kWStage = 4 * kWBlock;              // 9 KB of fn planes per stage
-constexpr int kSlotBytes = kXBytes + kWStage;     // 25 KB ring slot: x boxes, then fn blocks
+constexpr int kCols = 32;                         // columns per stream per stage (64-byte rows)
+constexpr int kHalf = 16;                         // columns per K16 MMA step / per output store
+constexpr int kBoxBytes = kTile * kCols * 2;      // 8 KB: one stream of one stage
+constexpr int kXBytes = 4 * kBoxBytes;            // 32 KB of x per stage
+constexpr int kMaxGroups = 10;                    // stages per tile (C <= 5120)
+constexpr int kWBlock = 9 * 512;                  // per (stage, stream): 9 row-atoms of 8 x 64 B
+constexpr int kWStage = 4 * kWBlock;              // 18 KB of fn planes per stage
+constexpr int kSlotBytes = kXBytes + kWStage;     // 50 KB ring slot: x boxes, then fn blocks
 constexpr int kN = 80;                            // MMA N: 72 plane rows + 8 ignored
 constexpr int kDots = 24;                         // projection dot products per token
 constexpr int kFinTok = kTile / kCtas;            // tokens finalized per CTA per tile
@@ -79,23 +80,25 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDCol0 = 0, kDCol1 = 96, kHCol = 192;  // accumulators, parked h (320 columns)
 
 constexpr int kOffStages = 0;                                         // 1 KB aligned
-// The last slot's ignored 10th B-operand atom reads 256 B past the ring: the
+// The last slot's ignored 10th B-operand atom reads 512 B past the ring: the
 // dots inbox follows it, so that read stays inside shared memory.
 constexpr int kOffDots = kOffStages + kStages * kSlotBytes;           // [16 src][8 tok][24] dots
 constexpr int kOffSq = kOffDots + kCtas * kFinTok * kDots * 4;        // [16 src][8 tok][2 grp][2] sums
 constexpr int kOffScale = kOffSq + kCtas * kFinTok * 2 * 2 * 4;       // [128] fold scales
 constexpr int kOffNormW = kOffScale + kTile * 4;                      // [C/16] bf16
-// [8 row warps][32 tok][16 col] bf16 staging tiles, 32-byte swizzled: the
-// swizzle pattern follows address bit 7, so each tile starts 1 KB aligned
+// [8 row warps][32 tok][16 col] bf16 staging tiles (half a stage each),
+// 32-byte swizzled: the swizzle pattern follows address bit 7, so each tile
+// starts 1 KB aligned
+constexpr int kOutTile = 32 * kHalf * 2;                              // 1 KB
 constexpr int kOffOut = (kOffNormW + kMaxGroups * kCols * 2 + 1023) / 1024 * 1024;
-constexpr int kOffBars = kOffOut + kRowWarps * 32 * kCols * 2;
+constexpr int kOffBars = kOffOut + kRowWarps * kOutTile;
 // full[8], empty[8], dfull[2], dempty[2], sq_full, dots_full, scale_full, dots_free, drain
 constexpr int kNumBars = 2 * kStages + 2 + 2 + 5;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;                     // tmem base, abort flag
 constexpr int kSmemBytes = kOffMisc + 16;
 static_assert(kOffBars % 8 == 0, "mbarriers need 8-byte alignment");
-static_assert(kSlotBytes % 1024 == 0 && kBoxBytes % 1024 == 0 && kXBytes % 256 == 0 && kWBlock % 256 == 0,
-              "swizzled TMA boxes and MMA operand atoms must stay 256-byte aligned");
+static_assert(kSlotBytes % 1024 == 0 && kBoxBytes % 1024 == 0 && kXBytes % 512 == 0 && kWBlock % 512 == 0,
+              "64-byte-swizzled TMA boxes and MMA operand atoms must stay 512-byte aligned");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Args {
@@ -114,17 +117,17 @@ struct Args {
     float* comb_out;
     uint16_t* layer_input;
     float* logits_out;
-    unsigned char* ws;  // fn planes, one region of ngroups x 9 KB per (cluster, rank)
+    unsigned char* ws;  // fn planes, one region of ngroups x 18 KB per (cluster, rank)
     const unsigned char* packed;  // or planes packed ahead (one region per rank, shared by the clusters)
     int ntiles;
 };
 
 // Byte offset, inside a CTA's fn-plane region, of 16-byte chunk c (k =
-// 8c..8c+7 of the stage's 16 columns) of plane row n for stage g and stream
-// s: blocks [g][s] of 9 atoms x 256 B, row n in atom n/8, 32-byte swizzle in
+// 8c..8c+7 of the stage's 32 columns) of plane row n for stage g and stream
+// s: blocks [g][s] of 9 atoms x 512 B, row n in atom n/8, 64-byte swizzle in
 // the atom (the layout the MMA reads once the block sits in a ring slot).
 __device__ __forceinline__ int w_off(int g, int s, int n, int c) {
-    return (g * 4 + s) * kWBlock + (n >> 3) * 256 + sw32_off(n & 7, c);
+    return (g * 4 + s) * kWBlock + (n >> 3) * 512 + sw64_off(n & 7, c);
 }
 
 __device__ __forceinline__ uint16_t bf16_bits_rn(float v) {
@@ -153,27 +156,27 @@ __device__ __forceinline__ void split3(const float (&w)[8], uint32_t (&pk)[3][4]
     }
 }
 
-// fn K-slice [c0, c0 + 16 ngroups) of all 24 rows and 4 streams -> the three
-// bf16 planes in the MMA operand layout at wreg (ngroups x 9 KB), by the 352
-// threads of a CTA.  Items of 8 columns; a warp takes units of 8 rows x 4
-// neighbouring column chunks (lane = row * 4 + chunk), so that a load covers
-// 8 runs of 128 contiguous bytes of fn and a plane store two whole 256-byte
-// row atoms; every thread first loads all of its items (one latency), then
-// splits and stores them.
-__device__ __forceinline__ void write_planes(const float* __restrict__ fn, int C, int c0, int ngroups,
-                                             unsigned char* wreg, int warp, int lane) {
+// fn K-slice [c0, c0 + slice) of all 24 rows and 4 streams -> the three
+// bf16 planes in the MMA operand layout at wreg (ngroups x 18 KB), by the 352
+// threads of a CTA.  A warp takes units of 8 rows x the 4 column chunks of
+// one (stage, stream) (lane = row * 4 + chunk), so that a load covers 8 runs
+// of 128 contiguous bytes of fn and a plane store one whole 512-byte row
+// atom; every thread first loads all of its items (one latency), then splits
+// and stores them.  Chunks past the slice (the second half of a 16-column
+// last stage) are neither read nor written: the MMA skips that half.
+__device__ __forceinline__ void write_planes(const float* __restrict__ fn, int C, int c0, int slice,
+                                             int ngroups, unsigned char* wreg, int warp, int lane) {
     const int64_t K = 4 * (int64_t)C;
-    constexpr int kUnitsMax = 11;   // ceil(4 streams x 10 chunk quads x 3 row octets / 11 warps)
-    const int nunits = 4 * ((ngroups + 1) / 2) * 3;   // an odd last chunk quad is half empty
-    const int mrow = lane >> 2, gc = lane & 3;
+    constexpr int kUnitsMax = 11;   // ceil(10 stages x 4 streams x 3 row octets / 11 warps)
+    const int nunits = ngroups * 4 * 3;
+    const int mrow = lane >> 2, c = lane & 3;
     float w[kUnitsMax][8];
 #pragma unroll
     for (int j = 0; j < kUnitsMax; ++j) {
         const int u = warp + j * (kThreads / 32);
-        if (u < nunits) {
-            const int mo = u % 3, rest = u / 3, st = rest & 3, gp = rest >> 2;
-            const int m = 8 * mo + mrow, g = 2 * gp + (gc >> 1), c = gc & 1;
-            if (g >= ngroups) continue;
+        const int mo = u % 3, rest = u / 3, st = rest & 3, g = rest >> 2;
+        if (u < nunits && kCols * g + 8 * c < slice) {
+            const int m = 8 * mo + mrow;
             const float4* src = reinterpret_cast<const float4*>(fn + (int64_t)m * K + (int64_t)st * C + c0 +
                                                                 kCols * g + 8 * c);
             const float4 u0 = __ldg(src), u1 = __ldg(src + 1);
@@ -184,10 +187,9 @@ __device__ __forceinline__ void write_planes(const float* __restrict__ fn, int C
 #pragma unroll
     for (int j = 0; j < kUnitsMax; ++j) {
         const int u = warp + j * (kThreads / 32);
-        if (u < nunits) {
-            const int mo = u % 3, rest = u / 3, st = rest & 3, gp = rest >> 2;
-            const int m = 8 * mo + mrow, g = 2 * gp + (gc >> 1), c = gc & 1;
-            if (g >= ngroups) continue;
+        const int mo = u % 3, rest = u / 3, st = rest & 3, g = rest >> 2;
+        if (u < nunits && kCols * g + 8 * c < slice) {
+            const int m = 8 * mo + mrow;
             uint32_t pk[3][4];
             split3(w[j], pk);
 #pragma unroll
@@ -223,7 +225,10 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_ctarank();
     const int cid = (int)cluster_id_x(), ncl = (int)ncluster_x();
-    const int C = a.C, K = 4 * C, slice = C / kCtas, ngroups = slice / kCols, c0 = (int)rank * slice;
+    // a slice of C/16 columns (a multiple of 16) walks ceil(slice/32) stages;
+    // an odd multiple of 16 ends in a half stage of 16 columns
+    const int C = a.C, K = 4 * C, slice = C / kCtas, ngroups = (slice + kCols - 1) / kCols;
+    const int c0 = (int)rank * slice;
     const bool fold = a.norm_w != nullptr;
     // broadcast seam: one x box per stage, read as all four streams
     constexpr int nbox = BCAST ? 1 : 4, xbox = BCAST ? 0 : kBoxBytes;
@@ -259,7 +264,7 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
 
     // ---- fn K-slice -> three bf16 planes in the operand layout, written to
     //      this CTA's workspace region (unless packed ahead of the call)
-    if (!a.packed) write_planes(a.fn, C, c0, ngroups, wreg, warp, lane);
+    if (!a.packed) write_planes(a.fn, C, c0, slice, ngroups, wreg, warp, lane);
     // the first ring slots' x boxes do not depend on fn: start them now,
     // after this CTA's fn reads (issued at the start they slowed those by
     // 2 us) and still well before the planes can be loaded
@@ -323,15 +328,20 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
                 const uint32_t dt = tmem + (d ? kDCol1 : kDCol0);
                 for (int grp = 0; grp < ngroups; ++grp, ++g) {
                     const int s = g % kStages;
+                    // a stage is two K16 steps (the halves of its 64-byte rows),
+                    // a half stage at the end of an odd slice one
+                    const int nk = kCols * grp + kHalf < slice ? 2 : 1;
                     mbar_wait(&full[s], (g / kStages) & 1, abort);
                     tc_fence_after();
+                    const uint32_t slot = sbase + s * kSlotBytes;
 #pragma unroll
-                    for (int st = 0; st < 4; ++st) {
-                        const uint32_t slot = sbase + s * kSlotBytes;
-                        const uint64_t ad = smem_desc(slot + st * xbox, 16, 256, kLayoutSwizzle32B);
-                        const uint64_t bd = smem_desc(slot + kXBytes + st * kWBlock, 16, 256, kLayoutSwizzle32B);
-                        mma_bf16(dt, ad, bd, idesc, (grp | st) != 0);
-                    }
+                    for (int st = 0; st < 4; ++st)
+                        for (int k = 0; k < nk; ++k) {
+                            const uint64_t ad = smem_desc(slot + st * xbox + 32 * k, 16, 512, kLayoutSwizzle64B);
+                            const uint64_t bd =
+                                smem_desc(slot + kXBytes + st * kWBlock + 32 * k, 16, 512, kLayoutSwizzle64B);
+                            mma_bf16(dt, ad, bd, idesc, (grp | st | k) != 0);
+                        }
                     mma_commit(&empty[s]);
                 }
                 mma_commit(&dfull[d]);
@@ -353,14 +363,16 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
         const uint32_t dots_dst = mapa(smem_u32(dots_in + ((int)rank * kFinTok + slot) * kDots), fin);
         const uint32_t dots_bar = mapa(smem_u32(dots_full), fin);
         const bool armer = (warp == 2 && lane == 0);   // arms this CTA's scale_full each tile
-        // byte offsets of this token's two 16-byte chunks in a 4 KB stream box
-        const int xo0 = (trow >> 3) * 256 + sw32_off(trow & 7, 0);
-        const int xo1 = (trow >> 3) * 256 + sw32_off(trow & 7, 1);
+        // byte offsets of this token's four 16-byte chunks (8 columns each)
+        // in an 8 KB stream box: 64-byte rows, 64-byte swizzle
+        int xo[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) xo[c] = (trow >> 3) * 512 + sw64_off(trow & 7, c);
         // layer_input leaves through a per-warp 32-token x 16-column staging
-        // tile (32-byte swizzle) and one TMA tensor store per warp and stage:
-        // full 32-byte sectors instead of 32 scattered 16-byte stores per
-        // instruction; rows past T are clipped by the store.
-        unsigned char* ostage = smem + kOffOut + (warp - 2) * (32 * kCols * 2);
+        // tile (32-byte swizzle) and one TMA tensor store per warp and half
+        // stage: full 32-byte sectors instead of 32 scattered 16-byte stores
+        // per instruction; rows past T are clipped by the store.
+        unsigned char* ostage = smem + kOffOut + (warp - 2) * kOutTile;
         const int oo0 = (lane >> 3) * 256 + sw32_off(lane & 7, 0);
         const int oo1 = (lane >> 3) * 256 + sw32_off(lane & 7, 1);
         // stg: the warp's own staging tile (reused: wait for the previous
@@ -383,17 +395,17 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
             }
         };
         // The folded store of tile i is deferred into tile i+1's stages: at a
-        // stage the thread first reads back tile i's parked h of those 16
-        // columns, scales, rounds and stores it, then parks tile i+1's h.
+        // stage half the thread first reads back tile i's parked h of those
+        // 16 columns, scales, rounds and stores it, then parks tile i+1's h.
         bool have_prev = false;
         int64_t t_prev = 0;
         float sc_prev = 1.f;
-        auto store_folded = [&](int grp, unsigned char* stg = nullptr) {
+        auto store_folded = [&](int grp, int hf, unsigned char* stg = nullptr) {
             uint32_t r[16];
-            tmem_ld16(tl + kHCol + kCols * grp, r);
+            tmem_ld16(tl + kHCol + kCols * grp + kHalf * hf, r);
             tmem_wait_ld();
             tmem_regs_ready(r);
-            const uint4* wv = reinterpret_cast<const uint4*>(nw_s + kCols * grp);
+            const uint4* wv = reinterpret_cast<const uint4*>(nw_s + kCols * grp + kHalf * hf);
             const f32x2 sc2 = make_f32x2(sc_prev, sc_prev);
             f32x2 o[8];
 #pragma unroll
@@ -406,7 +418,52 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
                     o[4 * c + e] = mul_rn2(mul_rn2(hv, sc2), bf16x2_to_f32x2(ww[e]));   // (h * s) * w
                 }
             }
-            store_out(o, c0 + kCols * grp, t_prev - lane, stg);
+            store_out(o, c0 + kCols * grp + kHalf * hf, t_prev - lane, stg);
+        };
+        // pair e (columns 2e, 2e+1) of a half's 16 columns: word e & 3 of chunk e >> 2
+        auto pair_of = [](const uint4 (&ch)[2], int e) -> uint32_t {
+            const uint4 v = ch[e >> 2];
+            return (e & 3) == 0 ? v.x : (e & 3) == 1 ? v.y : (e & 3) == 2 ? v.z : v.w;
+        };
+        // collapse 16 columns in scalar fp32, every product and sum rounded
+        // on its own, stream order (the bit-exact reference order); the sums
+        // of squares use the packed pipe in a fixed order
+        auto collapse16 = [&](const uint4 (&xr)[4][2], const float (&p)[4], f32x2 (&h)[8], f32x2& sx2,
+                              f32x2& sh2) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                f32x2 xv[4];
+#pragma unroll
+                for (int st = 0; st < 4; ++st) xv[st] = bf16x2_to_f32x2(pair_of(xr[st], e));
+                float x0l, x0h, x1l, x1h, x2l, x2h, x3l, x3h;
+                split_f32x2(xv[0], x0l, x0h);
+                split_f32x2(xv[1], x1l, x1h);
+                split_f32x2(xv[2], x2l, x2h);
+                split_f32x2(xv[3], x3l, x3h);
+                float vl = __fmul_rn(p[0], x0l), vh = __fmul_rn(p[0], x0h);
+                vl = __fadd_rn(vl, __fmul_rn(p[1], x1l));
+                vh = __fadd_rn(vh, __fmul_rn(p[1], x1h));
+                vl = __fadd_rn(vl, __fmul_rn(p[2], x2l));
+                vh = __fadd_rn(vh, __fmul_rn(p[2], x2h));
+                vl = __fadd_rn(vl, __fmul_rn(p[3], x3l));
+                vh = __fadd_rn(vh, __fmul_rn(p[3], x3h));
+                const f32x2 v = make_f32x2(vl, vh);
+                h[e] = v;
+                sh2 = fma_rn2(v, v, sh2);
+#pragma unroll
+                for (int st = 0; st < 4; ++st) sx2 = fma_rn2(xv[st], xv[st], sx2);
+            }
+        };
+        auto park = [&](int grp, int hf, const f32x2 (&h)[8]) {
+            uint32_t hb[16];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                float lo, hi;
+                split_f32x2(h[e], lo, hi);
+                hb[2 * e] = __float_as_uint(lo);
+                hb[2 * e + 1] = __float_as_uint(hi);
+            }
+            tmem_st16(tl + kHCol + kCols * grp + kHalf * hf, hb);
         };
         uint32_t g = 0;
         int it = 0;
@@ -423,67 +480,59 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
             for (int grp = 0; grp < ngroups; ++grp, ++g) {
                 if ((int)(g & 1) != grpsel) continue;  // stages alternate between the two groups
                 const int s = g % kStages;                // (kStages is even: slot s -> group s % 2)
+                const bool two = kCols * grp + kHalf < slice;   // a full stage, or a half stage at the end
                 mbar_wait(&full[s], (g / kStages) & 1, abort);
                 const unsigned char* sb = stages + s * kSlotBytes;
-                // x of the token: 4 streams x 16 columns as 8 column pairs each
-                f32x2 xv[4][8];
+                // x of the token: 4 streams x 32 (or 16) columns, raw bf16 pairs
+                uint4 x0[4][2], x1[4][2];
 #pragma unroll
-                for (int st = 0; st < 4; ++st) {
-                    const uint4 lo = *reinterpret_cast<const uint4*>(sb + st * xbox + xo0);
-                    const uint4 hi = *reinterpret_cast<const uint4*>(sb + st * xbox + xo1);
-                    xv[st][0] = bf16x2_to_f32x2(lo.x); xv[st][1] = bf16x2_to_f32x2(lo.y);
-                    xv[st][2] = bf16x2_to_f32x2(lo.z); xv[st][3] = bf16x2_to_f32x2(lo.w);
-                    xv[st][4] = bf16x2_to_f32x2(hi.x); xv[st][5] = bf16x2_to_f32x2(hi.y);
-                    xv[st][6] = bf16x2_to_f32x2(hi.z); xv[st][7] = bf16x2_to_f32x2(hi.w);
-                }
+                for (int st = 0; st < 4; ++st)
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) x0[st][c] = *reinterpret_cast<const uint4*>(sb + st * xbox + xo[c]);
+                if (two)
+#pragma unroll
+                    for (int st = 0; st < 4; ++st)
+#pragma unroll
+                        for (int c = 0; c < 2; ++c)
+                            x1[st][c] = *reinterpret_cast<const uint4*>(sb + st * xbox + xo[2 + c]);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
                 if (GATES) {
-                    // gates only: the sum of squares in the same order as
+                    // gates only: the sums of squares in the same order as
                     // below (the same RMS scale, so the same gates)
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
 #pragma unroll
-                        for (int st = 0; st < 4; ++st) sx2 = fma_rn2(xv[st][e], xv[st][e], sx2);
+                        for (int st = 0; st < 4; ++st) {
+                            const f32x2 v = bf16x2_to_f32x2(pair_of(x0[st], e));
+                            sx2 = fma_rn2(v, v, sx2);
+                        }
+                    if (two)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+#pragma unroll
+                            for (int st = 0; st < 4; ++st) {
+                                const f32x2 v = bf16x2_to_f32x2(pair_of(x1[st], e));
+                                sx2 = fma_rn2(v, v, sx2);
+                            }
                     continue;
                 }
-                // collapse in scalar fp32, every product and sum rounded on its
-                // own, stream order (the bit-exact reference order); the sums
-                // of squares use the packed pipe in a fixed order
-                f32x2 h[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    float x0l, x0h, x1l, x1h, x2l, x2h, x3l, x3h;
-                    split_f32x2(xv[0][e], x0l, x0h);
-                    split_f32x2(xv[1][e], x1l, x1h);
-                    split_f32x2(xv[2][e], x2l, x2h);
-                    split_f32x2(xv[3][e], x3l, x3h);
-                    float vl = __fmul_rn(p[0], x0l), vh = __fmul_rn(p[0], x0h);
-                    vl = __fadd_rn(vl, __fmul_rn(p[1], x1l));
-                    vh = __fadd_rn(vh, __fmul_rn(p[1], x1h));
-                    vl = __fadd_rn(vl, __fmul_rn(p[2], x2l));
-                    vh = __fadd_rn(vh, __fmul_rn(p[2], x2h));
-                    vl = __fadd_rn(vl, __fmul_rn(p[3], x3l));
-                    vh = __fadd_rn(vh, __fmul_rn(p[3], x3h));
-                    const f32x2 v = make_f32x2(vl, vh);
-                    h[e] = v;
-                    sh2 = fma_rn2(v, v, sh2);
-#pragma unroll
-                    for (int st = 0; st < 4; ++st) sx2 = fma_rn2(xv[st][e], xv[st][e], sx2);
-                }
-                if (fold) {
-                    if (have_prev) store_folded(grp);
-                    uint32_t hb[16];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        float lo, hi;
-                        split_f32x2(h[e], lo, hi);
-                        hb[2 * e] = __float_as_uint(lo);
-                        hb[2 * e + 1] = __float_as_uint(hi);
+                // first half: fold tile i-1's columns, collapse, park; the
+                // second half is collapsed before its fold so that the first
+                // half's store has two collapses' time to read its staging
+                f32x2 h0[8], h1[8];
+                if (fold && have_prev) store_folded(grp, 0);
+                collapse16(x0, p, h0, sx2, sh2);
+                if (fold) park(grp, 0, h0);
+                else store_out(h0, c0 + kCols * grp, t - lane);
+                if (two) {
+                    collapse16(x1, p, h1, sx2, sh2);
+                    if (fold) {
+                        if (have_prev) store_folded(grp, 1);
+                        park(grp, 1, h1);
+                    } else {
+                        store_out(h1, c0 + kCols * grp + kHalf, t - lane);
                     }
-                    tmem_st16(tl + kHCol + kCols * grp, hb);
-                } else {
-                    store_out(h, c0 + kCols * grp, t - lane);
                 }
             }
             float sx, sh;
@@ -540,13 +589,15 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
             tc_fence_after();
         }
         if (fold && !GATES && have_prev) {
-            // flush the last tile: this warp's share of the column groups,
-            // each through its own staging tile in the now idle ring (every
-            // load has landed and, past the tile-end barrier, every MMA that
-            // read the ring has completed), so no store waits for another
-            unsigned char* fstage = stages + (warp - 2) * ((kMaxGroups + 1) / 2) * (32 * kCols * 2);
-            for (int grp = grpsel, k = 0; grp < ngroups; grp += 2, ++k)
-                store_folded(grp, fstage + k * (32 * kCols * 2));
+            // flush the last tile: this warp's share of the stages, each half
+            // through its own staging tile in the now idle ring (every load
+            // has landed and, past the tile-end barrier, every MMA that read
+            // the ring has completed), so no store waits for another
+            unsigned char* fstage = stages + (warp - 2) * (kMaxGroups + 1) * kOutTile;
+            for (int grp = grpsel, k = 0; grp < ngroups; grp += 2) {
+                store_folded(grp, 0, fstage + (k++) * kOutTile);
+                if (kCols * grp + kHalf < slice) store_folded(grp, 1, fstage + (k++) * kOutTile);
+            }
         }
         if (lane == 0) bulk_wait_all();   // stores complete before the CTA exits
     } else {
@@ -654,9 +705,13 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
 // Planes packed ahead of the calls: CTA r writes rank r's region (the same
 // bytes the kernel's prologue writes into each cluster's region).
 __global__ void __launch_bounds__(kThreads, 1) pre_tc_pack_kernel(const float* fn, int C, unsigned char* out) {
-    const int slice = C / kCtas, ngroups = slice / kCols, r = blockIdx.x;
-    write_planes(fn, C, r * slice, ngroups, out + (size_t)r * ngroups * kWStage, threadIdx.x >> 5, threadIdx.x & 31);
+    const int slice = C / kCtas, ngroups = (slice + kCols - 1) / kCols, r = blockIdx.x;
+    write_planes(fn, C, r * slice, slice, ngroups, out + (size_t)r * ngroups * kWStage, threadIdx.x >> 5,
+                 threadIdx.x & 31);
 }
+
+// Stages (32 columns, the last possibly 16) of one CTA's slice.
+static int stages_of(int C) { return (C / kCtas + kCols - 1) / kCols; }
 
 }  // namespace tc
 
@@ -679,7 +734,7 @@ static PFN_encodeTiled encode_fn() {
     return fn;
 }
 
-size_t pre_tc_packed_bytes(int C) { return (size_t)tc::kCtas * (size_t)(C / (tc::kCols * tc::kCtas)) * tc::kWStage; }
+size_t pre_tc_packed_bytes(int C) { return (size_t)tc::kCtas * (size_t)tc::stages_of(C) * tc::kWStage; }
 
 cudaError_t launch_pre_tc_pack(const float* fn, int C, void* out, cudaStream_t stream) {
     tc::pre_tc_pack_kernel<<<tc::kCtas, tc::kThreads, 0, stream>>>(fn, C, static_cast<unsigned char*>(out));
@@ -689,11 +744,11 @@ cudaError_t launch_pre_tc_pack(const float* fn, int C, void* out, cudaStream_t s
 size_t pre_tc_workspace_bytes(int64_t T, int C, int max_clusters) {
     const int64_t tiles = (T + tc::kTile - 1) / tc::kTile;
     const int64_t ncl = tiles < max_clusters ? tiles : max_clusters;
-    return (size_t)ncl * tc::kCtas * (size_t)(C / (tc::kCols * tc::kCtas)) * tc::kWStage;
+    return (size_t)ncl * tc::kCtas * (size_t)tc::stages_of(C) * tc::kWStage;
 }
 
 bool pre_tc_supports(int C) {
-    return C % (tc::kCols * tc::kCtas) == 0 && C / tc::kCtas <= tc::kCols * tc::kMaxGroups;
+    return C % (tc::kHalf * tc::kCtas) == 0 && C / tc::kCtas <= tc::kCols * tc::kMaxGroups;
 }
 int pre_tc_tile_tokens() { return tc::kTile; }
 
@@ -733,10 +788,11 @@ cudaError_t launch_pre_tc(const uint16_t* x, const float* pre_in, const float* f
     if (!enc) return cudaErrorNotSupported;
     // x viewed as (column, token, stream) -- the token stride 4C and the
     // stream stride C elements (broadcast: one stream) -- so that one box of
-    // 16 columns (32 B) x 128 tokens x all streams lands in shared memory as
-    // one 4 KB tile per stream, 32-byte swizzled as the MMA reads it: a
+    // 32 columns (64 B) x 128 tokens x all streams lands in shared memory as
+    // one 8 KB tile per stream, 64-byte swizzled as the MMA reads it: a
     // single TMA instruction per stage (the producer's issue time per stage
-    // is on the kernel's critical path).
+    // is on the kernel's critical path).  Columns past C (a half last stage
+    // of the last slice) read as zeros and are not used.
     alignas(64) CUtensorMap map;
     const cuuint64_t ns = broadcast ? 1 : 4;
     const cuuint64_t dims[3] = {(cuuint64_t)C, (cuuint64_t)T, ns};
@@ -744,14 +800,14 @@ cudaError_t launch_pre_tc(const uint16_t* x, const float* pre_in, const float* f
     const cuuint32_t box[3] = {(cuuint32_t)tc::kCols, (cuuint32_t)tc::kTile, (cuuint32_t)ns};
     const cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(x), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     // layer_input [T][C] bf16; box = 16 columns x 32 tokens (one warp's rows)
     alignas(64) CUtensorMap omap;
     const cuuint64_t odims[2] = {(cuuint64_t)C, (cuuint64_t)T};
     const cuuint64_t ostrides[1] = {(cuuint64_t)C * 2};
-    const cuuint32_t obox[2] = {(cuuint32_t)tc::kCols, 32};
+    const cuuint32_t obox[2] = {(cuuint32_t)tc::kHalf, 32};
     const cuuint32_t oestr[2] = {1, 1};
     r = enc(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, layer_input, odims, ostrides, obox, oestr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE,

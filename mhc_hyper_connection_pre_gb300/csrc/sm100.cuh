@@ -253,7 +253,11 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 //   32-byte swizzle: rows of 32 bytes (16 bf16 of K), 8-row atoms of 256 B,
 //     the two 16-byte chunks of rows 4..7 of an atom exchanged; sbo = atom
 //     stride in M/N; lbo unused for one K16 step per atom (encoded as 16 B).
-constexpr uint64_t kLayoutNoSwizzle = 0, kLayoutSwizzle32B = 6;
+//   64-byte swizzle: rows of 64 bytes (32 bf16 of K), 8-row atoms of 512 B,
+//     chunk c of row r stored at chunk c ^ ((r >> 1) & 3); the second K16
+//     step of a row starts 32 B further (the swizzle follows the address
+//     bits, so the same atoms serve both steps).
+constexpr uint64_t kLayoutNoSwizzle = 0, kLayoutSwizzle64B = 4, kLayoutSwizzle32B = 6;
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
                                               uint64_t layout = kLayoutNoSwizzle) {
     return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
@@ -262,6 +266,11 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 // Byte offset of 16-byte chunk `c` (0/1) of row `r` inside an 8-row atom of
 // the 32-byte-swizzled layout (the pattern TMA writes for SWIZZLE_32B).
 __host__ __device__ constexpr int sw32_off(int r, int c) { return r * 32 + ((c ^ ((r >> 2) & 1)) << 4); }
+// Byte offset of 16-byte chunk `c` (0..3) of row `r` inside an 8-row, 512-byte
+// atom of the 64-byte-swizzled layout (SWIZZLE_64B: address bits 7-8 XORed
+// into bits 4-5, i.e. the chunk index XOR (r / 2) mod 4).  For one K16 step
+// per atom row half, the MMA descriptor's start address advances by 32 B.
+__host__ __device__ constexpr int sw64_off(int r, int c) { return r * 64 + ((c ^ ((r >> 1) & 3)) << 4); }
 // Instruction descriptor of kind::f16: bf16 A and B, fp32 accumulator,
 // both K-major, shape M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
