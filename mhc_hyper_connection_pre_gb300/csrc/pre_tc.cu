@@ -319,6 +319,11 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(kTile, kN);
             const uint32_t sbase = smem_u32(stages);
+            // descriptors of the ring's base: an operand's descriptor is this
+            // plus its byte offset / 16 (the 14-bit address field cannot carry:
+            // shared memory ends below 256 KB)
+            const uint64_t adesc0 = smem_desc(sbase, 16, 512, kLayoutSwizzle64B);
+            const uint64_t bdesc0 = smem_desc(sbase + kXBytes, 16, 512, kLayoutSwizzle64B);
             uint32_t g = 0;
             int it = 0;
             for (int tile = cid; tile < a.ntiles; tile += ncl, ++it) {
@@ -333,15 +338,16 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
                     const int nk = kCols * grp + kHalf < slice ? 2 : 1;
                     mbar_wait(&full[s], (g / kStages) & 1, abort);
                     tc_fence_after();
-                    const uint32_t slot = sbase + s * kSlotBytes;
+                    const uint32_t so = (uint32_t)(s * kSlotBytes) >> 4;
 #pragma unroll
                     for (int st = 0; st < 4; ++st)
-                        for (int k = 0; k < nk; ++k) {
-                            const uint64_t ad = smem_desc(slot + st * xbox + 32 * k, 16, 512, kLayoutSwizzle64B);
-                            const uint64_t bd =
-                                smem_desc(slot + kXBytes + st * kWBlock + 32 * k, 16, 512, kLayoutSwizzle64B);
-                            mma_bf16(dt, ad, bd, idesc, (grp | st | k) != 0);
-                        }
+#pragma unroll
+                        for (int k = 0; k < 2; ++k)
+                            if (k < nk) {
+                                const uint64_t ad = adesc0 + so + (uint32_t)((st * xbox + 32 * k) >> 4);
+                                const uint64_t bd = bdesc0 + so + (uint32_t)((st * kWBlock + 32 * k) >> 4);
+                                mma_bf16(dt, ad, bd, idesc, (grp | st | k) != 0);
+                            }
                     mma_commit(&empty[s]);
                 }
                 mma_commit(&dfull[d]);
@@ -465,17 +471,35 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
             }
             tmem_st16(tl + kHCol + kCols * grp + kHalf * hf, hb);
         };
-        uint32_t g = 0;
+        // The previous tile's fold scale is taken as late as possible: at the
+        // first fold of the next tile (or, where none comes, before this
+        // tile's sums go out -- the inbox protocol needs every scale phase
+        // received before the next sums are pushed), so the exchange's
+        // latency and the slowest CTA's lag overlap this tile's work.
+        // scale_full's phase for tile `it` is armed once tile it-1's phase
+        // has completed (by the arming thread, after its own wait).
+        bool need_scale = false;
         int it = 0;
+        auto take_scale = [&](bool arm) {
+            mbar_wait<true>(scale_full, (uint32_t)(it - 1) & 1u, abort);
+            sc_prev = scale[trow];
+            need_scale = false;
+            if (armer && arm) mbar_arrive_expect_tx(scale_full, kCtas * kFinTok * 4);
+        };
+        if (armer && cid < a.ntiles) mbar_arrive_expect_tx(scale_full, kCtas * kFinTok * 4);
+        // the pre-mix of the next tile's token is loaded a tile ahead
+        auto load_pre = [&](int tl) {
+            const int64_t tt = (int64_t)tl * kTile + trow;
+            float4 pv = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (tl < a.ntiles && tt < a.T) pv = __ldg(reinterpret_cast<const float4*>(a.pre_in) + tt);
+            return pv;
+        };
+        float4 pnext = load_pre(cid);
+        uint32_t g = 0;
         for (int tile = cid; tile < a.ntiles; tile += ncl, ++it) {
             const int64_t t = (int64_t)tile * kTile + trow;
-            const bool valid = t < a.T;
-            if (armer) mbar_arrive_expect_tx(scale_full, kCtas * kFinTok * 4);
-            float p[4] = {0.f, 0.f, 0.f, 0.f};
-            if (valid) {
-                const float4 pv = __ldg(reinterpret_cast<const float4*>(a.pre_in) + t);
-                p[0] = pv.x; p[1] = pv.y; p[2] = pv.z; p[3] = pv.w;
-            }
+            const float p[4] = {pnext.x, pnext.y, pnext.z, pnext.w};
+            pnext = load_pre(tile + ncl);
             f32x2 sx2 = make_f32x2(0.f, 0.f), sh2 = make_f32x2(0.f, 0.f);
             for (int grp = 0; grp < ngroups; ++grp, ++g) {
                 if ((int)(g & 1) != grpsel) continue;  // stages alternate between the two groups
@@ -517,10 +541,24 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
                             }
                     continue;
                 }
+                f32x2 h0[8], h1[8];
+                if (fold && need_scale) {
+                    // this group's first stage of the tile: both halves are
+                    // collapsed before the previous tile's scale is taken
+                    collapse16(x0, p, h0, sx2, sh2);
+                    if (two) collapse16(x1, p, h1, sx2, sh2);
+                    take_scale(true);
+                    store_folded(grp, 0);
+                    park(grp, 0, h0);
+                    if (two) {
+                        store_folded(grp, 1);
+                        park(grp, 1, h1);
+                    }
+                    continue;
+                }
                 // first half: fold tile i-1's columns, collapse, park; the
                 // second half is collapsed before its fold so that the first
                 // half's store has two collapses' time to read its staging
-                f32x2 h0[8], h1[8];
                 if (fold && have_prev) store_folded(grp, 0);
                 collapse16(x0, p, h0, sx2, sh2);
                 if (fold) park(grp, 0, h0);
@@ -543,6 +581,9 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
                 split_f32x2(sh2, a0, a1);
                 sh = a0 + a1;
             }
+            // no fold took the previous tile's scale in this tile: take it
+            // before this tile's sums go out
+            if (need_scale) take_scale(true);
             // this group's sums go out first: the finalizer needs only Σh² for
             // the fold scale, which gates every CTA's next tile
             st_async_v2(sq_dst, sx, sh, sq_bar);
@@ -577,17 +618,17 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
                     st_async_v4(dots_dst + 4 * k, dots[k], dots[k + 1], dots[k + 2], dots[k + 3], dots_bar);
             }
 
-            // this tile's fold scale from the finalizers
-            mbar_wait<true>(scale_full, it & 1, abort);
-            sc_prev = scale[trow];
+            // this tile's fold scale is taken during the next tile
             t_prev = t;
             have_prev = true;
+            need_scale = true;
             // both groups' parked h is complete before the other group reads it
             // in the next tile (stage parity can change between tiles)
             tc_fence_before();
             named_bar_sync(1, 32 * kRowWarps);
             tc_fence_after();
         }
+        if (need_scale) take_scale(false);
         if (fold && !GATES && have_prev) {
             // flush the last tile: this warp's share of the stages, each half
             // through its own staging tile in the now idle ring (every load
@@ -606,6 +647,11 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
         const uint32_t scale_dst = mapa(smem_u32(scale + (int)rank * kFinTok), peer);
         const uint32_t scale_bar = mapa(smem_u32(scale_full), peer);
         const uint32_t free_bar = mapa(smem_u32(dots_free), peer);
+        float bias_r[kLogits], al_r[3];
+#pragma unroll
+        for (int m = 0; m < kLogits; ++m) bias_r[m] = __ldg(a.bias + m);
+#pragma unroll
+        for (int i = 0; i < 3; ++i) al_r[i] = __ldg(a.alpha + i);
         int it = 0;
         for (int tile = cid; tile < a.ntiles; tile += ncl, ++it) {
             // (1) Σx², Σh² of the 8 tokens: lane (tok, value) sums 16 sources x
@@ -658,12 +704,11 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
             const int64_t t = (int64_t)tile * kTile + (int)rank * kFinTok + lane;
             if (lane < kFinTok && t < a.T) {
                 const float r = 1.0f / sqrtf(sx / (float)K + a.rms_eps);
-                const float al0 = __ldg(a.alpha), al1 = __ldg(a.alpha + 1), al2 = __ldg(a.alpha + 2);
                 float l[kLogits];
 #pragma unroll
                 for (int m = 0; m < kLogits; ++m) {
-                    const float al = m < 4 ? al0 : (m < 8 ? al1 : al2);
-                    l[m] = (r * dsum[m]) * al + __ldg(a.bias + m);
+                    const float al = m < 4 ? al_r[0] : (m < 8 ? al_r[1] : al_r[2]);
+                    l[m] = (r * dsum[m]) * al + bias_r[m];
                 }
                 if (a.logits_out) {
                     float4* lo = reinterpret_cast<float4*>(a.logits_out + t * kLogits);
