@@ -73,9 +73,11 @@ constexpr int kSlotBytes = kXBytes + kWStage;     // 50 KB ring slot: x boxes, t
 constexpr int kN = 80;                            // MMA N: 72 plane rows + 8 ignored
 constexpr int kDots = 24;                         // projection dot products per token
 constexpr int kFinTok = kTile / kCtas;            // tokens finalized per CTA per tile
-constexpr int kRowWarps = 8;
-constexpr int kThreads = 32 * (2 + kRowWarps + 1);
-constexpr int kFinWarp = 2 + kRowWarps;
+constexpr int kRowWarps = 8;                      // collapse warps: two groups of four
+constexpr int kFoldWarps = 4;                     // fold warps: one per TMEM lane quadrant
+constexpr int kFoldWarp0 = 2 + kRowWarps;
+constexpr int kFinWarp = kFoldWarp0 + kFoldWarps;
+constexpr int kThreads = 32 * (kFinWarp + 1);
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDCol0 = 0, kDCol1 = 96, kHCol = 192;  // accumulators, parked h (320 columns)
 
@@ -86,14 +88,15 @@ constexpr int kOffDots = kOffStages + kStages * kSlotBytes;           // [16 src
 constexpr int kOffSq = kOffDots + kCtas * kFinTok * kDots * 4;        // [16 src][8 tok][2 grp][2] sums
 constexpr int kOffScale = kOffSq + kCtas * kFinTok * 2 * 2 * 4;       // [128] fold scales
 constexpr int kOffNormW = kOffScale + kTile * 4;                      // [C/16] bf16
-// [8 row warps][32 tok][16 col] bf16 staging tiles (half a stage each),
-// 32-byte swizzled: the swizzle pattern follows address bit 7, so each tile
-// starts 1 KB aligned
+// [4 fold warps][2 halves][32 tok][16 col] bf16 staging tiles, 32-byte
+// swizzled: the swizzle pattern follows address bit 7, so each tile starts
+// 1 KB aligned
 constexpr int kOutTile = 32 * kHalf * 2;                              // 1 KB
 constexpr int kOffOut = (kOffNormW + kMaxGroups * kCols * 2 + 1023) / 1024 * 1024;
-constexpr int kOffBars = kOffOut + kRowWarps * kOutTile;
-// full[8], empty[8], dfull[2], dempty[2], sq_full, dots_full, scale_full, dots_free, drain
-constexpr int kNumBars = 2 * kStages + 2 + 2 + 5;
+constexpr int kOffBars = kOffOut + kFoldWarps * 2 * kOutTile;
+// full[4], empty[4], dfull[2], dempty[2], sq_full, dots_full, scale_full,
+// dots_free, drain, hfull[10], hfree[10]
+constexpr int kNumBars = 2 * kStages + 2 + 2 + 5 + 2 * kMaxGroups;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;                     // tmem base, abort flag
 constexpr int kSmemBytes = kOffMisc + 16;
 static_assert(kOffBars % 8 == 0, "mbarriers need 8-byte alignment");
@@ -167,7 +170,7 @@ __device__ __forceinline__ void split3(const float (&w)[8], uint32_t (&pk)[3][4]
 __device__ __forceinline__ void write_planes(const float* __restrict__ fn, int C, int c0, int slice,
                                              int ngroups, unsigned char* wreg, int warp, int lane) {
     const int64_t K = 4 * (int64_t)C;
-    constexpr int kUnitsMax = 11;   // ceil(10 stages x 4 streams x 3 row octets / 11 warps)
+    constexpr int kUnitsMax = (kMaxGroups * 4 * 3 + kThreads / 32 - 1) / (kThreads / 32);
     const int nunits = ngroups * 4 * 3;
     const int mrow = lane >> 2, c = lane & 3;
     float w[kUnitsMax][8];
@@ -219,6 +222,8 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
     uint64_t* scale_full = dots_full + 1; // this CTA's 128 fold scales arrived
     uint64_t* dots_free = scale_full + 1; // every finalizer has read this CTA's previous dots
     uint64_t* drain = dots_free + 1;
+    uint64_t* hfull = drain + 1;          // [stage]: its h of the tile is parked (collapse warps)
+    uint64_t* hfree = hfull + kMaxGroups; // [stage]: its parked h has been read (fold warps)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
 
@@ -247,7 +252,11 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
         }
         for (int d = 0; d < 2; ++d) {
             mbar_init(&dfull[d], 1);
-            mbar_init(&dempty[d], 4);    // group 0's 4 warps
+            mbar_init(&dempty[d], kFoldWarps);
+        }
+        for (int q = 0; q < kMaxGroups; ++q) {
+            mbar_init(&hfull[q], 4);             // the 4 collapse warps of the stage's group
+            mbar_init(&hfree[q], kFoldWarps);
         }
         // the three cluster exchanges complete by bytes (st.async); each has
         // one local arrival per phase that arms the expected byte count
@@ -357,75 +366,24 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
             mbar_wait_drain(drain, 0);
         }
         __syncwarp();
-    } else if (warp < kFinWarp) {
-        // ================================================== token rows
+    } else if (warp < kFoldWarp0) {
+        // ================================================== collapse warps
+        // Two groups of four taking alternate stages (thread = token, TMEM
+        // lane quadrant = warp % 4): load the stage's x, collapse h (fp32,
+        // fixed order), sum x^2 and h^2, park h in the stage's TMEM columns
+        // once the fold warps have read the previous tile's h there.
         const int grpsel = (warp - 2) >> 2;   // 0 or 1: which stages this warp takes
         const int quad = warp & 3;
         const int trow = quad * 32 + lane;
         const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
-        const int fin = trow / kFinTok, slot = trow % kFinTok;
-        const uint32_t sq_dst = mapa(smem_u32(sq_in + (((int)rank * kFinTok + slot) * 2 + grpsel) * 2), fin);
+        const int fin = trow / kFinTok, fslot = trow % kFinTok;
+        const uint32_t sq_dst = mapa(smem_u32(sq_in + (((int)rank * kFinTok + fslot) * 2 + grpsel) * 2), fin);
         const uint32_t sq_bar = mapa(smem_u32(sq_full), fin);
-        const uint32_t dots_dst = mapa(smem_u32(dots_in + ((int)rank * kFinTok + slot) * kDots), fin);
-        const uint32_t dots_bar = mapa(smem_u32(dots_full), fin);
-        const bool armer = (warp == 2 && lane == 0);   // arms this CTA's scale_full each tile
         // byte offsets of this token's four 16-byte chunks (8 columns each)
         // in an 8 KB stream box: 64-byte rows, 64-byte swizzle
         int xo[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) xo[c] = (trow >> 3) * 512 + sw64_off(trow & 7, c);
-        // layer_input leaves through a per-warp 32-token x 16-column staging
-        // tile (32-byte swizzle) and one TMA tensor store per warp and half
-        // stage: full 32-byte sectors instead of 32 scattered 16-byte stores
-        // per instruction; rows past T are clipped by the store.
-        unsigned char* ostage = smem + kOffOut + (warp - 2) * kOutTile;
-        const int oo0 = (lane >> 3) * 256 + sw32_off(lane & 7, 0);
-        const int oo1 = (lane >> 3) * 256 + sw32_off(lane & 7, 1);
-        // stg: the warp's own staging tile (reused: wait for the previous
-        // store to have read it), or a fresh one (no wait)
-        auto store_out = [&](const f32x2 (&o)[8], int col, int64_t row0, unsigned char* stg = nullptr) {
-            if (!stg) {
-                if (lane == 0) bulk_wait_read_all();   // the previous store has read the tile
-                __syncwarp();
-                stg = ostage;
-            }
-            *reinterpret_cast<uint4*>(stg + oo0) = make_uint4(f32x2_to_bf16x2(o[0]), f32x2_to_bf16x2(o[1]),
-                                                              f32x2_to_bf16x2(o[2]), f32x2_to_bf16x2(o[3]));
-            *reinterpret_cast<uint4*>(stg + oo1) = make_uint4(f32x2_to_bf16x2(o[4]), f32x2_to_bf16x2(o[5]),
-                                                              f32x2_to_bf16x2(o[6]), f32x2_to_bf16x2(o[7]));
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0 && row0 < a.T) {
-                tma_store_2d(&omap, stg, col, (int)row0);
-                bulk_commit_group();
-            }
-        };
-        // The folded store of tile i is deferred into tile i+1's stages: at a
-        // stage half the thread first reads back tile i's parked h of those
-        // 16 columns, scales, rounds and stores it, then parks tile i+1's h.
-        bool have_prev = false;
-        int64_t t_prev = 0;
-        float sc_prev = 1.f;
-        auto store_folded = [&](int grp, int hf, unsigned char* stg = nullptr) {
-            uint32_t r[16];
-            tmem_ld16(tl + kHCol + kCols * grp + kHalf * hf, r);
-            tmem_wait_ld();
-            tmem_regs_ready(r);
-            const uint4* wv = reinterpret_cast<const uint4*>(nw_s + kCols * grp + kHalf * hf);
-            const f32x2 sc2 = make_f32x2(sc_prev, sc_prev);
-            f32x2 o[8];
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const uint4 w4 = wv[c];
-                const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const f32x2 hv = make_f32x2(__uint_as_float(r[8 * c + 2 * e]), __uint_as_float(r[8 * c + 2 * e + 1]));
-                    o[4 * c + e] = mul_rn2(mul_rn2(hv, sc2), bf16x2_to_f32x2(ww[e]));   // (h * s) * w
-                }
-            }
-            store_out(o, c0 + kCols * grp + kHalf * hf, t_prev - lane, stg);
-        };
         // pair e (columns 2e, 2e+1) of a half's 16 columns: word e & 3 of chunk e >> 2
         auto pair_of = [](const uint4 (&ch)[2], int e) -> uint32_t {
             const uint4 v = ch[e >> 2];
@@ -471,33 +429,17 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
             }
             tmem_st16(tl + kHCol + kCols * grp + kHalf * hf, hb);
         };
-        // The previous tile's fold scale is taken as late as possible: at the
-        // first fold of the next tile (or, where none comes, before this
-        // tile's sums go out -- the inbox protocol needs every scale phase
-        // received before the next sums are pushed), so the exchange's
-        // latency and the slowest CTA's lag overlap this tile's work.
-        // scale_full's phase for tile `it` is armed once tile it-1's phase
-        // has completed (by the arming thread, after its own wait).
-        bool need_scale = false;
-        int it = 0;
-        auto take_scale = [&](bool arm) {
-            mbar_wait<true>(scale_full, (uint32_t)(it - 1) & 1u, abort);
-            sc_prev = scale[trow];
-            need_scale = false;
-            if (armer && arm) mbar_arrive_expect_tx(scale_full, kCtas * kFinTok * 4);
-        };
-        if (armer && cid < a.ntiles) mbar_arrive_expect_tx(scale_full, kCtas * kFinTok * 4);
         // the pre-mix of the next tile's token is loaded a tile ahead
-        auto load_pre = [&](int tl) {
-            const int64_t tt = (int64_t)tl * kTile + trow;
+        auto load_pre = [&](int tl_) {
+            const int64_t tt = (int64_t)tl_ * kTile + trow;
             float4 pv = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (tl < a.ntiles && tt < a.T) pv = __ldg(reinterpret_cast<const float4*>(a.pre_in) + tt);
+            if (tl_ < a.ntiles && tt < a.T) pv = __ldg(reinterpret_cast<const float4*>(a.pre_in) + tt);
             return pv;
         };
         float4 pnext = load_pre(cid);
         uint32_t g = 0;
+        int it = 0;
         for (int tile = cid; tile < a.ntiles; tile += ncl, ++it) {
-            const int64_t t = (int64_t)tile * kTile + trow;
             const float p[4] = {pnext.x, pnext.y, pnext.z, pnext.w};
             pnext = load_pre(tile + ncl);
             f32x2 sx2 = make_f32x2(0.f, 0.f), sh2 = make_f32x2(0.f, 0.f);
@@ -542,36 +484,19 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
                     continue;
                 }
                 f32x2 h0[8], h1[8];
-                if (fold && need_scale) {
-                    // this group's first stage of the tile: both halves are
-                    // collapsed before the previous tile's scale is taken
-                    collapse16(x0, p, h0, sx2, sh2);
-                    if (two) collapse16(x1, p, h1, sx2, sh2);
-                    take_scale(true);
-                    store_folded(grp, 0);
-                    park(grp, 0, h0);
-                    if (two) {
-                        store_folded(grp, 1);
-                        park(grp, 1, h1);
-                    }
-                    continue;
-                }
-                // first half: fold tile i-1's columns, collapse, park; the
-                // second half is collapsed before its fold so that the first
-                // half's store has two collapses' time to read its staging
-                if (fold && have_prev) store_folded(grp, 0);
                 collapse16(x0, p, h0, sx2, sh2);
-                if (fold) park(grp, 0, h0);
-                else store_out(h0, c0 + kCols * grp, t - lane);
-                if (two) {
-                    collapse16(x1, p, h1, sx2, sh2);
-                    if (fold) {
-                        if (have_prev) store_folded(grp, 1);
-                        park(grp, 1, h1);
-                    } else {
-                        store_out(h1, c0 + kCols * grp + kHalf, t - lane);
-                    }
+                if (two) collapse16(x1, p, h1, sx2, sh2);
+                // the fold warps have read the previous tile's h of this stage
+                if (it > 0) {
+                    mbar_wait(&hfree[grp], (uint32_t)(it - 1) & 1u, abort);
+                    tc_fence_after();
                 }
+                park(grp, 0, h0);
+                if (two) park(grp, 1, h1);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&hfull[grp]);
             }
             float sx, sh;
             {
@@ -581,63 +506,132 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
                 split_f32x2(sh2, a0, a1);
                 sh = a0 + a1;
             }
-            // no fold took the previous tile's scale in this tile: take it
-            // before this tile's sums go out
-            if (need_scale) take_scale(true);
-            // this group's sums go out first: the finalizer needs only Σh² for
-            // the fold scale, which gates every CTA's next tile
+            // the finalizer has read this CTA's previous sums once their
+            // scales are back (the sums inbox is single-buffered)
+            if (it > 0) mbar_wait<true>(scale_full, (uint32_t)(it - 1) & 1u, abort);
             st_async_v2(sq_dst, sx, sh, sq_bar);
-            if (fold && !GATES) tmem_wait_st();
-
-            if (grpsel == 0) {
-                // accumulated projection of this CTA's K-slice for the token
+        }
+    } else if (warp < kFinWarp) {
+        // ================================================== fold warps
+        // One warp per TMEM lane quadrant (thread = token).  Per tile: the
+        // accumulated projection of this CTA's K-slice to the token's
+        // finalizer, then the tile's fold scale, then every stage's parked h
+        // as soon as it is parked: read, scaled, weighted, rounded once and
+        // stored through a staging tile by TMA; the stage's TMEM columns are
+        // released to the collapse warps right after the read.
+        const int quad = warp & 3;
+        const int trow = quad * 32 + lane;
+        const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
+        const int fin = trow / kFinTok, fslot = trow % kFinTok;
+        const uint32_t dots_dst = mapa(smem_u32(dots_in + ((int)rank * kFinTok + fslot) * kDots), fin);
+        const uint32_t dots_bar = mapa(smem_u32(dots_full), fin);
+        const bool armer = (warp == kFoldWarp0 && lane == 0);   // arms this CTA's scale_full
+        // layer_input leaves through a per-warp pair of 32-token x 16-column
+        // staging tiles (32-byte swizzle), one TMA tensor store each: full
+        // 32-byte sectors instead of 32 scattered 16-byte stores per
+        // instruction; rows past T are clipped by the store.
+        unsigned char* ostage = smem + kOffOut + (warp - kFoldWarp0) * 2 * kOutTile;
+        const int oo0 = (lane >> 3) * 256 + sw32_off(lane & 7, 0);
+        const int oo1 = (lane >> 3) * 256 + sw32_off(lane & 7, 1);
+        auto stage_out = [&](const uint32_t (&r)[16], unsigned char* stg, int col, float sc) {
+            uint32_t o[8];
+            if (fold) {
+                const uint4* wv = reinterpret_cast<const uint4*>(nw_s + (col - c0));
+                const f32x2 sc2 = make_f32x2(sc, sc);
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const uint4 w4 = wv[c];
+                    const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const f32x2 hv = make_f32x2(__uint_as_float(r[8 * c + 2 * e]),
+                                                    __uint_as_float(r[8 * c + 2 * e + 1]));
+                        o[4 * c + e] = f32x2_to_bf16x2(mul_rn2(mul_rn2(hv, sc2), bf16x2_to_f32x2(ww[e])));  // (h * s) * w
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = pack_bf16x2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
+            }
+            *reinterpret_cast<uint4*>(stg + oo0) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(stg + oo1) = make_uint4(o[4], o[5], o[6], o[7]);
+        };
+        if (armer && my_tiles > 0) mbar_arrive_expect_tx(scale_full, kCtas * kFinTok * 4);
+        int it = 0;
+        for (int tile = cid; tile < a.ntiles; tile += ncl, ++it) {
+            const int64_t t = (int64_t)tile * kTile + trow;
+            {
+                // accumulated projection of this CTA's K-slice for the token:
+                // planes mid + lo first, then hi (24 columns each)
                 const int d = it & 1;
+                const uint32_t acc_col = d ? kDCol1 : kDCol0;
                 mbar_wait(&dfull[d], (it >> 1) & 1, abort);
                 tc_fence_after();
-                uint32_t raw[9][8];
+                uint32_t rm[3][8], rl[3][8];
 #pragma unroll
-                for (int c = 0; c < 9; ++c) tmem_ld8(tl + (d ? kDCol1 : kDCol0) + 8 * c, raw[c]);
+                for (int c = 0; c < 3; ++c) {
+                    tmem_ld8(tl + acc_col + 24 + 8 * c, rm[c]);
+                    tmem_ld8(tl + acc_col + 48 + 8 * c, rl[c]);
+                }
                 tmem_wait_ld();
-                float acc[72];
+                float dots[kDots];
 #pragma unroll
-                for (int c = 0; c < 9; ++c) {
-                    tmem_regs_ready(raw[c]);
+                for (int c = 0; c < 3; ++c) {
+                    tmem_regs_ready(rm[c]);
+                    tmem_regs_ready(rl[c]);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[8 * c + e] = __uint_as_float(raw[c][e]);
+                    for (int e = 0; e < 8; ++e) dots[8 * c + e] = __uint_as_float(rm[c][e]) + __uint_as_float(rl[c][e]);
+                }
+                uint32_t rh[3][8];
+#pragma unroll
+                for (int c = 0; c < 3; ++c) tmem_ld8(tl + acc_col + 8 * c, rh[c]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 3; ++c) {
+                    tmem_regs_ready(rh[c]);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) dots[8 * c + e] = __uint_as_float(rh[c][e]) + dots[8 * c + e];
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&dempty[d]);
-                float dots[kDots];
-#pragma unroll
-                for (int m = 0; m < kDots; ++m) dots[m] = acc[m] + (acc[24 + m] + acc[48 + m]);
                 // the finalizers have read this CTA's previous dots
                 mbar_wait<true>(dots_free, (it & 1) ^ 1, abort);
 #pragma unroll
                 for (int k = 0; k < kDots; k += 4)
                     st_async_v4(dots_dst + 4 * k, dots[k], dots[k + 1], dots[k + 2], dots[k + 3], dots_bar);
             }
-
-            // this tile's fold scale is taken during the next tile
-            t_prev = t;
-            have_prev = true;
-            need_scale = true;
-            // both groups' parked h is complete before the other group reads it
-            // in the next tile (stage parity can change between tiles)
-            tc_fence_before();
-            named_bar_sync(1, 32 * kRowWarps);
-            tc_fence_after();
-        }
-        if (need_scale) take_scale(false);
-        if (fold && !GATES && have_prev) {
-            // flush the last tile: this warp's share of the stages, each half
-            // through its own staging tile in the now idle ring (every load
-            // has landed and, past the tile-end barrier, every MMA that read
-            // the ring has completed), so no store waits for another
-            unsigned char* fstage = stages + (warp - 2) * (kMaxGroups + 1) * kOutTile;
-            for (int grp = grpsel, k = 0; grp < ngroups; grp += 2) {
-                store_folded(grp, 0, fstage + (k++) * kOutTile);
-                if (kCols * grp + kHalf < slice) store_folded(grp, 1, fstage + (k++) * kOutTile);
+            // this tile's fold scale (every phase is taken, with or without a
+            // fold: the collapse warps' sums protocol relies on the arming
+            // of the next phase that follows)
+            mbar_wait<true>(scale_full, (uint32_t)it & 1u, abort);
+            const float sc = scale[trow];
+            if (armer && it + 1 < my_tiles) mbar_arrive_expect_tx(scale_full, kCtas * kFinTok * 4);
+            if (GATES) continue;
+            for (int grp = 0; grp < ngroups; ++grp) {
+                const bool two = kCols * grp + kHalf < slice;
+                mbar_wait(&hfull[grp], (uint32_t)it & 1u, abort);
+                tc_fence_after();
+                uint32_t r0[16], r1[16];
+                tmem_ld16(tl + kHCol + kCols * grp, r0);
+                if (two) tmem_ld16(tl + kHCol + kCols * grp + kHalf, r1);
+                tmem_wait_ld();
+                tmem_regs_ready(r0);
+                if (two) tmem_regs_ready(r1);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&hfree[grp]);   // the collapse warps may park the next tile's h
+                if (lane == 0) bulk_wait_read_all();        // the previous stores have read the staging tiles
+                __syncwarp();
+                stage_out(r0, ostage, c0 + kCols * grp, sc);
+                if (two) stage_out(r1, ostage + kOutTile, c0 + kCols * grp + kHalf, sc);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && t - lane < a.T) {
+                    tma_store_2d(&omap, ostage, c0 + kCols * grp, (int)(t - lane));
+                    if (two) tma_store_2d(&omap, ostage + kOutTile, c0 + kCols * grp + kHalf, (int)(t - lane));
+                    bulk_commit_group();
+                }
             }
         }
         if (lane == 0) bulk_wait_all();   // stores complete before the CTA exits
@@ -738,7 +732,7 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
             mbar_wait_drain<true>(sq_full, lp);
             mbar_wait_drain<true>(dots_full, lp);
         }
-        if (warp == 2 && lane == 0) mbar_wait_drain<true>(scale_full, lp);
+        if (warp == kFoldWarp0 && lane == 0) mbar_wait_drain<true>(scale_full, lp);
     }
     if (warp == 1) {
         tc_fence_after();
