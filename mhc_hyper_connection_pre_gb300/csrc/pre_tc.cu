@@ -77,7 +77,8 @@ constexpr int kRowWarps = 8;                      // collapse warps: two groups 
 constexpr int kFoldWarps = 4;                     // fold warps: one per TMEM lane quadrant
 constexpr int kFoldWarp0 = 2 + kRowWarps;
 constexpr int kFinWarp = kFoldWarp0 + kFoldWarps;
-constexpr int kThreads = 32 * (kFinWarp + 1);
+constexpr int kScaleWarp = kFinWarp + 1;
+constexpr int kThreads = 32 * (kScaleWarp + 1);
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDCol0 = 0, kDCol1 = 96, kHCol = 192;  // accumulators, parked h (320 columns)
 
@@ -87,7 +88,8 @@ constexpr int kOffStages = 0;                                         // 1 KB al
 constexpr int kOffDots = kOffStages + kStages * kSlotBytes;           // [16 src][8 tok][24] dots
 constexpr int kOffSq = kOffDots + kCtas * kFinTok * kDots * 4;        // [16 src][8 tok][2 grp][2] sums
 constexpr int kOffScale = kOffSq + kCtas * kFinTok * 2 * 2 * 4;       // [128] fold scales
-constexpr int kOffNormW = kOffScale + kTile * 4;                      // [C/16] bf16
+constexpr int kOffSx = kOffScale + kTile * 4;                         // [2][8] Σx² handoff
+constexpr int kOffNormW = kOffSx + 2 * kFinTok * 4;                   // [C/16] bf16
 // [4 fold warps][2 halves][32 tok][16 col] bf16 staging tiles, 32-byte
 // swizzled: the swizzle pattern follows address bit 7, so each tile starts
 // 1 KB aligned
@@ -95,8 +97,8 @@ constexpr int kOutTile = 32 * kHalf * 2;                              // 1 KB
 constexpr int kOffOut = (kOffNormW + kMaxGroups * kCols * 2 + 1023) / 1024 * 1024;
 constexpr int kOffBars = kOffOut + kFoldWarps * 2 * kOutTile;
 // full[4], empty[4], dfull[2], dempty[2], sq_full, dots_full, scale_full,
-// dots_free, drain, hfull[10], hfree[10]
-constexpr int kNumBars = 2 * kStages + 2 + 2 + 5 + 2 * kMaxGroups;
+// dots_free, drain, hfull[10], hfree[10], sx_ready[2], sx_free[2]
+constexpr int kNumBars = 2 * kStages + 2 + 2 + 5 + 2 * kMaxGroups + 4;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;                     // tmem base, abort flag
 constexpr int kSmemBytes = kOffMisc + 16;
 static_assert(kOffBars % 8 == 0, "mbarriers need 8-byte alignment");
@@ -224,6 +226,9 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
     uint64_t* drain = dots_free + 1;
     uint64_t* hfull = drain + 1;          // [stage]: its h of the tile is parked (collapse warps)
     uint64_t* hfree = hfull + kMaxGroups; // [stage]: its parked h has been read (fold warps)
+    uint64_t* sx_ready = hfree + kMaxGroups;  // [tile & 1]: the scale warp's Σx² of the tile's 8 tokens
+    uint64_t* sx_free = sx_ready + 2;         // [tile & 1]: ... read by the finalizer
+    float* sx_buf = reinterpret_cast<float*>(smem + kOffSx);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
 
@@ -257,6 +262,10 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
         for (int q = 0; q < kMaxGroups; ++q) {
             mbar_init(&hfull[q], 4);             // the 4 collapse warps of the stage's group
             mbar_init(&hfree[q], kFoldWarps);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sx_ready[b], 1);
+            mbar_init(&sx_free[b], 1);
         }
         // the three cluster exchanges complete by bytes (st.async); each has
         // one local arrival per phase that arms the expected byte count
@@ -606,6 +615,11 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
             // of the next phase that follows)
             mbar_wait<true>(scale_full, (uint32_t)it & 1u, abort);
             const float sc = scale[trow];
+            // Every fold warp has taken this phase before the next one is
+            // armed: a parity wait must never fall two phases behind, and
+            // without a fold (the gates-only pass) nothing else keeps the
+            // four warps within one phase of each other.
+            named_bar_sync(1, 32 * kFoldWarps);
             if (armer && it + 1 < my_tiles) mbar_arrive_expect_tx(scale_full, kCtas * kFinTok * 4);
             if (GATES) continue;
             for (int grp = 0; grp < ngroups; ++grp) {
@@ -635,25 +649,18 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
             }
         }
         if (lane == 0) bulk_wait_all();   // stores complete before the CTA exits
-    } else {
-        // ================================================== finalizer
+    } else if (warp == kScaleWarp) {
+        // ================================================== scale warp
+        // For its 8 tokens of each tile: sums the 16 CTAs' Σx², Σh² partials
+        // in rank order and pushes the fold scales to all 16 CTAs at once
+        // (nothing else runs in this warp, so no scale waits behind the
+        // Sinkhorn chain); hands Σx² to the finalizer warp.
         const uint32_t peer = (uint32_t)(lane & (kCtas - 1));
         const uint32_t scale_dst = mapa(smem_u32(scale + (int)rank * kFinTok), peer);
         const uint32_t scale_bar = mapa(smem_u32(scale_full), peer);
-        const uint32_t free_bar = mapa(smem_u32(dots_free), peer);
-        float bias_r[kLogits], al_r[3];
-#pragma unroll
-        for (int m = 0; m < kLogits; ++m) bias_r[m] = __ldg(a.bias + m);
-#pragma unroll
-        for (int i = 0; i < 3; ++i) al_r[i] = __ldg(a.alpha + i);
         int it = 0;
         for (int tile = cid; tile < a.ntiles; tile += ncl, ++it) {
-            // (1) Σx², Σh² of the 8 tokens: lane (tok, value) sums 16 sources x
-            //     2 groups in fixed order; the scale goes out right away
-            if (lane == 0) {
-                mbar_arrive_expect_tx(sq_full, kCtas * kFinTok * 2 * 8);
-                mbar_arrive_expect_tx(dots_full, kCtas * kFinTok * kDots * 4);
-            }
+            if (lane == 0) mbar_arrive_expect_tx(sq_full, kCtas * kFinTok * 2 * 8);
             mbar_wait<true>(sq_full, it & 1, abort);
             float sum = 0.f;
             if (lane < 2 * kFinTok) {
@@ -674,7 +681,29 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
                 st_async_v4(scale_dst, sv[0], sv[1], sv[2], sv[3], scale_bar);
                 st_async_v4(scale_dst + 16, sv[4], sv[5], sv[6], sv[7], scale_bar);
             }
-            // (2) the dot products, off the tiles' critical path
+            // Σx² to the finalizer: buffer it & 1, once it has read the tile
+            // that used that buffer before
+            const int b = it & 1;
+            if (it >= 2) mbar_wait(&sx_free[b], (uint32_t)((it >> 1) - 1) & 1u, abort);
+            if (lane < kFinTok) sx_buf[b * kFinTok + lane] = sx;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sx_ready[b]);
+        }
+    } else {
+        // ================================================== finalizer
+        const uint32_t peer = (uint32_t)(lane & (kCtas - 1));
+        const uint32_t scale_dst = mapa(smem_u32(scale + (int)rank * kFinTok), peer);
+        const uint32_t scale_bar = mapa(smem_u32(scale_full), peer);
+        const uint32_t free_bar = mapa(smem_u32(dots_free), peer);
+        float bias_r[kLogits], al_r[3];
+#pragma unroll
+        for (int m = 0; m < kLogits; ++m) bias_r[m] = __ldg(a.bias + m);
+#pragma unroll
+        for (int i = 0; i < 3; ++i) al_r[i] = __ldg(a.alpha + i);
+        int it = 0;
+        if (lane == 0 && my_tiles > 0) mbar_arrive_expect_tx(dots_full, kCtas * kFinTok * kDots * 4);
+        for (int tile = cid; tile < a.ntiles; tile += ncl, ++it) {
+            // the dot products of the tile's 8 tokens, off the tiles' critical path
             mbar_wait<true>(dots_full, it & 1, abort);
             float dsum[kDots];
 #pragma unroll
@@ -695,6 +724,13 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
             }
             __syncwarp();
             if (lane < kCtas) mbar_arrive_remote(free_bar);   // inbox read: sources may push again
+            if (lane == 0 && it + 1 < my_tiles) mbar_arrive_expect_tx(dots_full, kCtas * kFinTok * kDots * 4);
+            // the tokens' Σx² from the scale warp
+            const int b = it & 1;
+            mbar_wait(&sx_ready[b], (uint32_t)(it >> 1) & 1u, abort);
+            const float sx = sx_buf[b * kFinTok + (lane & (kFinTok - 1))];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sx_free[b]);
             const int64_t t = (int64_t)tile * kTile + (int)rank * kFinTok + lane;
             if (lane < kFinTok && t < a.T) {
                 const float r = 1.0f / sqrtf(sx / (float)K + a.rms_eps);
