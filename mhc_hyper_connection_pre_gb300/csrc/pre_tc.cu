@@ -18,29 +18,35 @@
 //
 // Decomposition: a cluster of 16 CTAs owns a tile of 128 tokens (the MMA's
 // M); CTA r owns C/16 columns of all four streams and walks its slice in
-// stages of 16 columns x 4 streams x 128 tokens (16 KB: one 3-D TMA box of
-// 128 tokens x 32 bytes per stream, 32-byte swizzle, so every DRAM sector
-// fetched is used whole).  At the start of the call each CTA writes its
-// K-slice of the three fn planes (184 KB at C = 5120), already in the MMA's
-// operand layout, to its region of the caller's workspace; every stage then
-// brings the matching 9 KB block with one bulk copy (L2 evict-last) next to
-// the x boxes (L2 evict-first).  Keeping fn resident in shared memory instead
-// would leave room for only two x stages (32 KB in flight per SM); this
-// 8-slot ring keeps 128 KB of x in flight per SM.  Warp roles (11 warps):
-//   warp 0     TMA producer;
-//   warp 1     MMA issuer: 4 x tcgen05.mma (M128 N80 K16, one per stream) per
-//              stage into a double-buffered fp32 accumulator in TMEM;
-//   warps 2-9  token rows, two groups of four taking alternate stages (thread
-//              = token, TMEM lane quadrant = warp % 4): collapse h (fp32,
-//              fixed order), sum x^2, sum h^2; h parked in TMEM until the fold
-//              scale is known and stored, folded, during the next tile's
-//              stages.  At the tile end group 0 adds group 1's sums, reads the
-//              72 accumulator columns, adds the planes and pushes 26 partials
-//              to the token's finalizer CTA (st.async into its shared
-//              memory, bytes counted on its mbarrier);
-//   warp 10    finalizer: for its 8 tokens of the tile sums the 16 CTAs'
-//              partials in rank order, pushes the fold scale to all 16 CTAs,
-//              then logits, gates and the Sinkhorn comb in registers.
+// stages of 32 columns x 4 streams x 128 tokens (32 KB: one 3-D TMA box --
+// x described as (column, token, stream) -- of 64-byte rows, 64-byte
+// swizzle, one instruction per stage).  At the start of the call each CTA
+// writes its K-slice of the three fn planes (184 KB at C = 5120), already in
+// the MMA's operand layout, to its region of the caller's workspace; every
+// stage then brings the matching 18 KB block with one bulk copy (L2
+// evict-last) next to the x box (L2 evict-first).  A 4-slot ring of 50 KB
+// slots keeps 200 KB in flight per SM.  Warp roles (16 warps):
+//   warp 0       TMA producer;
+//   warp 1       MMA issuer: per stage 8 x tcgen05.mma (M128 N80 K16: two K
+//                steps per stream) into a double-buffered fp32 accumulator
+//                in TMEM;
+//   warps 2-9    collapse warps, two groups of four taking alternate stages
+//                (thread = token, TMEM lane quadrant = warp % 4): collapse h
+//                (fp32, fixed order), sum x^2, sum h^2, park h in the stage's
+//                TMEM columns once the fold warps have read the previous
+//                tile's h there; at the tile end push the sums to the
+//                token's scale warp (st.async into its shared memory, bytes
+//                counted on its mbarrier);
+//   warps 10-13  fold warps, one per lane quadrant: the tile's accumulated
+//                dot products to the token's finalizer, then the tile's fold
+//                scale, then every stage's parked h as soon as it is parked:
+//                folded, rounded once and stored through staging tiles by TMA;
+//   warp 14      finalizer: for its 8 tokens of each tile sums the 16 CTAs'
+//                dot products in rank order, then logits, gates and the
+//                Sinkhorn comb in registers;
+//   warp 15      scale warp: for the same 8 tokens sums the 16 CTAs' sums of
+//                squares in rank order and pushes the fold scales to all 16
+//                CTAs at once.
 // A gates-only instance (GATES) serves the first of the non-delayed block's
 // two passes: the token rows only sum x^2 (in the same order, so the gates
 // are the same bits), with no collapse, fold or layer_input.
