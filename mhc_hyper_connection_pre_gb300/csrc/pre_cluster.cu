@@ -102,7 +102,7 @@ struct Args {
 
 // Shared-memory carve-up (bytes), in this order.
 struct Layout {
-    int xs, hs, red, pin, nw, sq, dots, ys, gates, prex, shin, bars, abort_flag, total;
+    int xs, hs, red, pin, nw, sq, dots, ys, gates, prex, shin, ba, bars, abort_flag, total;
 };
 __host__ __device__ inline int dec_xstride(int lcmax) {
     // 64 bytes per group (4 streams x 8 bf16); rows an odd multiple of 64
@@ -126,6 +126,7 @@ __host__ __device__ inline Layout dec_layout(int lcmax, int mode) {
     // non-delayed: this tile's pre per token, sum h^2 partials [parity]
     L.prex = o;  o += mode == kNonDelayed ? 2 * kMaxTile * 16 : 0;
     L.shin = o;  o += mode == kNonDelayed ? 2 * kMaxTile * kCtas * 4 : 0;
+    L.ba = o;    o += 2 * kLogits * 4;   // per logit: bias, alpha of its group
     L.bars = o;  o += kNumBars * 8;
     L.abort_flag = o; o += 16;
     L.total = o;
@@ -287,11 +288,12 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
     if (fold)
         for (int cc = tid; cc < lc; cc += kThreads) cp_async16(smem_u32(nw + 8 * cc), a.norm_w + c0 + 8 * cc);
 
-    // finalising warps keep bias and alpha of their lane's logit
-    float bias_l = 0.f, alpha_l = 0.f;
-    if (warp < kSlots && lane < kLogits) {
-        bias_l = __ldg(a.bias + lane);
-        alpha_l = __ldg(a.alpha + (lane < 4 ? 0 : (lane < 8 ? 1 : 2)));
+    // bias and alpha of each logit, read by the finalising warps (shared
+    // memory rather than registers held through the whole tile)
+    float* ba = reinterpret_cast<float*>(smem + L.ba);
+    if (tid < kLogits) {
+        ba[tid] = __ldg(a.bias + tid);
+        ba[kLogits + tid] = __ldg(a.alpha + (tid < 4 ? 0 : (tid < 8 ? 1 : 2)));
     }
 
     // Everything above reads only the weights (fn, bias, alpha, norm_w).
@@ -359,11 +361,16 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
             }
         }
 
-        // ---- 2. collapse (warps 2..11), one token per warp at a time
+        // ---- 2. collapse, one token per warp at a time, on all 12 warps
         //         (non-delayed: only sum x^2 here, the collapse follows the
-        //         pre from the finaliser)
-        if (nondel && warp >= kRowWarp0) {
-            for (int tt = warp - kRowWarp0; tt < nv; tt += kRowWarps) {
+        //         pre from the finaliser).  Warps lc % 12 .. 11 hold one fn
+        //         chunk fewer than warps 0 .. lc % 12 - 1, so the tokens are
+        //         dealt to them first: collapse plus projection then take
+        //         about as long in every warp, and no warp idles at the
+        //         barrier that ends the projection.
+        const int tt0 = (warp - lc % kWarps + kWarps) % kWarps;
+        if (nondel) {
+            for (int tt = tt0; tt < nv; tt += kWarps) {
                 float sx = 0.f;
                 for (int cc = lane; cc < lc; cc += 32) {
                     float xv[4][8];
@@ -384,8 +391,8 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
                                 mapa(smem_u32(&sq_full[par]), lane));
             }
         }
-        if (!nondel && warp >= kRowWarp0) {
-            for (int tt = warp - kRowWarp0; tt < nv; tt += kRowWarps) {
+        if (!nondel) {
+            for (int tt = tt0; tt < nv; tt += kWarps) {
                 const float p0 = pin[4 * tt], p1 = pin[4 * tt + 1], p2 = pin[4 * tt + 2], p3 = pin[4 * tt + 3];
                 float sx = 0.f, sh = 0.f;
                 for (int cc = lane; cc < lc; cc += 32) {
@@ -423,9 +430,15 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
             }
         }
 
-        // ---- 3. projection on the tensor cores, one 16-token m-tile at a time
-        const int nm = (nv + 15) >> 4;
-        for (int mt = 0; mt < nm; ++mt) {
+        // ---- 3. projection on the tensor cores.  Up to 16 tokens: one
+        //         16-row m-tile, hi and lo products in separate accumulators.
+        //         17..32 tokens: each fn fragment is split once and feeds
+        //         both m-tiles, hi and lo products sharing one accumulator
+        //         per m-tile so that the two tiles fit the registers of one
+        //         (the lo products then round against the running hi sum:
+        //         one more fp32 rounding per k-block, inside the fp32 dot
+        //         bound).
+        if (nv <= 16) {
             float dh[3][4], dl[3][4];
 #pragma unroll
             for (int nt = 0; nt < 3; ++nt)
@@ -435,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
             for (int j = 0; j < JMAX; ++j) {
                 const int q = warp + kWarps * j;
                 if (q < lc) {
-                    const unsigned char* r0 = xs + (16 * mt + g) * a.xstride + (32 * q + 8 * t4) * 2;
+                    const unsigned char* r0 = xs + g * a.xstride + (32 * q + 8 * t4) * 2;
                     const uint4 x0 = *reinterpret_cast<const uint4*>(r0);
                     const uint4 x1 = *reinterpret_cast<const uint4*>(r0 + 8 * a.xstride);
                     const uint32_t w0[4] = {x0.x, x0.y, x0.z, x0.w}, w1[4] = {x1.x, x1.y, x1.z, x1.w};
@@ -458,11 +471,54 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
             }
 #pragma unroll
             for (int nt = 0; nt < 3; ++nt) {
-                float* rr = red + (warp * kMaxTile + 16 * mt + g) * kLogits + 8 * nt + 2 * t4;
+                float* rr = red + (warp * kMaxTile + g) * kLogits + 8 * nt + 2 * t4;
                 *reinterpret_cast<float2*>(rr) = make_float2(dh[nt][0] + dl[nt][0], dh[nt][1] + dl[nt][1]);
                 *reinterpret_cast<float2*>(rr + 8 * kLogits) =
                     make_float2(dh[nt][2] + dl[nt][2], dh[nt][3] + dl[nt][3]);
             }
+        } else {
+            float d[2][3][4];
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int nt = 0; nt < 3; ++nt)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) d[mt][nt][k] = 0.f;
+#pragma unroll
+            for (int j = 0; j < JMAX; ++j) {
+                const int q = warp + kWarps * j;
+                if (q < lc) {
+                    // rows g, g + 8 (m-tile 0) and g + 16, g + 24 (m-tile 1)
+                    const unsigned char* r0 = xs + g * a.xstride + (32 * q + 8 * t4) * 2;
+#pragma unroll
+                    for (int blk = 0; blk < 4; ++blk) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int r = 0; r < 4; ++r)
+                            w[r] = *reinterpret_cast<const uint32_t*>(r0 + 8 * r * a.xstride + 4 * blk);
+                        const uint32_t af0[4] = {w[0] << 16, w[1] << 16, w[0] & 0xffff0000u, w[1] & 0xffff0000u};
+                        const uint32_t af1[4] = {w[2] << 16, w[3] << 16, w[2] & 0xffff0000u, w[3] & 0xffff0000u};
+#pragma unroll
+                        for (int nt = 0; nt < 3; ++nt) {
+                            uint32_t h0, l0, h1, l1;
+                            split_tf32(b[j][nt][2 * blk], h0, l0);
+                            split_tf32(b[j][nt][2 * blk + 1], h1, l1);
+                            mma_tf32(d[0][nt], af0, h0, h1);
+                            mma_tf32(d[1][nt], af1, h0, h1);
+                            mma_tf32(d[0][nt], af0, l0, l1);
+                            mma_tf32(d[1][nt], af1, l0, l1);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int nt = 0; nt < 3; ++nt) {
+                    float* rr = red + (warp * kMaxTile + 16 * mt + g) * kLogits + 8 * nt + 2 * t4;
+                    *reinterpret_cast<float2*>(rr) = make_float2(d[mt][nt][0], d[mt][nt][1]);
+                    *reinterpret_cast<float2*>(rr + 8 * kLogits) = make_float2(d[mt][nt][2], d[mt][nt][3]);
+                }
         }
         if (fused && tid < 4 * nv) bulk_wait_read_all();   // x_new copies done reading the x tile
         __syncthreads();  // partials complete; the x tile (delayed: also pre_in) is free
@@ -515,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
 #pragma unroll
                         for (int s2 = 0; s2 < kCtas; ++s2) l += src[s2 * kLogits];
                         const float r = 1.0f / sqrtf(sx / (float)K + a.rms_eps);
-                        l = (r * l) * alpha_l + bias_l;
+                        l = (r * l) * ba[kLogits + lane] + ba[lane];
                         if (a.logits_out) a.logits_out[t * kLogits + lane] = l;
                     }
                     // gates: lanes 0..3 pre, 4..7 post
