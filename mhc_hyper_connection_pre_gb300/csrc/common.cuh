@@ -91,19 +91,20 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 // post + pre kernel both use these steps, so the two give the same bits.
 // cw / pw: the coefficients of the NJ outputs taken (comb row i from the
 // first of them, post of each).
-template <int NJ>
-__device__ __forceinline__ void post_mix_first(float (&acc)[NJ][8], const float (&x)[8], const float* cw) {
+// NE: elements (columns) per call, 8 unless a caller works on half an item.
+template <int NJ, int NE = 8>
+__device__ __forceinline__ void post_mix_first(float (&acc)[NJ][NE], const float (&x)[NE], const float* cw) {
 #pragma unroll
     for (int j = 0; j < NJ; ++j)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[j][e] = cw[j] * x[e];
+        for (int e = 0; e < NE; ++e) acc[j][e] = cw[j] * x[e];
 }
-template <int NJ>
-__device__ __forceinline__ void post_mix_next(float (&acc)[NJ][8], const float (&x)[8], const float* cw) {
+template <int NJ, int NE = 8>
+__device__ __forceinline__ void post_mix_next(float (&acc)[NJ][NE], const float (&x)[NE], const float* cw) {
 #pragma unroll
     for (int j = 0; j < NJ; ++j)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[j][e] = fmaf(cw[j], x[e], acc[j][e]);
+        for (int e = 0; e < NE; ++e) acc[j][e] = fmaf(cw[j], x[e], acc[j][e]);
 }
 template <int NJ>
 __device__ __forceinline__ void post_mix_last(const float (&acc)[NJ][8], const float (&y)[8], const float* pw,
@@ -114,6 +115,19 @@ __device__ __forceinline__ void post_mix_last(const float (&acc)[NJ][8], const f
 #pragma unroll
         for (int e = 0; e < 8; ++e) o[e] = fmaf(pw[j], y[e], acc[j][e]);
         out[j] = pack8(o);
+    }
+}
+
+// post_mix_last on four columns: two packed bf16 pairs per output.
+template <int NJ>
+__device__ __forceinline__ void post_mix_last4(const float (&acc)[NJ][4], const float (&y)[4], const float* pw,
+                                               uint2 (&out)[NJ]) {
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+        float o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[e] = fmaf(pw[j], y[e], acc[j][e]);
+        out[j] = make_uint2(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]));
     }
 }
 

@@ -329,25 +329,33 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
                 const int tt = it / lc, cc = it - tt * lc;
                 const float* gt = gts + tt * 20;
                 // the item's four streams stay packed in registers, so each
-                // output can overwrite its stream in place at once
+                // output can overwrite its stream in place; all four outputs
+                // are formed four columns at a time, so every element is
+                // widened from bf16 once
                 uint4 xp[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     xp[i] = *reinterpret_cast<const uint4*>(xs + tt * a.xstride + (i * ncols + 8 * cc) * 2);
                 const uint4 yp = *reinterpret_cast<const uint4*>(ys + tt * 8 * a.lcmax + 8 * cc);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    float acc[1][8], v[8];
+                for (int hf = 0; hf < 2; ++hf) {
+                    float acc[4][4], v[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        unpack8(xp[i], v);
-                        if (i == 0) post_mix_first<1>(acc, v, gt + j);
-                        else post_mix_next<1>(acc, v, gt + 4 * i + j);
+                        const uint32_t w0 = hf ? xp[i].z : xp[i].x, w1 = hf ? xp[i].w : xp[i].y;
+                        v[0] = bf16lo(w0); v[1] = bf16hi(w0); v[2] = bf16lo(w1); v[3] = bf16hi(w1);
+                        if (i == 0) post_mix_first<4, 4>(acc, v, gt);
+                        else post_mix_next<4, 4>(acc, v, gt + 4 * i);
                     }
-                    unpack8(yp, v);
-                    uint4 o[1];
-                    post_mix_last<1>(acc, v, gt + 16 + j, o);
-                    *reinterpret_cast<uint4*>(xs + tt * a.xstride + (j * ncols + 8 * cc) * 2) = o[0];
+                    {
+                        const uint32_t w0 = hf ? yp.z : yp.x, w1 = hf ? yp.w : yp.y;
+                        v[0] = bf16lo(w0); v[1] = bf16hi(w0); v[2] = bf16lo(w1); v[3] = bf16hi(w1);
+                    }
+                    uint2 o[4];
+                    post_mix_last4<4>(acc, v, gt + 16, o);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        *reinterpret_cast<uint2*>(xs + tt * a.xstride + (j * ncols + 8 * cc + 4 * hf) * 2) = o[j];
                 }
             }
             fence_proxy_async_smem();   // the tile's x_new is read by bulk copies below
