@@ -64,6 +64,7 @@ constexpr int kWarps = 12;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kMaxTile = 32;               // tokens per cluster tile
 constexpr int kSlots = kMaxTile / kCtas;   // tokens each CTA finalises per tile
+constexpr int kFfmaTile = 4;    // tiles of up to this many tokens project with FFMA (project_ffma)
 constexpr int kRowWarp0 = kSlots;          // warps kRowWarp0.. collapse and fold
 constexpr int kRowWarps = kWarps - kRowWarp0;
 constexpr int kSqBytes = kCtas * 2 * 4;            // per token: 16 x (sum x^2, sum h^2)
@@ -153,6 +154,44 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Projection of a tile of NT (<= 4) tokens with fp32 FMAs on the fn
+// registers.  Lane (g, t4) sums logits g, g + 8, g + 16 over its 8 columns
+// of each of its chunks, token by token; the four lanes of a group then add
+// their sums (xor 1, then xor 2) and one of them stores the warp's partial.
+template <int JMAX, int NT>
+__device__ __forceinline__ void project_ffma(const float (&b)[JMAX][3][8], const unsigned char* xs, int xstride,
+                                             int warp, int lc, int g, int t4, float* red) {
+    float acc[NT][3];
+#pragma unroll
+    for (int tt = 0; tt < NT; ++tt)
+#pragma unroll
+        for (int nt = 0; nt < 3; ++nt) acc[tt][nt] = 0.f;
+#pragma unroll
+    for (int j = 0; j < JMAX; ++j) {
+        const int q = warp + kWarps * j;
+        if (q < lc) {
+#pragma unroll
+            for (int tt = 0; tt < NT; ++tt) {
+                float xv[8];
+                unpack8(*reinterpret_cast<const uint4*>(xs + tt * xstride + (32 * q + 8 * t4) * 2), xv);
+#pragma unroll
+                for (int nt = 0; nt < 3; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[tt][nt] = fmaf(b[j][nt][e], xv[e], acc[tt][nt]);
+            }
+        }
+    }
+#pragma unroll
+    for (int tt = 0; tt < NT; ++tt)
+#pragma unroll
+        for (int nt = 0; nt < 3; ++nt) {
+            float v = acc[tt][nt];
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            if (t4 == (tt & 3)) red[(warp * kMaxTile + tt) * kLogits + 8 * nt + g] = v;
+        }
 }
 
 template <int JMAX, int MODE>
@@ -446,7 +485,16 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
         //         (the lo products then round against the running hi sum:
         //         one more fp32 rounding per k-block, inside the fp32 dot
         //         bound).
-        if (nv <= 16) {
+        if (nv <= kFfmaTile) {
+            // a few tokens: fp32 FMAs on the fn registers (a 16-row MMA
+            // would spend most of its rows on absent tokens)
+            switch (nv) {
+                case 1: project_ffma<JMAX, 1>(b, xs, a.xstride, warp, lc, g, t4, red); break;
+                case 2: project_ffma<JMAX, 2>(b, xs, a.xstride, warp, lc, g, t4, red); break;
+                case 3: project_ffma<JMAX, 3>(b, xs, a.xstride, warp, lc, g, t4, red); break;
+                default: project_ffma<JMAX, 4>(b, xs, a.xstride, warp, lc, g, t4, red); break;
+            }
+        } else if (nv <= 16) {
             float dh[3][4], dl[3][4];
 #pragma unroll
             for (int nt = 0; nt < 3; ++nt)
