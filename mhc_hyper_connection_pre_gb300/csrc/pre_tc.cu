@@ -24,7 +24,8 @@
 // writes its K-slice of the three fn planes (184 KB at C = 5120), already in
 // the MMA's operand layout, to its region of the caller's workspace; every
 // stage then brings the matching 18 KB block with one bulk copy (L2
-// evict-last) next to the x box (L2 evict-first).  A 4-slot ring of 50 KB
+// evict-last) next to the x box (default L2 policy; evict-first was 1.6 us
+// slower).  A 4-slot ring of 50 KB
 // slots keeps 200 KB in flight per SM.  Warp roles (16 warps):
 //   warp 0       TMA producer;
 //   warp 1       MMA issuer: per stage 8 x tcgen05.mma (M128 N80 K16: two K
@@ -293,11 +294,10 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
     // after this CTA's fn reads (issued at the start they slowed those by
     // 2 us) and still well before the planes can be loaded
     if (tid == 0) {
-        const uint64_t pol_x = policy_evict_first();
         for (uint32_t q = 0; q < early; ++q) {
             const int tile = cid + (int)(q / ngroups) * ncl, grp = (int)(q % ngroups);
             mbar_arrive_expect_tx(&full[q], slot_bytes);
-            tma_load_3d_hint(stages + q * kSlotBytes, &xmap, c0 + kCols * grp, tile * kTile, 0, &full[q], pol_x);
+            tma_load_3d(stages + q * kSlotBytes, &xmap, c0 + kCols * grp, tile * kTile, 0, &full[q]);
         }
     }
     if (fold)
@@ -313,7 +313,7 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
     if (warp == 0) {
         // ================================================== TMA producer
         if (lane == 0) {
-            const uint64_t pol_x = policy_evict_first(), pol_w = policy_evict_last();
+            const uint64_t pol_w = policy_evict_last();
             for (uint32_t q = 0; q < early; ++q)   // fn blocks of the slots started before the planes existed
                 bulk_load_hint(stages + q * kSlotBytes + kXBytes, wreg + (q % ngroups) * kWStage, kWStage,
                                &full[q], pol_w);
@@ -329,7 +329,7 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
                 if (!mbar_wait(&empty[s], ((g / kStages) & 1) ^ 1, abort) || *abort) break;
                 unsigned char* slot = stages + s * kSlotBytes;
                 mbar_arrive_expect_tx(&full[s], slot_bytes);
-                tma_load_3d_hint(slot, &xmap, c0 + kCols * grp, tile * kTile, 0, &full[s], pol_x);
+                tma_load_3d(slot, &xmap, c0 + kCols * grp, tile * kTile, 0, &full[s]);
                 bulk_load_hint(slot + kXBytes, wreg + grp * kWStage, kWStage, &full[s], pol_w);
             }
             // drain: the last load of every slot has landed before the CTA
