@@ -156,6 +156,16 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// ((q0 + q1) + (q2 + q3)) + ... : a fixed pairwise order, depth 4.
+__device__ __forceinline__ float tree_sum16(const float (&q)[16]) {
+    float a[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = q[2 * i] + q[2 * i + 1];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = a[2 * i] + a[2 * i + 1];
+    return (a[0] + a[1]) + (a[2] + a[3]);
+}
+
 // Projection of a tile of NT (<= 4) tokens with fp32 FMAs on the fn
 // registers.  Lane (g, t4) sums logits g, g + 8, g + 16 over its 8 columns
 // of each of its chunks, token by token; the four lanes of a group then add
@@ -202,6 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t4 = lane & 3;
     const int C = a.C, K = 4 * C, nch = C >> 3;
+    const float inv_k = 1.0f / (float)K;
     const int ch0 = rank * nch / kCtas;
     const int lc = (rank + 1) * nch / kCtas - ch0;   // 8-column groups of this CTA
     const int ncols = 8 * lc;
@@ -616,17 +627,21 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
                 bool ok = mbar_wait<true>(&dots_full[par * kSlots + slot], (round >> 1) & 1, abort);
                 ok = ok && mbar_wait<true>(&sq_full[par], (round >> 1) & 1, abort);
                 if (ok) {
-                    // sum x^2 over the 16 slices, rank order (every lane)
+                    // sums over the 16 slices as fixed pairwise trees (four
+                    // dependent adds instead of sixteen): x^2 in every lane,
+                    // the lane's logit in lanes 0..23
                     const float* sq = inbox_sq + (par * kMaxTile + tok) * kCtas * 2;
-                    float sx = 0.f;
+                    float q[kCtas];
 #pragma unroll
-                    for (int s2 = 0; s2 < kCtas; ++s2) sx += sq[2 * s2];
+                    for (int s2 = 0; s2 < kCtas; ++s2) q[s2] = sq[2 * s2];
+                    const float sx = tree_sum16(q);
                     float l = 0.f;
                     if (lane < kLogits) {
                         const float* src = inbox_dots + (par * kSlots + slot) * kCtas * kLogits + lane;
 #pragma unroll
-                        for (int s2 = 0; s2 < kCtas; ++s2) l += src[s2 * kLogits];
-                        const float r = 1.0f / sqrtf(sx / (float)K + a.rms_eps);
+                        for (int s2 = 0; s2 < kCtas; ++s2) q[s2] = src[s2 * kLogits];
+                        l = tree_sum16(q);
+                        const float r = rsqrtf(sx * inv_k + a.rms_eps);
                         l = (r * l) * ba[kLogits + lane] + ba[lane];
                         if (a.logits_out) a.logits_out[t * kLogits + lane] = l;
                     }
