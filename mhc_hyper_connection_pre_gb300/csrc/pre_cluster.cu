@@ -18,21 +18,23 @@
 // (fp32) for the whole launch.  Per tile of TT tokens:
 //   1. the tile's x slice and pre_in arrive by cp.async (the next tile's load
 //      is issued as soon as this one's MMA is done);
-//   2. warps 2..11 collapse one token at a time (h to shared memory, or
-//      straight to layer_input without the fold) and push the token's
-//      partial sum x^2 and sum h^2 to every CTA of the cluster;
-//   3. every warp multiplies its chunks on the tensor cores:
-//      mma.sync m16n8k8 with tf32 inputs and fp32 accumulation, tokens as M,
-//      the 24 logits as three n-tiles of 8.  x (bf16) is exact in tf32; fn is
-//      split into hi = fn with the low 13 mantissa bits cleared (exactly a
-//      tf32 value) and lo = fn - hi (exact in fp32), two MMAs per block; the
-//      MMA keeps 10 mantissa bits of lo, so each product carries a relative
-//      error below 2^-20;
+//   2. all 12 warps collapse one token at a time (h to shared memory, or
+//      straight to layer_input without the fold), the tokens dealt first to
+//      the warps with one chunk fewer, and push the token's partial sum x^2
+//      and sum h^2 to every CTA of the cluster;
+//   3. every warp multiplies its chunks: up to 4 tokens with fp32 FMAs on
+//      the fn registers, otherwise on the tensor cores with mma.sync m16n8k8
+//      (tf32 inputs, fp32 accumulation, tokens as M in one or two 16-row
+//      m-tiles, the 24 logits as three n-tiles of 8).  x (bf16) is exact in
+//      tf32; fn is split into hi = fn with the low 13 mantissa bits cleared
+//      (exactly a tf32 value) and lo = fn - hi (exact in fp32), two MMAs per
+//      block; the MMA keeps 10 mantissa bits of lo, so each product carries
+//      a relative error below 2^-20;
 //   4. the 12 warps' partial dot products are summed in shared memory in a
 //      fixed order and pushed to the finalising CTA, four logits per store;
 //   5. CTA r finalises tokens r and r + 16 of the tile (warps 0 and 1): it
-//      sums the 16 CTAs' partials in rank order and forms r, the logits, the
-//      gates and the Sinkhorn comb;
+//      sums the 16 CTAs' partials in a fixed pairwise order and forms r, the
+//      logits, the gates and the Sinkhorn comb;
 //   6. meanwhile warps 2..11 form each token's fold scale from the 16 sum h^2
 //      partials (the same sum, in rank order, in every CTA: the same bits),
 //      fold h and store layer_input.
@@ -65,7 +67,7 @@ constexpr int kThreads = 32 * kWarps;
 constexpr int kMaxTile = 32;               // tokens per cluster tile
 constexpr int kSlots = kMaxTile / kCtas;   // tokens each CTA finalises per tile
 constexpr int kFfmaTile = 4;    // tiles of up to this many tokens project with FFMA (project_ffma)
-constexpr int kRowWarp0 = kSlots;          // warps kRowWarp0.. collapse and fold
+constexpr int kRowWarp0 = kSlots;          // warps kRowWarp0.. fold (and run the non-delayed collapse)
 constexpr int kRowWarps = kWarps - kRowWarp0;
 constexpr int kSqBytes = kCtas * 2 * 4;            // per token: 16 x (sum x^2, sum h^2)
 constexpr int kNumBars = 6 + 2 * kSlots;           // sq_full[p], dots_full[p][slot], pre_full[p], sh_full[p]
