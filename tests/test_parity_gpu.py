@@ -84,6 +84,10 @@ def test_config1_decode_sweep(T):
     (127, 5120, False), (129, 5120, True), (17, 6144, True), (64, 6144, False),
     (1000, 5120, True), (33, 4096, False), (5, 128, True), (2, 2048, True),
     (300, 1000, True), (500, 6144, False), (225, 136, False),
+    # tile sizes at the projection's form boundaries: 4 tokens (the largest
+    # fp32-FMA tile), 16 (the largest single m-tile), 17 and 32 (two m-tiles
+    # sharing each fn fragment)
+    (26, 5120, True), (112, 5120, False), (113, 5120, True), (224, 5120, True),
 ])
 def test_token_and_hidden_sweep(T, C, fold):
     """Ragged token tails (tile sizes that do not divide T), hidden sizes
@@ -225,8 +229,9 @@ def _fused_case(T, C, fold, seed):
     return d, gd, g["comb"].clone(), g["post"].clone()
 
 
-@pytest.mark.parametrize("T,C,fold", [(1, 5120, True), (5, 5120, False), (32, 5120, True), (100, 5120, True),
-                                      (33, 1000, False), (300, 1000, True), (300, 5120, True), (7, 8, True)])
+@pytest.mark.parametrize("T,C,fold", [(1, 5120, True), (5, 5120, False), (20, 5120, True), (32, 5120, True),
+                                      (100, 5120, True), (120, 5120, False), (33, 1000, False), (300, 1000, True),
+                                      (300, 5120, True), (7, 8, True)])
 def test_fused_seam_is_bit_identical_to_post_then_pre(T, C, fold):
     """mhc_post_pre_delayed gives exactly the bits of mhc_post followed by
     mhc_pre_delayed: one kernel below 256 tokens (and at C = 1000), two at
@@ -295,8 +300,9 @@ def test_fused_seam_is_one_launch_in_a_graph():
     g.close()
 
 
-@pytest.mark.parametrize("T,C,fold", [(1, 5120, True), (7, 5120, False), (33, 5120, True), (128, 5120, False),
-                                      (100, 1000, True), (300, 1000, False), (300, 5120, True), (1000, 5120, False),
+@pytest.mark.parametrize("T,C,fold", [(1, 5120, True), (7, 5120, False), (26, 5120, True), (33, 5120, True),
+                                      (128, 5120, False), (100, 1000, True), (300, 1000, False), (300, 5120, True),
+                                      (1000, 5120, False),
                                       (5, 8, True), (2000, 768, True), (2000, 768, False), (4097, 4096, True),
                                       (600, 6144, True), (600, 6144, False), (256, 5120, True), (257, 2048, False)])
 def test_nondelayed_pre_equals_delayed_with_its_own_pre(T, C, fold):
