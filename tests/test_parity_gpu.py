@@ -231,11 +231,16 @@ def _fused_case(T, C, fold, seed):
 
 @pytest.mark.parametrize("T,C,fold", [(1, 5120, True), (5, 5120, False), (20, 5120, True), (32, 5120, True),
                                       (100, 5120, True), (120, 5120, False), (33, 1000, False), (300, 1000, True),
-                                      (300, 5120, True), (7, 8, True)])
+                                      (300, 5120, True), (7, 8, True),
+                                      # from 256 tokens: a ragged last tile, other hidden sizes,
+                                      # several tiles per cluster, a half last stage (C = 768)
+                                      (1383, 5120, False), (4097, 4096, True), (300, 2048, False),
+                                      (2000, 5120, True), (600, 768, True)])
 def test_fused_seam_is_bit_identical_to_post_then_pre(T, C, fold):
     """mhc_post_pre_delayed gives exactly the bits of mhc_post followed by
-    mhc_pre_delayed: one kernel below 256 tokens (and at C = 1000), two at
-    T = 300, C = 5120; multi-round tiles at T = 300, C = 1000."""
+    mhc_pre_delayed: one kernel below 256 tokens (and at C = 1000, multi-round
+    tiles at T = 300), the post kernel then the tensor-core pre from 256
+    tokens."""
     d, gd, comb, post = _fused_case(T, C, fold, seed=1100 + T + C)
     xn_ref = mhc.post(gd["x"], gd["y"], comb, post)
     ref = mhc.pre_delayed(xn_ref, gd["pre_in"], gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"], return_logits=True)
@@ -265,10 +270,12 @@ def test_fused_seam_in_place_and_shared_gate_buffers(T):
         assert torch.equal(got[k], ref[k]), k
 
 
-def test_fused_seam_against_the_oracle():
+@pytest.mark.parametrize("T", [24, 300])
+def test_fused_seam_against_the_oracle(T):
     """The fused call checked against the oracle directly: x_new against the
-    oracle's post, the pre outputs against the oracle's pre on that x_new."""
-    T, C = 24, 5120
+    oracle's post, the pre outputs against the oracle's pre on that x_new
+    (T = 300: the post kernel, then the tensor-core pre)."""
+    C = 5120
     d, gd, comb, post = _fused_case(T, C, True, seed=1500)
     got = mhc.post_pre_delayed(gd["x"], gd["y"], comb, post, gd["pre_in"], gd["fn"], gd["bias"], gd["alpha"],
                                gd["norm_w"], return_logits=True)
@@ -283,17 +290,20 @@ def test_fused_seam_against_the_oracle():
     _check_pre({k: v.cpu() for k, v in got.items() if k != "x_new"}, o, xb2, d2, fold=True)
 
 
-def test_fused_seam_is_one_launch_in_a_graph():
-    d, gd, comb, post = _fused_case(4, 5120, True, seed=1600)
-    out = {"pre": torch.empty(4, 4, device="cuda"), "post": torch.empty(4, 4, device="cuda"),
-           "comb": torch.empty(4, 4, 4, device="cuda"),
-           "layer_input": torch.empty(4, 5120, dtype=torch.bfloat16, device="cuda")}
+@pytest.mark.parametrize("T,nodes", [(4, 1), (300, 2)])
+def test_fused_seam_is_one_launch_in_a_graph(T, nodes):
+    """One kernel node below 256 tokens (the cluster kernel); from 256
+    tokens the post kernel and the tensor-core pre."""
+    d, gd, comb, post = _fused_case(T, 5120, True, seed=1600)
+    out = {"pre": torch.empty(T, 4, device="cuda"), "post": torch.empty(T, 4, device="cuda"),
+           "comb": torch.empty(T, 4, 4, device="cuda"),
+           "layer_input": torch.empty(T, 5120, dtype=torch.bfloat16, device="cuda")}
     xn = torch.empty_like(gd["x"])
     s = torch.cuda.Stream()
     g = SeamGraph(lambda st: mhc.post_pre_delayed(gd["x"], gd["y"], comb, post, gd["pre_in"], gd["fn"],
                                                   gd["bias"], gd["alpha"], gd["norm_w"], x_new=xn, out=out,
                                                   stream=st), s)
-    assert g.kernel_nodes == 1, g.kernel_nodes
+    assert g.kernel_nodes == nodes, g.kernel_nodes
     g.replay(3)
     s.synchronize()
     assert mhc.device_status() == 0
