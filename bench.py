@@ -488,13 +488,14 @@ def run_ours(args, rank, world, local):
             mhc.post(cx, cy, co["comb"], co["post"], out=cx, stream=st)
 
         chain_us = {}
-        for fused, ov in ((False, False), (False, True), (True, False), (True, True)):
+        for fused, ov, early in ((False, False, False), (False, True, False), (True, False, False),
+                                 (True, True, False), (False, True, True), (True, True, True)):
             mhc.set_launch_overlap(ov)
             step_fn = chain_step_fused if fused else chain_step
             with torch.cuda.stream(s):
                 step_fn(s)
             s.synchronize()
-            g = SeamGraph(step_fn, s)
+            g = SeamGraph(step_fn, s, early_launch=early)
             g.replay(3)
             meds = []
             for _ in range(5):
@@ -504,15 +505,19 @@ def run_ours(args, rank, world, local):
                 b.record(s)
                 s.synchronize()
                 meds.append(a.elapsed_time(b) * 1e3 / 200)
-            chain_us[(fused, ov)] = round(statistics.median(meds), 2)
+            chain_us[(fused, ov, early)] = round(statistics.median(meds), 2)
             if fused:
                 fused_nodes = g.kernel_nodes
             else:
                 nodes = g.kernel_nodes
             g.close()
         mhc.set_launch_overlap(False)
-        chain = {"us_per_step": chain_us[(False, False)], "us_per_step_overlap": chain_us[(False, True)],
-                 "us_per_step_fused": chain_us[(True, False)], "us_per_step_fused_overlap": chain_us[(True, True)],
+        chain = {"us_per_step": chain_us[(False, False, False)],
+                 "us_per_step_overlap": chain_us[(False, True, False)],
+                 "us_per_step_fused": chain_us[(True, False, False)],
+                 "us_per_step_fused_overlap": chain_us[(True, True, False)],
+                 "us_per_step_overlap_early": chain_us[(False, True, True)],
+                 "us_per_step_fused_overlap_early": chain_us[(True, True, True)],
                  "seams": CHAIN_SEAMS, "T": CHAIN_T, "kernel_nodes": nodes,
                  "launches_per_seam": (nodes - CHAIN_SEAMS) / CHAIN_SEAMS,
                  "launches_per_seam_fused": (fused_nodes - CHAIN_SEAMS) / CHAIN_SEAMS,

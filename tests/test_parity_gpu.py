@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import mhc_hyper_connection_pre_gb300 as mhc
-from mhc_hyper_connection_pre_gb300.graphs import SeamGraph
+from mhc_hyper_connection_pre_gb300.graphs import SeamGraph, edge_ports
 from workloads import seam_inputs, bf16_bits, chain_seam_params, chain_stub_delta
 from parity import (assert_gates, assert_bf16, assert_bitexact, assert_logits, logit_bound,
                     post_abs_scale)
@@ -591,6 +591,74 @@ def test_fused_chain_matches_and_overlaps_exactly(T):
         assert mhc.device_status() == 0
         for got, want in zip(_chain_result(b), ref):
             assert torch.equal(got, want)
+        g.close()
+    finally:
+        mhc.set_launch_overlap(prev)
+
+
+def _stub_chain(b, params, deltas, y, stream, fused):
+    """The decode step as the benchmark runs it: each seam's sublayer is a
+    PyTorch kernel (y = layer_input + D_s) between pre and post; with
+    ``fused``, post(s - 1) runs inside pre(s) and the last post alone."""
+    outs = b["outs"]
+    for si, o in enumerate(outs):
+        p = params[si]
+        out = dict(o, pre=b["pre"][(si + 1) & 1])
+        if fused and si > 0:
+            q = outs[si - 1]
+            mhc.post_pre_delayed(b["x"], y, q["comb"], q["post"], b["pre"][si & 1], p["fn"], p["bias"],
+                                 p["alpha"], p["norm_w"], x_new=b["x"], out=out, stream=stream)
+        else:
+            mhc.pre_delayed(b["x"], b["pre"][si & 1], p["fn"], p["bias"], p["alpha"], p["norm_w"], out=out,
+                            stream=stream)
+        with torch.cuda.stream(stream):
+            torch.add(o["layer_input"], deltas[si], out=y)
+        if not fused:
+            mhc.post(b["x"], y, o["comb"], o["post"], out=b["x"], stream=stream)
+    if fused:
+        mhc.post(b["x"], y, outs[-1]["comb"], outs[-1]["post"], out=b["x"], stream=stream)
+
+
+@pytest.mark.parametrize("T,fused", [(4, False), (4, True), (100, False), (100, True)])
+def test_early_launch_after_a_torch_kernel_is_bit_identical(T, fused):
+    """A graph whose programmatic edges leave the upstream kernel's
+    launch-completion port (SeamGraph early_launch), with a PyTorch kernel
+    between pre and post, gives the bits of the same chain run eagerly with
+    launch overlap off.  Every programmatic edge is moved: one into each
+    seam kernel that follows another kernel."""
+    seams, C, dev = 8, 5120, "cuda"
+    params = [chain_seam_params(si, device=dev) for si in range(seams)]
+    deltas = [chain_stub_delta(si, T=T, device=dev) for si in range(seams)]
+    d = seam_inputs(T, seed=970 + T, device=dev)
+    b = _chain_buffers(T, seams, C, dev)
+    y = torch.empty(T, C, dtype=torch.bfloat16, device=dev)
+    s = torch.cuda.Stream()
+
+    def reset():
+        b["x"].copy_(d["x"])
+        b["pre"][0].copy_(d["pre_in"])
+        y.zero_()
+        torch.cuda.synchronize()
+
+    prev = mhc.set_launch_overlap(False)
+    try:
+        reset()
+        _stub_chain(b, params, deltas, y, s, fused)
+        s.synchronize()
+        ref = _chain_result(b) + [y.clone()]
+        mhc.set_launch_overlap(True)
+        g = SeamGraph(lambda st: _stub_chain(b, params, deltas, y, st, fused), s, early_launch=True)
+        assert g.kernel_nodes == (2 * seams + 1 if fused else 3 * seams), g.kernel_nodes
+        assert g.moved_edges == (seams if fused else 2 * seams - 1), g.moved_edges
+        ports = edge_ports(g.graph)
+        assert ports.get((1, 1), 0) == 0 and ports.get((2, 1), 0) == g.moved_edges, ports
+        for _ in range(3):
+            reset()
+            g.replay(1)
+            s.synchronize()
+            assert mhc.device_status() == 0
+            for got, want in zip(_chain_result(b) + [y], ref):
+                assert torch.equal(got, want)
         g.close()
     finally:
         mhc.set_launch_overlap(prev)
