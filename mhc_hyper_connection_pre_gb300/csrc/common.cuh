@@ -91,7 +91,7 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 // post + pre kernel both use these steps, so the two give the same bits.
 // cw / pw: the coefficients of the NJ outputs taken (comb row i from the
 // first of them, post of each).
-// NE: elements (columns) per call, 8 unless a caller works on half an item.
+// NE: elements (columns) per call: 8, or 4 / 2 where a caller splits an item.
 template <int NJ, int NE = 8>
 __device__ __forceinline__ void post_mix_first(float (&acc)[NJ][NE], const float (&x)[NE], const float* cw) {
 #pragma unroll
@@ -129,6 +129,14 @@ __device__ __forceinline__ void post_mix_last4(const float (&acc)[NJ][4], const 
         for (int e = 0; e < 4; ++e) o[e] = fmaf(pw[j], y[e], acc[j][e]);
         out[j] = make_uint2(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]));
     }
+}
+
+// post_mix_last on two columns: one packed bf16 pair per output.
+template <int NJ>
+__device__ __forceinline__ void post_mix_last2(const float (&acc)[NJ][2], const float (&y)[2], const float* pw,
+                                               uint32_t (&out)[NJ]) {
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) out[j] = pack_bf16x2(fmaf(pw[j], y[0], acc[j][0]), fmaf(pw[j], y[1], acc[j][1]));
 }
 
 // Streaming 16-byte global load / store (data touched once).

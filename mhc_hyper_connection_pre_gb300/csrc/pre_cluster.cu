@@ -129,7 +129,7 @@ __host__ __device__ inline Layout dec_layout(int lcmax, int mode) {
     // non-delayed: this tile's pre per token, sum h^2 partials [parity]
     L.prex = o;  o += mode == kNonDelayed ? 2 * kMaxTile * 16 : 0;
     L.shin = o;  o += mode == kNonDelayed ? 2 * kMaxTile * kCtas * 4 : 0;
-    L.ba = o;    o += 2 * kLogits * 4;   // per logit: bias, alpha of its group
+    L.ba = o;    o += 2 * kLogits * 4;   // bias of each logit, then the three alphas
     L.bars = o;  o += kNumBars * 8;
     L.abort_flag = o; o += 16;
     L.total = o;
@@ -138,6 +138,9 @@ __host__ __device__ inline Layout dec_layout(int lcmax, int mode) {
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
@@ -340,13 +343,14 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
     if (fold)
         for (int cc = tid; cc < lc; cc += kThreads) cp_async16(smem_u32(nw + 8 * cc), a.norm_w + c0 + 8 * cc);
 
-    // bias and alpha of each logit, read by the finalising warps (shared
-    // memory rather than registers held through the whole tile)
+    // bias and alpha, read by the finalising warps (shared memory rather
+    // than registers held through the whole tile).  Copied asynchronously:
+    // a thread that stored a loaded value itself would wait here for the
+    // load, which queues behind its warp's fn loads, and would then issue
+    // its share of the x tile's copies that much later.
     float* ba = reinterpret_cast<float*>(smem + L.ba);
-    if (tid < kLogits) {
-        ba[tid] = __ldg(a.bias + tid);
-        ba[kLogits + tid] = __ldg(a.alpha + (tid < 4 ? 0 : (tid < 8 ? 1 : 2)));
-    }
+    if (tid < kLogits) cp_async4(smem_u32(ba + tid), a.bias + tid);
+    else if (tid < kLogits + 3) cp_async4(smem_u32(ba + tid), a.alpha + (tid - kLogits));
 
     // Everything above reads only the weights (fn, bias, alpha, norm_w).
     // Under programmatic dependent launch it overlaps the previous kernel;
@@ -377,37 +381,65 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
         // ---- 1b. fused post of the previous seam: x_new for this CTA's
         //          slice of the tile, written out and kept in place of x
         if (fused) {
-            for (int it = tid; it < nv * lc; it += kThreads) {
-                const int tt = it / lc, cc = it - tt * lc;
-                const float* gt = gts + tt * 20;
-                // the item's four streams stay packed in registers, so each
-                // output can overwrite its stream in place; all four outputs
-                // are formed four columns at a time, so every element is
-                // widened from bf16 once
-                uint4 xp[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    xp[i] = *reinterpret_cast<const uint4*>(xs + tt * a.xstride + (i * ncols + 8 * cc) * 2);
-                const uint4 yp = *reinterpret_cast<const uint4*>(ys + tt * 8 * a.lcmax + 8 * cc);
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    float acc[4][4], v[4];
+            if (4 * nv * lc <= kThreads) {
+                // a few items (decode): four threads per item, two columns
+                // each, all in one pass; every thread reads and overwrites
+                // only its own columns, with the per-output order below
+                for (int it = tid; it < 4 * nv * lc; it += kThreads) {
+                    const int item = it >> 2, qq = it & 3;
+                    const int tt = item / lc, cc = item - tt * lc;
+                    const float* gt = gts + tt * 20;
+                    unsigned char* xb = xs + tt * a.xstride + (8 * cc + 2 * qq) * 2;
+                    float acc[4][2], v[2];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const uint32_t w0 = hf ? xp[i].z : xp[i].x, w1 = hf ? xp[i].w : xp[i].y;
-                        v[0] = bf16lo(w0); v[1] = bf16hi(w0); v[2] = bf16lo(w1); v[3] = bf16hi(w1);
-                        if (i == 0) post_mix_first<4, 4>(acc, v, gt);
-                        else post_mix_next<4, 4>(acc, v, gt + 4 * i);
+                        const uint32_t w = *reinterpret_cast<const uint32_t*>(xb + i * ncols * 2);
+                        v[0] = bf16lo(w);
+                        v[1] = bf16hi(w);
+                        if (i == 0) post_mix_first<4, 2>(acc, v, gt);
+                        else post_mix_next<4, 2>(acc, v, gt + 4 * i);
                     }
-                    {
-                        const uint32_t w0 = hf ? yp.z : yp.x, w1 = hf ? yp.w : yp.y;
-                        v[0] = bf16lo(w0); v[1] = bf16hi(w0); v[2] = bf16lo(w1); v[3] = bf16hi(w1);
-                    }
-                    uint2 o[4];
-                    post_mix_last4<4>(acc, v, gt + 16, o);
+                    const uint32_t wy = *reinterpret_cast<const uint32_t*>(ys + tt * 8 * a.lcmax + 8 * cc + 2 * qq);
+                    v[0] = bf16lo(wy);
+                    v[1] = bf16hi(wy);
+                    uint32_t o[4];
+                    post_mix_last2<4>(acc, v, gt + 16, o);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        *reinterpret_cast<uint2*>(xs + tt * a.xstride + (j * ncols + 8 * cc + 4 * hf) * 2) = o[j];
+                    for (int j = 0; j < 4; ++j) *reinterpret_cast<uint32_t*>(xb + j * ncols * 2) = o[j];
+                }
+            } else {
+                for (int it = tid; it < nv * lc; it += kThreads) {
+                    const int tt = it / lc, cc = it - tt * lc;
+                    const float* gt = gts + tt * 20;
+                    // the item's four streams stay packed in registers, so each
+                    // output can overwrite its stream in place; all four outputs
+                    // are formed four columns at a time, so every element is
+                    // widened from bf16 once
+                    uint4 xp[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        xp[i] = *reinterpret_cast<const uint4*>(xs + tt * a.xstride + (i * ncols + 8 * cc) * 2);
+                    const uint4 yp = *reinterpret_cast<const uint4*>(ys + tt * 8 * a.lcmax + 8 * cc);
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        float acc[4][4], v[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const uint32_t w0 = hf ? xp[i].z : xp[i].x, w1 = hf ? xp[i].w : xp[i].y;
+                            v[0] = bf16lo(w0); v[1] = bf16hi(w0); v[2] = bf16lo(w1); v[3] = bf16hi(w1);
+                            if (i == 0) post_mix_first<4, 4>(acc, v, gt);
+                            else post_mix_next<4, 4>(acc, v, gt + 4 * i);
+                        }
+                        {
+                            const uint32_t w0 = hf ? yp.z : yp.x, w1 = hf ? yp.w : yp.y;
+                            v[0] = bf16lo(w0); v[1] = bf16hi(w0); v[2] = bf16lo(w1); v[3] = bf16hi(w1);
+                        }
+                        uint2 o[4];
+                        post_mix_last4<4>(acc, v, gt + 16, o);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            *reinterpret_cast<uint2*>(xs + tt * a.xstride + (j * ncols + 8 * cc + 4 * hf) * 2) = o[j];
+                    }
                 }
             }
             fence_proxy_async_smem();   // the tile's x_new is read by bulk copies below
@@ -644,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
                         for (int s2 = 0; s2 < kCtas; ++s2) q[s2] = src[s2 * kLogits];
                         l = tree_sum16(q);
                         const float r = rsqrtf(sx * inv_k + a.rms_eps);
-                        l = (r * l) * ba[kLogits + lane] + ba[lane];
+                        l = (r * l) * ba[kLogits + (lane < 4 ? 0 : (lane < 8 ? 1 : 2))] + ba[lane];
                         if (a.logits_out) a.logits_out[t * kLogits + lane] = l;
                     }
                     // gates: lanes 0..3 pre, 4..7 post
