@@ -188,6 +188,24 @@ __device__ __forceinline__ void sinkhorn_iterations(float (&P)[16], int iters) {
         for (int j = 0; j < 4; ++j) P[4 * i + j] = (P[4 * i + j] * R[i]) * Cs[j];
 }
 
+// Iteration 1's row step of the comb's Sinkhorn, by one thread: the row
+// softmax (max subtracted per row) of the 4x4 row-major comb logits l16,
+// plus eps on every entry.
+__device__ __forceinline__ void comb_softmax_eps(const float* l16, float eps, float (&P)[16]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float* l = l16 + 4 * i;
+        float mx = fmaxf(fmaxf(l[0], l[1]), fmaxf(l[2], l[3]));
+        float e0 = expf(l[0] - mx), e1 = expf(l[1] - mx);
+        float e2 = expf(l[2] - mx), e3 = expf(l[3] - mx);
+        float inv = rcp_approx(((e0 + e1) + e2) + e3);
+        P[4 * i + 0] = e0 * inv + eps;
+        P[4 * i + 1] = e1 * inv + eps;
+        P[4 * i + 2] = e2 * inv + eps;
+        P[4 * i + 3] = e3 * inv + eps;
+    }
+}
+
 // Per-token gates and comb from the 2n+n^2 logits, in fp32, by one thread.
 // pre = sigmoid(l[0:4]), post = 2 sigmoid(l[4:8]); comb = Sinkhorn on the
 // 4x4 row-major comb logits l[8:24]: iteration 1 is the row softmax (max
@@ -203,17 +221,7 @@ __device__ __forceinline__ void gates_and_comb(const float (&l)[kLogits], int it
         pre[i] = __fdividef(1.0f, 1.0f + expf(-l[i]));
         post[i] = __fdividef(2.0f, 1.0f + expf(-l[4 + i]));
     }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float mx = fmaxf(fmaxf(l[8 + 4 * i], l[9 + 4 * i]), fmaxf(l[10 + 4 * i], l[11 + 4 * i]));
-        float e0 = expf(l[8 + 4 * i] - mx), e1 = expf(l[9 + 4 * i] - mx);
-        float e2 = expf(l[10 + 4 * i] - mx), e3 = expf(l[11 + 4 * i] - mx);
-        float inv = rcp_approx(((e0 + e1) + e2) + e3);
-        P[4 * i + 0] = e0 * inv + eps;
-        P[4 * i + 1] = e1 * inv + eps;
-        P[4 * i + 2] = e2 * inv + eps;
-        P[4 * i + 3] = e3 * inv + eps;
-    }
+    comb_softmax_eps(l + 8, eps, P);
     sinkhorn_iterations(P, iters);
 }
 

@@ -32,17 +32,18 @@
 //      a relative error below 2^-20;
 //   4. the 12 warps' partial dot products are summed in shared memory in a
 //      fixed order and pushed to the finalising CTA, four logits per store;
-//   5. CTA r finalises tokens r and r + 16 of the tile (warps 0 and 1): it
-//      sums the 16 CTAs' partials in a fixed pairwise order and forms r, the
-//      logits, the gates and the Sinkhorn comb;
+//   5. CTA r finalises tokens r and r + 16 of the tile: it sums the 16
+//      CTAs' partials in a fixed pairwise order and forms r and the logits;
+//      warps 0 and 1 form the comb (row softmax and Sinkhorn in one lane,
+//      the steps of the prefill kernels), warps 2 and 3 the gates;
 //   6. meanwhile warps 2..11 form each token's fold scale from the 16 sum h^2
 //      partials (the same sum, in rank order, in every CTA: the same bits),
 //      fold h and store layer_input.
 // Non-delayed (MODE kNonDelayed, the V4 form without an incoming pre-mix):
 // the collapse needs this tile's own pre, so step 2 only sums x^2; the
-// finalising CTA sends each token's pre to all 16 CTAs as soon as it has the
-// logits, then every CTA collapses with it and exchanges sum h^2 for the
-// fold, while the finaliser goes on with the comb.  The x tile is read by
+// finalising CTA's gate warp sends each token's pre to all 16 CTAs as soon
+// as it has the logits, then every CTA collapses with it and exchanges sum
+// h^2 for the fold, while the comb warp runs the Sinkhorn chain.  The x tile is read by
 // that collapse, so the next tile's x is fetched only after it.
 //
 // Fused with the previous seam's post (MODE kFusedPost): before step 2 every
@@ -67,7 +68,8 @@ constexpr int kThreads = 32 * kWarps;
 constexpr int kMaxTile = 32;               // tokens per cluster tile
 constexpr int kSlots = kMaxTile / kCtas;   // tokens each CTA finalises per tile
 constexpr int kFfmaTile = 4;    // tiles of up to this many tokens project with FFMA (project_ffma)
-constexpr int kRowWarp0 = kSlots;          // warps kRowWarp0.. fold (and run the non-delayed collapse)
+constexpr int kRowWarp0 = kSlots;          // warps kRowWarp0.. fold (and run the non-delayed collapse);
+                                            // the first kSlots of them also form the gates
 constexpr int kRowWarps = kWarps - kRowWarp0;
 constexpr int kSqBytes = kCtas * 2 * 4;            // per token: 16 x (sum x^2, sum h^2)
 constexpr int kNumBars = 6 + 2 * kSlots;           // sq_full[p], dots_full[p][slot], pre_full[p], sh_full[p]
@@ -652,60 +654,67 @@ __global__ void __launch_bounds__(kThreads, 1) pre_decode_kernel(const Args a) {
             arrived = true;
         }
 
-        // ---- 5. finalise token 16 * warp + rank (warps 0, 1)
-        if (warp < kSlots) {
-            const int slot = warp;
+        // ---- 5. finalise token 16 * slot + rank.  Warp slot (0, 1) forms the
+        //         comb: its 16 logits gathered into lane 0, which takes the
+        //         row softmax and the Sinkhorn chain.  Warp kSlots + slot
+        //         (2, 3) forms the pre and post gates (and stores the logits)
+        //         meanwhile, so that none of that precedes the chain.
+        if (warp < 2 * kSlots) {
+            const bool comb_warp = warp < kSlots;
+            const int slot = comb_warp ? warp : warp - kSlots;
             const int tok = kCtas * slot + rank;
             if (tok < nv) {
                 const int64_t t = t0 + tok;
                 bool ok = mbar_wait<true>(&dots_full[par * kSlots + slot], (round >> 1) & 1, abort);
                 ok = ok && mbar_wait<true>(&sq_full[par], (round >> 1) & 1, abort);
+                ok = __all_sync(0xffffffffu, ok);   // one outcome per warp (its shuffles below)
                 if (ok) {
                     // sums over the 16 slices as fixed pairwise trees (four
                     // dependent adds instead of sixteen): x^2 in every lane,
-                    // the lane's logit in lanes 0..23
+                    // logit li in the lanes that form one
                     const float* sq = inbox_sq + (par * kMaxTile + tok) * kCtas * 2;
                     float q[kCtas];
 #pragma unroll
                     for (int s2 = 0; s2 < kCtas; ++s2) q[s2] = sq[2 * s2];
                     const float sx = tree_sum16(q);
+                    const int li = comb_warp ? 8 + lane : lane;
+                    const int nl = comb_warp ? 16 : (a.logits_out ? kLogits : 8);
                     float l = 0.f;
-                    if (lane < kLogits) {
-                        const float* src = inbox_dots + (par * kSlots + slot) * kCtas * kLogits + lane;
+                    if (lane < nl) {
+                        const float* src = inbox_dots + (par * kSlots + slot) * kCtas * kLogits + li;
 #pragma unroll
                         for (int s2 = 0; s2 < kCtas; ++s2) q[s2] = src[s2 * kLogits];
                         l = tree_sum16(q);
                         const float r = rsqrtf(sx * inv_k + a.rms_eps);
-                        l = (r * l) * ba[kLogits + (lane < 4 ? 0 : (lane < 8 ? 1 : 2))] + ba[lane];
-                        if (a.logits_out) a.logits_out[t * kLogits + lane] = l;
+                        l = (r * l) * ba[kLogits + (li < 4 ? 0 : (li < 8 ? 1 : 2))] + ba[li];
                     }
-                    // gates: lanes 0..3 pre, 4..7 post
-                    const float gate = lane < 4 ? __fdividef(1.0f, 1.0f + expf(-l)) : __fdividef(2.0f, 1.0f + expf(-l));
-                    if (lane < 4) a.pre_out[t * 4 + lane] = gate;
-                    else if (lane < 8) a.post_out[t * 4 + lane - 4] = gate;
-                    if (nondel) {   // this token's pre to every CTA, for their collapse
-                        const float q0 = __shfl_sync(0xffffffffu, gate, 0), q1 = __shfl_sync(0xffffffffu, gate, 1);
-                        const float q2 = __shfl_sync(0xffffffffu, gate, 2), q3 = __shfl_sync(0xffffffffu, gate, 3);
-                        if (lane < kCtas)
-                            st_async_v4(mapa(smem_u32(prex + (par * kMaxTile + tok) * 4), lane), q0, q1, q2, q3,
-                                        mapa(smem_u32(&pre_full[par]), lane));
-                    }
-                    // comb: lanes 8..23 hold the 4x4 logits row-major; row softmax
-                    // across each group of 4 lanes, plus eps
-                    float mx = fmaxf(l, __shfl_xor_sync(0xffffffffu, l, 1));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                    const float e = expf(l - mx);
-                    const float e01 = e + __shfl_xor_sync(0xffffffffu, e, 1);
-                    const float sum = e01 + __shfl_xor_sync(0xffffffffu, e01, 2);
-                    const float p = e * rcp_approx(sum) + a.sk_eps;
-                    float P[16];
+                    if (comb_warp) {
+                        float lc16[16];
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) P[k] = __shfl_sync(0xffffffffu, p, 8 + k);
-                    if (lane == 0) {
-                        sinkhorn_iterations(P, a.iters);
-                        float4* co = reinterpret_cast<float4*>(a.comb_out + t * 16);
+                        for (int k = 0; k < 16; ++k) lc16[k] = __shfl_sync(0xffffffffu, l, k);
+                        if (lane == 0) {
+                            float P[16];
+                            comb_softmax_eps(lc16, a.sk_eps, P);
+                            sinkhorn_iterations(P, a.iters);
+                            float4* co = reinterpret_cast<float4*>(a.comb_out + t * 16);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) co[i] = make_float4(P[4 * i], P[4 * i + 1], P[4 * i + 2], P[4 * i + 3]);
+                            for (int i = 0; i < 4; ++i)
+                                co[i] = make_float4(P[4 * i], P[4 * i + 1], P[4 * i + 2], P[4 * i + 3]);
+                        }
+                    } else {
+                        if (a.logits_out && lane < kLogits) a.logits_out[t * kLogits + lane] = l;
+                        // gates: lanes 0..3 pre, 4..7 post
+                        const float gate =
+                            lane < 4 ? __fdividef(1.0f, 1.0f + expf(-l)) : __fdividef(2.0f, 1.0f + expf(-l));
+                        if (lane < 4) a.pre_out[t * 4 + lane] = gate;
+                        else if (lane < 8) a.post_out[t * 4 + lane - 4] = gate;
+                        if (nondel) {   // this token's pre to every CTA, for their collapse
+                            const float q0 = __shfl_sync(0xffffffffu, gate, 0), q1 = __shfl_sync(0xffffffffu, gate, 1);
+                            const float q2 = __shfl_sync(0xffffffffu, gate, 2), q3 = __shfl_sync(0xffffffffu, gate, 3);
+                            if (lane < kCtas)
+                                st_async_v4(mapa(smem_u32(prex + (par * kMaxTile + tok) * 4), lane), q0, q1, q2, q3,
+                                            mapa(smem_u32(&pre_full[par]), lane));
+                        }
                     }
                 }
             }
