@@ -564,7 +564,9 @@ def run_ours(args, rank, world, local):
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 2 * args.steps,
+        # per step: the post, and the pre (from 256 tokens on the tensor-core
+        # path: fn's planes packed, then the kernel; one launch with --packed)
+        "gpu_launches": (1 + (2 if mhc.pre_plan(T)["kernel"] == 2 and not args.packed else 1)) * args.steps,
         "clocks": clk.summary(),
         "other_prefill": other_prefill,
         "decode_graph": decode,

@@ -86,7 +86,9 @@ typedef enum mhc_status {
  * Outputs must not overlap any input or the workspace (pre_out must not
  * alias pre_in: ping-pong two buffers across seams).  Errors:
  * MHC_ERR_INVALID_ARGUMENT (also: workspace too small or misaligned),
- * MHC_ERR_UNSUPPORTED, MHC_ERR_CUDA.  One kernel launch per call.
+ * MHC_ERR_UNSUPPORTED, MHC_ERR_CUDA.  One kernel launch per call below 256
+ * tokens; from 256 tokens two: fn split into its bf16 planes (one copy, in
+ * the workspace), then the tensor-core kernel.
  */
 mhc_status mhc_pre_delayed(const uint16_t *x, const float *pre_in, const float *fn,
                            const float *bias, const float *alpha,
@@ -100,10 +102,10 @@ mhc_status mhc_pre_delayed(const uint16_t *x, const float *pre_in, const float *
  * Workspace bytes mhc_pre_delayed needs for a shape on the current device
  * (host only).  0 when the shape runs on the CUDA-core kernel (fewer than 256
  * tokens, or a hidden size the tensor-core kernel does not take); otherwise
- * the per-call copy of the fn slices split into three bf16 planes, one copy
- * per co-resident 16-CTA cluster (about 20 MB at C = 5120 on a GB300), plus
- * T x 16 bytes (rounded to 256) that mhc_pre uses; the same size serves
- * mhc_pre_delayed, mhc_pre and mhc_post_pre_delayed.
+ * the per-call copy of fn split into three bf16 planes (2,949,120 bytes at
+ * C = 5120, shared by every cluster), plus T x 16 bytes (rounded to 256)
+ * that mhc_pre uses; the same size serves mhc_pre_delayed, mhc_pre and
+ * mhc_post_pre_delayed.
  * Returns 0 as well for shapes mhc_pre_delayed rejects.
  */
 size_t mhc_pre_workspace_bytes(int64_t T, int n, int C);
@@ -121,9 +123,9 @@ size_t mhc_pre_workspace_bytes(int64_t T, int n, int C);
  * workspace.  It always runs the tensor-core kernel, with its scratch in a
  * fixed device array of MHC_NOALLOC_SCRATCH_BYTES that the library holds on
  * every GPU that loads it, until the process exits; it never calls
- * cudaMalloc, cudaFree or any allocating routine.  The array fits at most two
- * 16-CTA clusters, so the kernel uses at most 32 SMs: correct for every T,
- * but slower than mhc_pre_delayed for large T.
+ * cudaMalloc, cudaFree or any allocating routine.  The array holds one copy
+ * of fn's planes, packed by a first launch; the tensor-core kernel then runs
+ * on the whole GPU as in mhc_pre_delayed (two launches per call).
  *  C            multiple of 256, 256 <= C <= 5120 (else MHC_ERR_UNSUPPORTED)
  * First call on a device: resolves the array's device address and sets the
  * kernel up for that device (no allocation); make that first call outside any
@@ -136,7 +138,7 @@ size_t mhc_pre_workspace_bytes(int64_t T, int n, int C);
  * stream of it: otherwise MHC_ERR_INVALID_ARGUMENT, returned before anything
  * is set up or launched.  Other errors as mhc_pre_delayed.
  */
-#define MHC_NOALLOC_SCRATCH_BYTES 5898240u
+#define MHC_NOALLOC_SCRATCH_BYTES 2949120u
 mhc_status mhc_pre_delayed_noalloc(const uint16_t *x, const float *pre_in, const float *fn,
                                    const float *bias, const float *alpha,
                                    const uint16_t *norm_weight, int64_t T, int n, int C,
@@ -173,10 +175,10 @@ mhc_status mhc_post(const uint16_t *x, const uint16_t *y, const float *comb,
  * other arguments as mhc_pre_delayed.  Below 256 tokens (and for hidden sizes
  * the tensor-core kernel does not take) one kernel, where the finalising CTA
  * sends each token's pre to the cluster before the collapse; from 256 tokens
- * two launches: the tensor-core kernel for the gates only, then a streaming
- * collapse and fold with the pre it wrote, in the tensor-core kernel's order
- * of summation (mhc_pre_workspace_bytes covers both: the planes plus T * 16
- * bytes of scratch).
+ * three launches: fn's planes, the tensor-core kernel for the gates only,
+ * then a streaming collapse and fold with the pre it wrote, in the
+ * tensor-core kernel's order of summation (mhc_pre_workspace_bytes covers
+ * both: the planes plus T * 16 bytes of scratch).
  */
 mhc_status mhc_pre(const uint16_t *x, const float *fn, const float *bias, const float *alpha,
                    const uint16_t *norm_weight, int64_t T, int n, int C, int sinkhorn_iters,
@@ -199,9 +201,9 @@ mhc_status mhc_pre(const uint16_t *x, const float *fn, const float *bias, const 
  * same arguments.  Below 256 tokens (and for hidden sizes the tensor-core
  * kernel does not take) this is ONE kernel: each CTA forms x_new for its
  * column slice of the tile, writes it out and runs the pre block on it from
- * shared memory (x is read once).  From 256 tokens on it is two launches,
- * the post kernel then the tensor-core pre kernel; the workspace is then
- * needed as for mhc_pre_delayed (mhc_pre_workspace_bytes).
+ * shared memory (x is read once).  From 256 tokens on it is three launches:
+ * the post kernel, fn's planes, then the tensor-core pre kernel; the
+ * workspace is then needed as for mhc_pre_delayed (mhc_pre_workspace_bytes).
  * Aliasing: x_new may be exactly x; comb_out may be exactly comb and
  * post_out exactly post (one gate buffer carried along a chain); pre_out
  * must not overlap pre_in; nothing else may overlap.

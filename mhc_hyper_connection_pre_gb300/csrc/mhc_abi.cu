@@ -25,7 +25,6 @@ int pre_cluster_prepare(int C);
 bool pre_tc_supports(int C);
 int pre_tc_tile_tokens();
 int pre_tc_prepare();
-size_t pre_tc_workspace_bytes(int64_t T, int C, int max_clusters);
 cudaError_t launch_pre_tc(const uint16_t* x, const float* pre_in, const float* fn, const float* bias,
                           const float* alpha, const uint16_t* norm_w, int64_t T, int C, int iters,
                           float rms_eps, float norm_eps, float sk_eps, float* pre_out, float* post_out,
@@ -184,8 +183,8 @@ size_t mhc_pre_workspace_bytes(int64_t T, int n, int C) {
     int dev = current_device();
     if (dev < 0) return 0;
     int tcc = tc_clusters(dev);
-    // fn planes, then (mhc_pre only) the first pass's pre-mix
-    return tcc > 0 ? mhc::pre_tc_workspace_bytes(T, C, tcc) + nondelayed_scratch_bytes(T) : 0;
+    // one copy of fn's planes, then (mhc_pre only) the first pass's pre-mix
+    return tcc > 0 ? mhc::pre_tc_packed_bytes(C) + nondelayed_scratch_bytes(T) : 0;
 }
 
 }  // extern "C"
@@ -253,10 +252,18 @@ mhc_status pre_entry(const uint16_t* x, const float* pre_in, const float* fn, co
     if (use_tc(T, C)) {
         int tcc = tc_clusters(dev);
         if (tcc > 0) {
-            const size_t planes = packed ? 0 : mhc::pre_tc_workspace_bytes(T, C, tcc);
+            // fn's planes: packed by the caller, or packed here into the
+            // workspace by one launch over the whole GPU ahead of the kernel
+            // (one shared copy instead of a conversion in every cluster's
+            // prologue before its first MMA)
+            const size_t planes = packed ? 0 : mhc::pre_tc_packed_bytes(C);
             const size_t need = planes + (nondelayed ? nondelayed_scratch_bytes(T) : 0);
             if (workspace_bytes < need || (need && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))))
                 return MHC_ERR_INVALID_ARGUMENT;
+            if (!packed) {
+                if (mhc::launch_pre_tc_pack(fn, C, workspace, s) != cudaSuccess) return MHC_ERR_CUDA;
+                packed = workspace;
+            }
             if (nondelayed) {
                 // pass 1: the gates only (no collapse, fold or layer_input),
                 // its unused pre_in pointed at the workspace scratch; pass 2:
@@ -267,7 +274,7 @@ mhc_status pre_entry(const uint16_t* x, const float* pre_in, const float* fn, co
                 cudaError_t e = mhc::launch_pre_tc(x, scratch, fn, bias, alpha, norm_weight, T, C, sinkhorn_iters,
                                                    rms_eps, norm_eps, sinkhorn_eps, pre_out, post_out, comb_out,
                                                    layer_input, logits_out, workspace, s, tcc, bcast, true,
-                                                   nullptr);
+                                                   packed);
                 if (e == cudaSuccess) {
                     const int64_t ntiles = (T + 127) / 128;
                     const int ncl = ntiles < tcc ? (int)ntiles : tcc;

@@ -12,11 +12,10 @@
 // that lives in this file; it never calls cudaMalloc, cudaFree or any
 // allocating routine.
 //
-// Limit: the array holds the fn planes for at most kNoAllocClusters 16-CTA
-// clusters (2 x 16 x 10 x 18 KB = 5,898,240 bytes for C = 5120), so the kernel
-// runs on at most 32 SMs here: correct for any token count, slower for large
-// ones than mhc_pre_delayed on the whole GPU.  Every GPU that loads the
-// library holds the array until the process exits.
+// The array holds one copy of the fn planes (16 x 10 x 18 KB = 2,949,120
+// bytes at C = 5120), packed by one launch over the whole GPU; the kernel
+// then runs on every co-resident cluster, as mhc_pre_delayed does.  Every GPU
+// that loads the library holds the array until the process exits.
 #include "../../include/mhc.h"
 
 #include <cuda_runtime.h>
@@ -26,7 +25,8 @@
 namespace mhc {
 bool pre_tc_supports(int C);
 int pre_tc_prepare();
-size_t pre_tc_workspace_bytes(int64_t T, int C, int max_clusters);
+size_t pre_tc_packed_bytes(int C);
+cudaError_t launch_pre_tc_pack(const float* fn, int C, void* out, cudaStream_t stream);
 cudaError_t launch_pre_tc(const uint16_t* x, const float* pre_in, const float* fn, const float* bias,
                           const float* alpha, const uint16_t* norm_w, int64_t T, int C, int iters,
                           float rms_eps, float norm_eps, float sk_eps, float* pre_out, float* post_out,
@@ -37,13 +37,11 @@ cudaError_t launch_pre_tc(const uint16_t* x, const float* pre_in, const float* f
 
 namespace {
 
-constexpr int kNoAllocClusters = 2;
 constexpr size_t kNoAllocBytes = MHC_NOALLOC_SCRATCH_BYTES;
 // Every shape the entry point accepts fits: C is at most 5120 (the
 // tensor-core kernel's limit, checked first), i.e. at most 10 stages of
-// 18 KB of planes per CTA, for at most kNoAllocClusters clusters of 16 CTAs.
-static_assert((size_t)kNoAllocClusters * 16 * 10 * 18432 <= kNoAllocBytes,
-              "the scratch array holds the planes of every accepted shape");
+// 18 KB of planes for each of the 16 CTA ranks.
+static_assert((size_t)16 * 10 * 18432 <= kNoAllocBytes, "the scratch array holds the planes of every accepted shape");
 
 // The scratch itself.  Its name is a host-side stand-in in host code, not a
 // device address: host code uses the address cudaGetSymbolAddress returns.
@@ -63,7 +61,7 @@ bool setup(int dev, void** scratch, int* clusters) {
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return false;
         const int n = mhc::pre_tc_prepare();
         if (n <= 0) return false;
-        g_clusters[dev] = n < kNoAllocClusters ? n : kNoAllocClusters;
+        g_clusters[dev] = n;
         g_scratch_ptr[dev] = p;
     }
     *scratch = g_scratch_ptr[dev];
@@ -111,9 +109,9 @@ extern "C" mhc_status mhc_pre_delayed_noalloc(const uint16_t* x, const float* pr
         for (const R& o2 : outs)
             if (&o != &o2 && overlaps(o.p, o.n, o2.p, o2.n)) return MHC_ERR_INVALID_ARGUMENT;
     }
-    // the planes of at most kNoAllocClusters clusters fit the array (host
-    // arithmetic only: nothing has been set up or launched yet)
-    if (mhc::pre_tc_workspace_bytes(T, C, kNoAllocClusters) > kNoAllocBytes) return MHC_ERR_UNSUPPORTED;
+    // one copy of the planes fits the array (host arithmetic only: nothing
+    // has been set up or launched yet)
+    if (mhc::pre_tc_packed_bytes(C) > kNoAllocBytes) return MHC_ERR_UNSUPPORTED;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MHC_ERR_CUDA;
     // The scratch address below belongs to the current device: x and the
@@ -137,9 +135,11 @@ extern "C" mhc_status mhc_pre_delayed_noalloc(const uint16_t* x, const float* pr
     void* scratch = nullptr;
     int clusters = 0;
     if (!setup(dev, &scratch, &clusters)) return MHC_ERR_CUDA;
-    cudaError_t e = mhc::launch_pre_tc(x, pre_in, fn, bias, alpha, norm_weight, T, C, sinkhorn_iters, rms_eps,
-                                       norm_eps, sinkhorn_eps, pre_out, post_out, comb_out, layer_input,
-                                       logits_out, scratch, static_cast<cudaStream_t>(stream), clusters, false,
-                                       false, nullptr);
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = mhc::launch_pre_tc_pack(fn, C, scratch, s);
+    if (e == cudaSuccess)
+        e = mhc::launch_pre_tc(x, pre_in, fn, bias, alpha, norm_weight, T, C, sinkhorn_iters, rms_eps, norm_eps,
+                               sinkhorn_eps, pre_out, post_out, comb_out, layer_input, logits_out, nullptr, s,
+                               clusters, false, false, scratch);
     return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA;
 }

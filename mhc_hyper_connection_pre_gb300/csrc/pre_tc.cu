@@ -783,11 +783,14 @@ pre_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ 
     cluster_sync_all();  // no CTA leaves while a peer may still write into its shared memory
 }
 
-// Planes packed ahead of the calls: CTA r writes rank r's region (the same
-// bytes the kernel's prologue writes into each cluster's region).
-__global__ void __launch_bounds__(kThreads, 1) pre_tc_pack_kernel(const float* fn, int C, unsigned char* out) {
-    const int slice = C / kCtas, ngroups = (slice + kCols - 1) / kCols, r = blockIdx.x;
-    write_planes(fn, C, r * slice, slice, ngroups, out + (size_t)r * ngroups * kWStage, threadIdx.x >> 5,
+// Planes packed ahead of the kernel: rank r's region holds the bytes the
+// kernel's prologue would write into each cluster's region.  One stage of
+// one rank per CTA (grid ngroups x 16), so the whole GPU converts fn at once
+// (write_planes on a one-stage slice writes that stage's bytes).
+__global__ void __launch_bounds__(kThreads, 1) pre_tc_pack_stage_kernel(const float* fn, int C, unsigned char* out) {
+    const int slice = C / kCtas, ngroups = (slice + kCols - 1) / kCols, g = blockIdx.x, r = blockIdx.y;
+    const int sl = slice - kCols * g < kCols ? slice - kCols * g : kCols;
+    write_planes(fn, C, r * slice + kCols * g, sl, 1, out + ((size_t)r * ngroups + g) * kWStage, threadIdx.x >> 5,
                  threadIdx.x & 31);
 }
 
@@ -818,14 +821,9 @@ static PFN_encodeTiled encode_fn() {
 size_t pre_tc_packed_bytes(int C) { return (size_t)tc::kCtas * (size_t)tc::stages_of(C) * tc::kWStage; }
 
 cudaError_t launch_pre_tc_pack(const float* fn, int C, void* out, cudaStream_t stream) {
-    tc::pre_tc_pack_kernel<<<tc::kCtas, tc::kThreads, 0, stream>>>(fn, C, static_cast<unsigned char*>(out));
+    tc::pre_tc_pack_stage_kernel<<<dim3((unsigned)tc::stages_of(C), tc::kCtas), tc::kThreads, 0, stream>>>(
+        fn, C, static_cast<unsigned char*>(out));
     return cudaGetLastError();
-}
-
-size_t pre_tc_workspace_bytes(int64_t T, int C, int max_clusters) {
-    const int64_t tiles = (T + tc::kTile - 1) / tc::kTile;
-    const int64_t ncl = tiles < max_clusters ? tiles : max_clusters;
-    return (size_t)ncl * tc::kCtas * (size_t)tc::stages_of(C) * tc::kWStage;
 }
 
 bool pre_tc_supports(int C) {

@@ -290,10 +290,10 @@ def test_fused_seam_against_the_oracle(T):
     _check_pre({k: v.cpu() for k, v in got.items() if k != "x_new"}, o, xb2, d2, fold=True)
 
 
-@pytest.mark.parametrize("T,nodes", [(4, 1), (300, 2)])
+@pytest.mark.parametrize("T,nodes", [(4, 1), (300, 3)])
 def test_fused_seam_is_one_launch_in_a_graph(T, nodes):
     """One kernel node below 256 tokens (the cluster kernel); from 256
-    tokens the post kernel and the tensor-core pre."""
+    tokens the post kernel, the fn-plane packing and the tensor-core pre."""
     d, gd, comb, post = _fused_case(T, 5120, True, seed=1600)
     out = {"pre": torch.empty(T, 4, device="cuda"), "post": torch.empty(T, 4, device="cuda"),
            "comb": torch.empty(T, 4, 4, device="cuda"),
