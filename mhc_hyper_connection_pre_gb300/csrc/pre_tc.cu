@@ -20,12 +20,16 @@
 // M); CTA r owns C/16 columns of all four streams and walks its slice in
 // stages of 32 columns x 4 streams x 128 tokens (32 KB: one 3-D TMA box --
 // x described as (column, token, stream) -- of 64-byte rows, 64-byte
-// swizzle, one instruction per stage).  At the start of the call each CTA
-// writes its K-slice of the three fn planes (184 KB at C = 5120), already in
-// the MMA's operand layout, to its region of the caller's workspace; every
-// stage then brings the matching 18 KB block with one bulk copy (L2
-// evict-last) next to the x box (default L2 policy; evict-first was 1.6 us
-// slower).  A 4-slot ring of 50 KB
+// swizzle, one instruction per stage).  The three fn planes (184 KB per CTA
+// rank at C = 5120), in the MMA's operand layout, come packed ahead of the
+// kernel by pre_tc_pack_stage_kernel (one copy of 16 rank regions that every
+// cluster reads; the library packs them per call into the workspace, or the
+// caller once with mhc_pre_pack).  The kernel can still write its own
+// cluster's copy in its prologue when Args::packed is null, a path the
+// library no longer takes (removing it changed code generation and made the
+// kernel 1.4 us slower).  Every stage brings the matching 18 KB block with
+// one bulk copy (L2 evict-last) next to the x box (default L2 policy;
+// evict-first was 1.6 us slower).  A 4-slot ring of 50 KB
 // slots keeps 200 KB in flight per SM.  Warp roles (16 warps):
 //   warp 0       TMA producer;
 //   warp 1       MMA issuer: per stage 8 x tcgen05.mma (M128 N80 K16: two K
