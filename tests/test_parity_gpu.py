@@ -130,6 +130,29 @@ def test_kernel_choice():
     assert p["cluster"] == 16 and p["tokens_per_tile"] == 128 and p["grid"] % 16 == 0
 
 
+def test_tensor_core_workspace_is_one_plane_copy():
+    """From 256 tokens mhc_pre_delayed first packs fn's planes into the
+    workspace (one copy that every cluster reads): the workspace it asks for
+    is that copy plus mhc_pre's T x 16-byte scratch; a workspace of just the
+    copy gives the same bits as the default one, and one 256-byte step less
+    is rejected before anything launches."""
+    lib = mhc.load_library()
+    T, C = 300, 5120
+    packed = int(lib.mhc_pre_packed_bytes(4, C))
+    assert int(lib.mhc_pre_workspace_bytes(T, 4, C)) == packed + (T * 16 + 255) // 256 * 256
+    gd = _to_dev(seam_inputs(T, seed=1700, fold=True))
+    ref = mhc.pre_delayed(gd["x"], gd["pre_in"], gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"])
+    ws = torch.empty(packed, dtype=torch.uint8, device="cuda")
+    got = mhc.pre_delayed(gd["x"], gd["pre_in"], gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"], workspace=ws)
+    torch.cuda.synchronize()
+    for k in ref:
+        assert torch.equal(got[k], ref[k]), k
+    with pytest.raises(mhc.MhcError):
+        mhc.pre_delayed(gd["x"], gd["pre_in"], gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"],
+                        workspace=ws[: packed - 256])
+    assert mhc.device_status() == 0
+
+
 def test_alpha_and_sinkhorn_parameters():
     """Non-unit alphas, another iteration count and eps reach the kernel."""
     d = seam_inputs(24, seed=5, fold=True)
