@@ -18,13 +18,14 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int64_t kChunkTokens = 1024;  // a multiple of the tensor-core kernel's 128-token tile
 constexpr int64_t kTcMinTokens = 256;   // the pre block's tensor-core threshold
+constexpr int kSets = 2;                // device buffer sets in rotation (three measured the same)
 
 // Internal streams and events, created once per device on first use and
 // kept for the life of the process.
 struct Pipe {
     bool ready = false;
     cudaStream_t in = nullptr, out = nullptr;
-    cudaEvent_t start, in_done[2], comp_done[2], out_done[2], end_in, end_out;
+    cudaEvent_t start, in_done[kSets], comp_done[kSets], out_done[kSets], end_in, end_out;
 };
 std::mutex g_pipe_mutex;
 Pipe g_pipe[kMaxDevices];
@@ -37,7 +38,7 @@ bool make_pipe(Pipe& p) {
               cudaEventCreateWithFlags(&p.start, ef) == cudaSuccess &&
               cudaEventCreateWithFlags(&p.end_in, ef) == cudaSuccess &&
               cudaEventCreateWithFlags(&p.end_out, ef) == cudaSuccess;
-    for (int b = 0; ok && b < 2; ++b)
+    for (int b = 0; ok && b < kSets; ++b)
         ok = cudaEventCreateWithFlags(&p.in_done[b], ef) == cudaSuccess &&
              cudaEventCreateWithFlags(&p.comp_done[b], ef) == cudaSuccess &&
              cudaEventCreateWithFlags(&p.out_done[b], ef) == cudaSuccess;
@@ -45,19 +46,48 @@ bool make_pipe(Pipe& p) {
     return ok;
 }
 
-// Tokens per chunk: one chunk below 512 tokens (so that a call under 256
-// tokens stays on the cluster kernel and one from 256 on the tensor-core
-// kernel); otherwise chunks of 1024 tokens (below 2048 tokens: half of T
-// rounded down to the tile), the remainder joining the last chunk, so that
-// no chunk falls under 256 tokens.
-int64_t chunk_tokens(int64_t T) {
-    if (T < 2 * kTcMinTokens) return T > 0 ? T : 1;
-    if (T >= 2 * kChunkTokens) return kChunkTokens;
-    return (T / 2) / 128 * 128;
+// The chunks of a call over T tokens.  No chunk falls under 256 tokens
+// (unless T does), so a call under 256 tokens stays on the cluster kernel
+// and every chunk of a larger one takes the tensor-core kernel:
+//  * below 512 tokens, one chunk;
+//  * below 2048, two: half of T rounded down to the tile, then the rest;
+//  * from 2048, a 256-token head (the first copies in wait for no kernel,
+//    so a short head starts the pipeline sooner), 1024-token chunks, then
+//    512 tokens plus what does not fill a 1024-token chunk, then a 256-token
+//    tail (the last copies out follow the last kernels, so a short tail ends
+//    it sooner).
+struct Chunk {
+    int64_t t0, n;
+};
+int64_t num_chunks(int64_t T) {
+    if (T <= 0) return 0;
+    if (T < 2 * kTcMinTokens) return 1;
+    if (T < 2 * kChunkTokens) return 2;
+    return (T - kChunkTokens) / kChunkTokens + 3;
 }
-int64_t num_chunks(int64_t T) { return T <= 0 ? 0 : (T / chunk_tokens(T) > 0 ? T / chunk_tokens(T) : 1); }
-// the largest chunk: the last, which also takes the remainder
-int64_t max_chunk(int64_t T) { return T <= 0 ? 0 : T - (num_chunks(T) - 1) * chunk_tokens(T); }
+Chunk chunk_of(int64_t T, int64_t k) {
+    const int64_t nch = num_chunks(T);
+    if (nch == 1) return {0, T};
+    if (nch == 2) {
+        const int64_t c = (T / 2) / 128 * 128;
+        return k == 0 ? Chunk{0, c} : Chunk{c, T - c};
+    }
+    const int64_t body = nch - 3;   // 1024-token chunks
+    if (k == 0) return {0, kTcMinTokens};
+    if (k <= body) return {kTcMinTokens + (k - 1) * kChunkTokens, kChunkTokens};
+    if (k == body + 1) {
+        const int64_t t0 = kTcMinTokens + body * kChunkTokens;
+        return {t0, T - kTcMinTokens - t0};
+    }
+    return {T - kTcMinTokens, kTcMinTokens};
+}
+// the largest chunk (the buffers of both sets are sized for it)
+int64_t max_chunk(int64_t T) {
+    const int64_t nch = num_chunks(T);
+    if (nch <= 2) return nch == 0 ? 0 : chunk_of(T, nch - 1).n;
+    const int64_t before_tail = chunk_of(T, nch - 2).n;   // 512 .. 1535 tokens
+    return before_tail > kChunkTokens ? before_tail : kChunkTokens;
+}
 
 size_t up256(size_t b) { return (b + 255) / 256 * 256; }
 
@@ -102,7 +132,7 @@ extern "C" {
 size_t mhc_seam_host_workspace_bytes(int64_t T, int n, int C) {
     if (T <= 0 || n != 4 || C < 8 || C % 8 != 0) return 0;
     const int64_t cap = max_chunk(T);
-    return up256(mhc_pre_workspace_bytes(cap, n, C)) + 2 * set_layout(cap, n, C).total;
+    return up256(mhc_pre_workspace_bytes(cap, n, C)) + kSets * set_layout(cap, n, C).total;
 }
 
 mhc_status mhc_seam_host(const uint16_t* x_h, const uint16_t* y_h, const float* pre_in_h, const float* fn,
@@ -142,11 +172,12 @@ mhc_status mhc_seam_host(const uint16_t* x_h, const uint16_t* y_h, const float* 
     Pipe& p = g_pipe[dev];
     if (!make_pipe(p)) return MHC_ERR_CUDA;
 
-    const int64_t ck = chunk_tokens(T), nch = num_chunks(T), cap = max_chunk(T);
+    const int64_t nch = num_chunks(T), cap = max_chunk(T);
     const SetLayout L = set_layout(cap, n, C);
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     const size_t tc_bytes = up256(mhc_pre_workspace_bytes(cap, n, C));
-    unsigned char* sets[2] = {ws + tc_bytes, ws + tc_bytes + L.total};
+    unsigned char* sets[kSets];
+    for (int b = 0; b < kSets; ++b) sets[b] = ws + tc_bytes + b * L.total;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     mhc_status st = MHC_OK;
@@ -159,8 +190,9 @@ mhc_status mhc_seam_host(const uint16_t* x_h, const uint16_t* y_h, const float* 
     cu(cudaStreamWaitEvent(p.in, p.start, 0));
     cu(cudaStreamWaitEvent(p.out, p.start, 0));
     for (int64_t k = 0; k < nch && st == MHC_OK; ++k) {
-        const int b = (int)(k & 1);
-        const int64_t t0 = k * ck, nk = (k == nch - 1) ? T - t0 : ck;
+        const int b = (int)(k % kSets);
+        const Chunk ch = chunk_of(T, k);
+        const int64_t t0 = ch.t0, nk = ch.n;
         unsigned char* S = sets[b];
         uint16_t* dx = reinterpret_cast<uint16_t*>(S + L.x);
         uint16_t* dy = reinterpret_cast<uint16_t*>(S + L.y);
@@ -170,16 +202,16 @@ mhc_status mhc_seam_host(const uint16_t* x_h, const uint16_t* y_h, const float* 
         float* dpost = reinterpret_cast<float*>(S + L.post);
         float* dcomb = reinterpret_cast<float*>(S + L.comb);
         uint16_t* dli = reinterpret_cast<uint16_t*>(S + L.li);
-        // in: set b's inputs are free once chunk k-2's kernels are done
-        if (k >= 2) cu(cudaStreamWaitEvent(p.in, p.comp_done[b], 0));
+        // in: set b's inputs are free once chunk k-kSets's kernels are done
+        if (k >= kSets) cu(cudaStreamWaitEvent(p.in, p.comp_done[b], 0));
         cu(cudaMemcpyAsync(dx, x_h + t0 * n * C, (size_t)nk * n * C * 2, cudaMemcpyHostToDevice, p.in));
         cu(cudaMemcpyAsync(dy, y_h + t0 * C, (size_t)nk * C * 2, cudaMemcpyHostToDevice, p.in));
         cu(cudaMemcpyAsync(dpi, pre_in_h + t0 * n, (size_t)nk * n * 4, cudaMemcpyHostToDevice, p.in));
         cu(cudaEventRecord(p.in_done[b], p.in));
         // kernels on the caller's stream: set b's outputs are free once chunk
-        // k-2's results have left
+        // k-kSets's results have left
         cu(cudaStreamWaitEvent(s, p.in_done[b], 0));
-        if (k >= 2) cu(cudaStreamWaitEvent(s, p.out_done[b], 0));
+        if (k >= kSets) cu(cudaStreamWaitEvent(s, p.out_done[b], 0));
         if (st != MHC_OK) break;
         mhc_status r = mhc_pre_delayed(dx, dpi, fn, bias, alpha, norm_weight, nk, n, C, sinkhorn_iters, rms_eps,
                                        norm_eps, sinkhorn_eps, dpre, dpost, dcomb, dli, nullptr, ws, tc_bytes, s);
