@@ -642,13 +642,16 @@ def _stub_chain(b, params, deltas, y, stream, fused):
         mhc.post(b["x"], y, outs[-1]["comb"], outs[-1]["post"], out=b["x"], stream=stream)
 
 
-@pytest.mark.parametrize("T,fused", [(4, False), (4, True), (100, False), (100, True)])
+@pytest.mark.parametrize("T,fused", [(4, False), (4, True), (100, False), (100, True), (300, False), (300, True)])
 def test_early_launch_after_a_torch_kernel_is_bit_identical(T, fused):
     """A graph whose programmatic edges leave the upstream kernel's
     launch-completion port (SeamGraph early_launch), with a PyTorch kernel
     between pre and post, gives the bits of the same chain run eagerly with
-    launch overlap off.  Every programmatic edge is moved: one into each
-    seam kernel that follows another kernel."""
+    launch overlap off.  Every programmatic edge is moved: below 256 tokens
+    one into each seam kernel that follows another kernel; from 256 tokens
+    (the pre is the plane pack and the tensor-core kernel, launched without
+    programmatic serialization) one into each post, while the edges into the
+    pack launches stay as captured."""
     seams, C, dev = 8, 5120, "cuda"
     params = [chain_seam_params(si, device=dev) for si in range(seams)]
     deltas = [chain_stub_delta(si, T=T, device=dev) for si in range(seams)]
@@ -671,8 +674,12 @@ def test_early_launch_after_a_torch_kernel_is_bit_identical(T, fused):
         ref = _chain_result(b) + [y.clone()]
         mhc.set_launch_overlap(True)
         g = SeamGraph(lambda st: _stub_chain(b, params, deltas, y, st, fused), s, early_launch=True)
-        assert g.kernel_nodes == (2 * seams + 1 if fused else 3 * seams), g.kernel_nodes
-        assert g.moved_edges == (seams if fused else 2 * seams - 1), g.moved_edges
+        if T >= 256:
+            assert g.kernel_nodes == 4 * seams, g.kernel_nodes
+            assert g.moved_edges == seams, g.moved_edges
+        else:
+            assert g.kernel_nodes == (2 * seams + 1 if fused else 3 * seams), g.kernel_nodes
+            assert g.moved_edges == (seams if fused else 2 * seams - 1), g.moved_edges
         ports = edge_ports(g.graph)
         assert ports.get((1, 1), 0) == 0 and ports.get((2, 1), 0) == g.moved_edges, ports
         for _ in range(3):
