@@ -518,6 +518,12 @@ def run_ours(args, rank, world, local):
                  "us_per_step_fused_overlap": chain_us[(True, True, False)],
                  "us_per_step_overlap_early": chain_us[(False, True, True)],
                  "us_per_step_fused_overlap_early": chain_us[(True, True, True)],
+                 "us_per_step_best": min(chain_us.values()),
+                 "best_config": {(False, False, False): "2 launches/seam", (False, True, False): "2 launches/seam, overlap",
+                                 (True, False, False): "fused", (True, True, False): "fused, overlap",
+                                 (False, True, True): "2 launches/seam, overlap, early launch",
+                                 (True, True, True): "fused, overlap, early launch"}[
+                     min(chain_us, key=chain_us.get)],
                  "seams": CHAIN_SEAMS, "T": CHAIN_T, "kernel_nodes": nodes,
                  "launches_per_seam": (nodes - CHAIN_SEAMS) / CHAIN_SEAMS,
                  "launches_per_seam_fused": (fused_nodes - CHAIN_SEAMS) / CHAIN_SEAMS,
