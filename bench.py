@@ -558,12 +558,7 @@ def run_ours(args, rank, world, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16/fp32",
         "data": "synthetic (seeded N(0,1) streams, N(0,0.02^2) fn; no checkpoint)",
-        "config": {"workload": f"prefill seam: {pre_name} (fold) + mhc_post, T={T}, n=4, C=5120, "
-                               "20 Sinkhorn iters", "T": T, "n": N_STREAMS, "C": HIDDEN,
-                   "sinkhorn_iters": ITERS, "fold": True, "per_rank_tokens": T,
-                   "fn": "bf16 planes packed once ahead (mhc_pre_pack)" if args.packed else "fp32, converted per call",
-                   "l2": f"inputs larger than L2 (x {T * 40960 / 1e6:.0f} MB vs 129 MB), no flush",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(T, world, pre_name, args.packed),
         "seam_hbm_frac": round(seam_frac, 4),
         "kernels": {k: {kk: round(vv, 3) if isinstance(vv, float) else vv for kk, vv in v.items()}
                     for k, v in kernels.items()},
@@ -591,6 +586,16 @@ def run_ours(args, rank, world, local):
 
 
 # ------------------------------------------------------ reference arm ---
+
+def workload_config(T: int, world: int, pre_name: str = "mhc_pre_delayed", packed: bool = False) -> dict:
+    """The workload both arms time, described the same way (the driver
+    compares the two lines' config)."""
+    return {"workload": f"prefill seam: {pre_name} (fold) + mhc_post, T={T}, n=4, C=5120, 20 Sinkhorn iters",
+            "T": T, "n": N_STREAMS, "C": HIDDEN, "sinkhorn_iters": ITERS, "fold": True, "per_rank_tokens": T,
+            "fn": "bf16 planes packed once ahead (mhc_pre_pack)" if packed else "fp32 weights given to every call",
+            "l2": f"inputs larger than L2 (x {T * 40960 / 1e6:.0f} MB vs 129 MB), no flush",
+            "parallelism": f"replicas x{world}"}
+
 
 def run_reference(args, rank, world, local):
     if rank != 0:
@@ -620,9 +625,7 @@ def run_reference(args, rank, world, local):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"prefill seam: mhc_pre_delayed (fold) + mhc_post, T={T}, n=4, C=5120, "
-                               "20 Sinkhorn iters", "T": T, "n": N_STREAMS, "C": HIDDEN,
-                   "sinkhorn_iters": ITERS, "fold": True},
+        "config": workload_config(T, world),
         "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
