@@ -940,13 +940,14 @@ def _pinned(t):
     return t.cpu().pin_memory()
 
 
-@pytest.mark.parametrize("T", [1, 100, 300, 1000, 4097, 16384])
+@pytest.mark.parametrize("T", [1, 100, 300, 1000, 2048, 3000, 4097, 16384])
 def test_seam_host_is_bit_identical_to_the_device_calls(T):
     """mhc_seam_host on pinned host activations (chunked, copies and kernels
     on three streams) gives the bits of mhc_pre_delayed + mhc_post on device
-    copies: one chunk below 512 tokens, two chunks (384 + 616) at 1000,
-    1024-token chunks with the remainder joined to the last at 4097 and
-    16384."""
+    copies: one chunk below 512 tokens, two chunks (384 + 616) at 1000; from
+    2048 a 256-token head, 1024-token chunks, 512 tokens plus the remainder
+    and a 256-token tail (2048: 256 + 1024 + 512 + 256; 3000: a 1464-token
+    chunk, the largest, which sizes the buffers; 4097: a 513-token chunk)."""
     gd = seam_inputs(T, seed=2300 + T, fold=True, with_y=True, device="cuda")
     ref = mhc.pre_delayed(gd["x"], gd["pre_in"], gd["fn"], gd["bias"], gd["alpha"], gd["norm_w"])
     xn_ref = mhc.post(gd["x"], gd["y"], ref["comb"], ref["post"])
